@@ -1,0 +1,530 @@
+"""Benchmark: paged decode attention over a PagedAttention KV cache on GB300.
+
+One step = one decode step of one layer: append the new token's k/v of every
+sequence into its pool slot, then paged decode attention over all cached
+tokens (the split-KV attention kernel and the log-sum-exp merge).  Inputs are
+seeded synthetic tensors resident in HBM; the KV pool of the headline workload
+(537 MB) is far larger than L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun: every rank runs the same workload on its own GPU
+(data-parallel decode has no exchange between sequences), the time is the max
+over ranks and `value` is the sum of all ranks' KV bytes over that time.
+`--impl reference` times the fp64 CPU oracle on the host cores instead.
+Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np
+import torch
+
+from paged_kv_cache_215_gb300 import workloads as wl
+
+METRIC = "paged decode attn KV GB/s (fraction of HBM peak); decode tokens/s at 128K"
+UNIT = "GB/s"
+PRIMARY = "long_128k"
+SECONDARY = ["llama8b_b32_8k", "long_1m", "fp8_b8_32k", "llama70b_prefix_bs16",
+             "llama70b_prefix_bs32"]
+MODEL_LAYERS = {"long_128k": 32, "long_1m": 32, "llama8b_b32_8k": 32, "fp8_b8_32k": 32,
+                "llama70b_prefix_bs16": 80, "llama70b_prefix_bs32": 80}
+KERNEL_SOURCES = ["paged_kv_cache_215_gb300/csrc/decode_mma.cu",
+                  "paged_kv_cache_215_gb300/csrc/device.cuh"]
+
+
+# ---------------------------------------------------------------------------- helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """dram bytes per launch of the attention kernel from the committed ncu summary,
+    if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"decode_mma_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m_hash = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", txt)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not m_hash or not m_tr or m_hash.group(1) != kernel_hash():
+        return None
+    return float(m_tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.2)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [l.split(", ") for l in self.lines if l and l[0].isdigit()]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if len(r) > 5 + i and r[5 + i].strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def kv_bytes(case):
+    return int(case.seq_lens.astype(np.int64).sum()) * 2 * case.num_kv_heads * case.head_dim * \
+        case.kv_elem_bytes()
+
+
+def algorithmic_attn_bytes(case):
+    """What one attention launch must move: every cached K/V element once, q in,
+    out, and the table entries it follows."""
+    q = case.batch * case.num_q_heads * case.head_dim * 2
+    out = case.batch * case.num_q_heads * case.head_dim * 2
+    tables = sum((int(n) + case.block_size - 1) // case.block_size for n in case.seq_lens) * 4
+    return kv_bytes(case) + q + out + tables
+
+
+def unique_kv_bytes(case):
+    if not case.shared_prefix_tokens:
+        return kv_bytes(case)
+    bs = case.block_size
+    per_tok = 2 * case.num_kv_heads * case.head_dim * case.kv_elem_bytes()
+    shared = [min(int(n), case.shared_prefix_tokens) // bs * bs for n in case.seq_lens]
+    dup = sum(shared) - max(shared)
+    return kv_bytes(case) - dup * per_tok
+
+
+# ---------------------------------------------------------------------------- our arm
+class Workload:
+    def __init__(self, name, device):
+        from paged_kv_cache_215_gb300 import pkv
+        self.pkv = pkv
+        self.name = name
+        self.case = wl.FULL[name]()
+        c = self.case
+        self.tens = wl.make_tensors(c, device=device)
+        t = self.tens
+        self.geom = pkv.geometry(c.num_layers, c.num_q_heads, c.num_kv_heads, c.head_dim,
+                                 c.block_size, c.num_blocks, c.kv_dtype)
+        self.pool = pkv.KVPool(self.geom, device=device)
+        self.pool.storage.zero_()
+        ids = c.tables[c.tables >= 0]
+        uniq, counts = np.unique(ids, return_counts=True)
+        self.pool.reserve(uniq.tolist())
+        if (counts > 1).any():
+            self.pool.share(np.repeat(uniq, counts - 1).tolist())
+        self.tables = torch.from_numpy(c.tables).to(device)
+        self.seq_lens = torch.from_numpy(c.seq_lens).to(device)
+        self.max_len = int(c.seq_lens.max())
+        self.ks = self.vs = 1.0
+        if c.kv_dtype == "e4m3":
+            amax = torch.zeros(4, dtype=torch.float32, device=device)
+            for i, x in enumerate((t.k_tokens, t.k_new, t.v_tokens, t.v_new)):
+                pkv.kv_absmax(x, amax[i:i + 1])
+            a = amax.cpu().numpy()
+            self.ks = pkv.fp8_scale(float(max(a[0], a[1])))
+            self.vs = pkv.fp8_scale(float(max(a[2], a[3])))
+        self.pool.append_tokens(c.layer, t.k_tokens, t.v_tokens, self.tables, t.tok_seq,
+                                t.tok_pos, self.ks, self.vs)
+        # the logical token arrays are no longer needed on the device
+        self.tens.k_tokens = self.tens.v_tokens = None
+        self.out = torch.empty(c.batch, c.num_q_heads, c.head_dim,
+                               dtype=wl.TORCH_DT[c.out_dtype], device=device)
+        nb = pkv.workspace_bytes(self.geom, c.batch, self.max_len, 0)
+        self.ws = torch.empty(nb, dtype=torch.uint8, device=device)
+        self.o_attn = pkv.launch_opts(phase=1)
+        self.o_merge = pkv.launch_opts(phase=2)
+        torch.cuda.synchronize()
+
+    def append(self, k=None, v=None, pos=None):
+        t = self.tens
+        self.pool.append(self.case.layer, t.k_new if k is None else k, t.v_new if v is None else v,
+                         self.tables, t.new_pos if pos is None else pos, self.ks, self.vs)
+
+    def attention(self, opts=None, q=None, seq_lens=None, out=None):
+        c = self.case
+        self.pkv.paged_decode_attention(self.out if out is None else out,
+                                        self.tens.q if q is None else q, self.pool, c.layer,
+                                        self.tables, self.seq_lens if seq_lens is None else seq_lens,
+                                        self.max_len, c.scale, self.ks, self.vs, 0, self.ws, opts)
+
+    def close(self):
+        self.pool.close()
+
+
+def time_steps(w, steps, warmup, split_phases):
+    """Run warm-up then `steps` timed steps; returns (total ms, per-step attention ms list)."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        w.append()
+        w.attention()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps if split_phases else 0)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        w.append()
+        if split_phases:
+            ev[i][0].record(stream)
+            w.attention(w.o_attn)
+            ev[i][1].record(stream)
+            w.attention(w.o_merge)
+        else:
+            w.attention()
+    end.record(stream)
+    torch.cuda.synchronize()
+    total = start.elapsed_time(end)
+    attn = [a.elapsed_time(b) for a, b in ev]
+    return total, attn
+
+
+def time_e2e(w, steps, warmup):
+    """Through the C ABI from pinned host buffers: per step copy q, k_new, v_new,
+    positions and lengths host->device, append, attend, copy out device->host."""
+    c = w.case
+    t = w.tens
+    host = {k: getattr(t, k).cpu().pin_memory() for k in ("q", "k_new", "v_new", "new_pos")}
+    host["seq_lens"] = torch.from_numpy(c.seq_lens).pin_memory()
+    dev = {k: torch.empty_like(v, device="cuda") for k, v in host.items()}
+    out_h = torch.empty(w.out.shape, dtype=w.out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        w.append(dev["k_new"], dev["v_new"], dev["new_pos"])
+        w.attention(q=dev["q"], seq_lens=dev["seq_lens"])
+        out_h.copy_(w.out, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / steps, h2d, d2h
+
+
+def cpu_baseline(w, budget_s=15.0):
+    """The fp64 oracle, as it stands, on this host's cores: a bounded sample of
+    query rows of the same workload (its own pool built by its own append)."""
+    import oracle
+    c = w.case
+    tens = wl.make_tensors(c, device="cuda")
+    raw = wl.raw_numpy
+    eb = c.kv_elem_bytes()
+    pool = np.zeros(oracle.kv_bytes(c.num_layers, c.num_kv_heads, c.head_dim,
+                                    c.num_blocks * c.block_size, eb), dtype=np.uint8)
+    in_dt = "bf16" if c.kv_dtype == "e4m3" else c.kv_dtype
+    oracle.append_tokens(pool, c.kv_dtype, c.geometry, c.layer, raw(tens.k_tokens),
+                         raw(tens.v_tokens), in_dt, c.tables, raw(tens.tok_seq), raw(tens.tok_pos),
+                         w.ks, w.vs)
+    q = raw(tens.q)
+    del tens
+    rows_all = c.batch * c.num_q_heads
+    per_row_bytes = kv_bytes(c) / rows_all
+    done_rows, spent, n = 0, 0.0, max(1, oracle.num_threads())
+    while spent < budget_s and done_rows < rows_all:
+        rows = np.arange(done_rows, min(rows_all, done_rows + n), dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.decode(q, c.q_dtype, pool, c.kv_dtype, c.geometry, c.layer, c.tables, c.seq_lens,
+                      c.scale, w.ks, w.vs, rows=rows)
+        spent += time.perf_counter() - t0
+        done_rows += rows.size
+    gbs = done_rows * per_row_bytes / spent / 1e9
+    return {"value": gbs, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{done_rows} of {rows_all} (sequence, query head) rows of the same "
+                      f"workload, fp64, {spent:.1f} s; GB/s counts each row's share of the "
+                      f"KV bytes"}
+
+
+def measure(name, steps, warmup, device, with_clocks=False, gpu_index=0, e2e=True):
+    from paged_kv_cache_215_gb300 import pkv
+    w = Workload(name, device)
+    c = w.case
+    peak, peak_kind = peaks()
+    sampler = ClockSampler(gpu_index) if with_clocks else None
+    # headline: the production path (attention + merge chained with PDL)
+    if sampler:
+        sampler.start()
+    n0 = pkv.launch_count()
+    total_ms, _ = time_steps(w, steps, warmup, split_phases=False)
+    launches = pkv.launch_count() - n0 - 3 * warmup
+    clocks = sampler.stop() if sampler else None
+    # the attention kernel alone, timed per launch with events on its stream
+    _, attn = time_steps(w, steps, 3, split_phases=True)
+    ms = total_ms / steps
+    attn_ms = float(np.mean(attn))
+    res = {
+        "ms_per_step": ms,
+        "kv_bytes": kv_bytes(c),
+        "kv_gbs": kv_bytes(c) / (ms * 1e-3) / 1e9,
+        "attn_kernel_us": attn_ms * 1e3,
+        "attn_kernel_p10_p90_us": [float(np.percentile(attn, 10)) * 1e3,
+                                   float(np.percentile(attn, 90)) * 1e3],
+        "algorithmic_bytes": algorithmic_attn_bytes(c),
+        "roofline": {
+            "bound": "hbm",
+            "achieved": algorithmic_attn_bytes(c) / (attn_ms * 1e-3) / 1e9,
+            "peak": peak, "unit": "GB/s",
+            "frac": algorithmic_attn_bytes(c) / (attn_ms * 1e-3) / 1e9 / peak,
+            "traffic": profiled_traffic(name),
+            "peak_kind": peak_kind,
+        },
+        "tokens_per_s_per_layer": c.batch / (ms * 1e-3),
+        "decode_tokens_per_s_model": c.batch / (ms * 1e-3 * MODEL_LAYERS[name]),
+        "model_layers": MODEL_LAYERS[name],
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "batch": c.batch,
+        "seq_len_max": int(c.seq_lens.max()),
+        "block_waste": wl.block_waste(c),
+    }
+    if c.shared_prefix_tokens:
+        res["unique_kv_bytes"] = unique_kv_bytes(c)
+        res["unique_kv_gbs"] = unique_kv_bytes(c) / (ms * 1e-3) / 1e9
+    if e2e:
+        e_ms, h2d, d2h = time_e2e(w, max(10, steps // 10), 3)
+        res["e2e"] = {"value": kv_bytes(c) / (e_ms * 1e-3) / 1e9, "unit": UNIT,
+                      "ms_per_step": e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    return w, res
+
+
+def run_ours(args):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    from paged_kv_cache_215_gb300 import build
+    if rank == 0:
+        build.build()
+    if ws > 1:
+        dist.barrier()
+    name = args.workload
+    w, res = measure(name, args.steps, args.warmup, device, with_clocks=True, gpu_index=local)
+    # whole-job time: max over ranks of the headline loop
+    ms = res["ms_per_step"]
+    if ws > 1:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = ws * res["kv_bytes"] / (ms * 1e-3) / 1e9
+    extra = {}
+    if rank == 0 and not args.no_cpu_baseline:
+        extra["cpu_baseline"] = cpu_baseline(w)
+    w.close()
+    del w
+    torch.cuda.empty_cache()
+    others = {}
+    if rank == 0 and not args.only_primary:
+        for other in SECONDARY:
+            ow, ores = measure(other, max(50, args.steps // 20), args.warmup, device,
+                               with_clocks=False, e2e=False)
+            ow.close()
+            del ow
+            torch.cuda.empty_cache()
+            others[other] = {k: ores[k] for k in ("ms_per_step", "kv_gbs", "attn_kernel_us",
+                                                  "tokens_per_s_per_layer",
+                                                  "decode_tokens_per_s_model", "batch",
+                                                  "block_waste")}
+            others[other]["roofline_frac"] = ores["roofline"]["frac"]
+            others[other]["achieved_gbs"] = ores["roofline"]["achieved"]
+            if "unique_kv_gbs" in ores:
+                others[other]["unique_kv_gbs"] = ores["unique_kv_gbs"]
+    if ws > 1:
+        dist.barrier()
+    if rank != 0:
+        return
+    c = wl.FULL[name]()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": c.kv_dtype, "data": "synthetic (seeded N(0,1))",
+        "config": {"workload": wl.FULL[name]().name, "batch": c.batch,
+                   "seq_len": int(c.seq_lens.max()), "q_heads": c.num_q_heads,
+                   "kv_heads": c.num_kv_heads, "head_dim": c.head_dim,
+                   "block_size": c.block_size, "kv_dtype": c.kv_dtype,
+                   "parallelism": f"dp{ws} (independent sequences per GPU)",
+                   "l2": "inputs larger than L2 (KV read per step >> 129 MB), no flush"},
+        "decode_tokens_per_s": res["decode_tokens_per_s_model"],
+        "decode_tokens_per_s_per_layer": res["tokens_per_s_per_layer"],
+        "roofline": res["roofline"],
+        "attn_kernel_us": res["attn_kernel_us"],
+        "e2e": res["e2e"],
+        "gpu_launches": res["gpu_launches"],
+        "clocks": res["clocks"],
+        "block_waste": res["block_waste"],
+    }
+    line.update(extra)
+    if others:
+        line["workloads"] = others
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    name = args.workload
+    c = wl.FULL[name]()
+    tens = wl.make_tensors(c, device="cpu" if not torch.cuda.is_available() else "cuda")
+    raw = wl.raw_numpy
+    ks = vs = 1.0
+    if c.kv_dtype == "e4m3":
+        ka = max(oracle.absmax(raw(tens.k_tokens), "bf16"), oracle.absmax(raw(tens.k_new), "bf16"))
+        va = max(oracle.absmax(raw(tens.v_tokens), "bf16"), oracle.absmax(raw(tens.v_new), "bf16"))
+        ks = float(np.float32(ka) / np.float32(448)) if ka > 0 else 1.0
+        vs = float(np.float32(va) / np.float32(448)) if va > 0 else 1.0
+    eb = c.kv_elem_bytes()
+    pool = np.zeros(oracle.kv_bytes(c.num_layers, c.num_kv_heads, c.head_dim,
+                                    c.num_blocks * c.block_size, eb), dtype=np.uint8)
+    in_dt = "bf16" if c.kv_dtype == "e4m3" else c.kv_dtype
+    oracle.append_tokens(pool, c.kv_dtype, c.geometry, c.layer, raw(tens.k_tokens),
+                         raw(tens.v_tokens), in_dt, c.tables, raw(tens.tok_seq), raw(tens.tok_pos),
+                         ks, vs)
+    q = raw(tens.q)
+    knew, vnew, npos = raw(tens.k_new), raw(tens.v_new), raw(tens.new_pos)
+    del tens
+    rows_all = c.batch * c.num_q_heads
+    per_row = kv_bytes(c) / rows_all
+    threads = oracle.num_threads()
+
+    def step(rows):
+        oracle.append(pool, c.kv_dtype, c.geometry, c.layer, knew, vnew, in_dt, c.tables, npos,
+                      ks, vs)
+        oracle.decode(q, c.q_dtype, pool, c.kv_dtype, c.geometry, c.layer, c.tables, c.seq_lens,
+                      c.scale, ks, vs, rows=rows)
+
+    # size one step's sample so that the whole run takes about two minutes
+    probe = np.arange(min(threads, rows_all), dtype=np.int32)
+    t0 = time.perf_counter()
+    step(probe)
+    per_row_s = (time.perf_counter() - t0) / probe.size
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n_rows = int(max(1, min(rows_all, budget / max(per_row_s, 1e-9))))
+    cursor = 0
+
+    def next_rows():
+        nonlocal cursor
+        r = (np.arange(n_rows) + cursor) % rows_all
+        cursor = (cursor + n_rows) % rows_all
+        return r.astype(np.int32)
+
+    for _ in range(args.warmup):
+        step(next_rows())
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step(next_rows())
+    total = time.perf_counter() - t0
+    value = args.steps * n_rows * per_row / total / 1e9
+    sample = (f"{n_rows} of {rows_all} (sequence, query head) rows per step, fp64 oracle "
+              f"(append + paged decode), GB/s counts each row's share of the KV bytes")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1))",
+        "config": {"workload": c.name, "batch": c.batch, "seq_len": int(c.seq_lens.max()),
+                   "q_heads": c.num_q_heads, "kv_heads": c.num_kv_heads,
+                   "head_dim": c.head_dim, "block_size": c.block_size, "kv_dtype": c.kv_dtype},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=PRIMARY, choices=sorted(wl.FULL))
+    ap.add_argument("--only-primary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,245 @@
+/*
+ * pkv.h -- C ABI of the GB300 (sm_103a) paged KV-cache decode-attention library.
+ *
+ * The operations follow the problem statement of these web pages:
+ *   [ENG26]  "The engineering truth of long-context inference 2026: PagedAttention,
+ *            Ring Attention and KV-cache offload from 128K to 1M context"
+ *            (blog.lonae.com), sections 1.1, 2.1-2.3, 3.1.
+ *   [UNLOCK] "Unlocking long context: engineering practice for million-token LLM
+ *            inference" (ybb.press), sections 3.1, 3.2, 4.1, 5.1.
+ *   [MHPN]   long-context article at mhpn.cn (news 2466452), sections 1.1, 3.1, 3.2.
+ *   [SEQPAR] "Sequence-parallel engineering for long-context LLM inference: Ring
+ *            Attention and distributed KV cache" (ybb.press), section
+ *            "numerically stable incremental softmax".
+ *
+ * Conventions shared by every call:
+ *   - Every device buffer is owned by the caller (for example a torch tensor);
+ *     the library never allocates device memory.  `d_` marks a device pointer,
+ *     `h_` or no prefix a host pointer.
+ *   - Shapes are row-major: q and out [batch, num_q_heads, head_dim];
+ *     k and v of new tokens [tokens, num_kv_heads, head_dim]; block tables
+ *     int32 [batch, max_blocks_per_seq] (entries past ceil(seq_len/block_size)
+ *     are never read).
+ *   - The pool has the pages' layout [num_blocks, 2, num_layers, num_kv_heads,
+ *     block_size, head_dim] ([ENG26] 2.2): the K (index 0) and V (index 1)
+ *     tiles of one (block, layer, kv head) are block_size x head_dim contiguous
+ *     elements.
+ *   - GQA ([MHPN] 3.2): G = num_q_heads / num_kv_heads consecutive query heads
+ *     share one KV head: query head h reads KV head h / G.
+ *   - Calls that take a cudaStream_t are asynchronous on that stream; their
+ *     return code reports host-side validation and launch errors only.  Errors
+ *     found on the device (a block id outside the pool, a bounded wait that ran
+ *     out) are recorded in the pool's status word and read by pkv_check_status.
+ *   - No C++ exception crosses this boundary.  Functions returning int return a
+ *     pkv_status (0 = success, negative = error).
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_API __attribute__((visibility("default")))
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_EINVAL = -1,       /* an argument is out of range or inconsistent */
+  PKV_ENOMEM = -2,       /* the pool has too few free blocks, or the workspace is too small */
+  PKV_ECUDA = -3,        /* a CUDA runtime call failed */
+  PKV_EBOUNDS = -4,      /* (device) a block id or position outside the pool or table */
+  PKV_ETIMEOUT = -5,     /* (device) a bounded wait inside a kernel ran out */
+  PKV_EUNSUPPORTED = -6  /* a valid combination this build has no kernel for */
+} pkv_status;
+
+typedef enum { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2, PKV_FP8_E4M3 = 3 } pkv_dtype;
+
+/* Geometry of one pool.  kv_dtype is fixed for the pool's lifetime. */
+typedef struct {
+  int32_t num_layers, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks;
+  int32_t kv_dtype; /* a pkv_dtype */
+} pkv_geometry;
+
+/* Opaque, library-owned host state of a pool: geometry, the caller's device
+ * buffer, the host block allocator (free list plus per-block reference counts)
+ * and cached TMA descriptors. */
+typedef struct pkv_pool pkv_pool;
+
+/* Bytes of a device status word (int32 x 4) that kv_pool_create accepts. */
+#define PKV_STATUS_BYTES 16
+
+/* ---------------------------------------------------------------- pool sizing */
+
+/* [MHPN] 3.1, [ENG26] 1.1: 2 x num_layers x num_kv_heads x head_dim x
+ * (num_blocks x block_size) x bytes(kv_dtype).  Returns 0 for an invalid
+ * geometry. */
+PKV_API size_t kv_pool_bytes(const pkv_geometry* geom);
+
+/* ---------------------------------------------------------------- pool lifetime */
+
+/* Create the host state for a pool whose storage the caller owns.
+ *   d_pool     device buffer of at least kv_pool_bytes(geom) bytes, 16-byte aligned
+ *   pool_bytes its size
+ *   d_status   device buffer of PKV_STATUS_BYTES bytes for the device error word
+ *              (zeroed here), or NULL to not record device errors
+ * Supported: head_dim in [8, 256] and a multiple of 8 (16 for E4M3);
+ * block_size in [1, 256]; num_q_heads a multiple of num_kv_heads.
+ * All blocks start free.  Returns PKV_OK and *out, or PKV_EINVAL. */
+PKV_API int kv_pool_create(const pkv_geometry* geom, void* d_pool, size_t pool_bytes,
+                           int32_t* d_status, pkv_pool** out);
+PKV_API int kv_pool_destroy(pkv_pool* pool);
+PKV_API int kv_pool_geometry(const pkv_pool* pool, pkv_geometry* out);
+
+/* ---------------------------------------------------------------- host block allocator */
+/* [ENG26] 2.2 allocate_block and [UNLOCK] 3.1 on-demand allocation: a
+ * sequence's table grows by one block when its next token starts a new block.
+ * The allocator is host-only and not thread-safe; ids are in [0, num_blocks). */
+
+/* Take n free blocks (all or nothing: PKV_ENOMEM leaves the pool unchanged).
+ * Each gets reference count 1.  out_block_ids: host int32[n]. */
+PKV_API int kv_pool_alloc(pkv_pool* pool, int n, int32_t* out_block_ids);
+/* Take these specific free blocks (all or nothing; PKV_EINVAL if one is taken
+ * or repeated).  Lets a caller lay tables out over chosen ids. */
+PKV_API int kv_pool_reserve(pkv_pool* pool, int n, const int32_t* block_ids);
+/* Drop one reference from each block; a block whose count reaches 0 is free
+ * again.  PKV_EINVAL (and no change) if any id is free or out of range. */
+PKV_API int kv_pool_free(pkv_pool* pool, int n, const int32_t* block_ids);
+/* Add one reference to each block (a shared prefix, [UNLOCK] 3.1 copy-on-write). */
+PKV_API int kv_pool_share(pkv_pool* pool, int n, const int32_t* block_ids);
+/* Reference count of a block (0 = free), or PKV_EINVAL. */
+PKV_API int kv_pool_refcount(const pkv_pool* pool, int32_t block_id);
+PKV_API int kv_pool_num_free(const pkv_pool* pool);
+/* Copy-on-write before writing into block `id`: if its count is 1, *out_id = id;
+ * otherwise take a free block, copy all of `id`'s bytes (every layer, K and V)
+ * into it on `stream`, drop one reference from `id` and return the new id.
+ * PKV_ENOMEM if no block is free. */
+PKV_API int kv_pool_cow(pkv_pool* pool, int32_t id, int32_t* out_id, cudaStream_t stream);
+
+/* ---------------------------------------------------------------- append (reshape_and_cache) */
+
+/* [ENG26] 2.2 append_token, one token per sequence: for s in [0, batch),
+ *   pos = d_positions[s], block = d_block_tables[s][pos / block_size],
+ *   offset = pos % block_size,
+ *   pool[block, 0, layer, :, offset, :] = d_k[s];  pool[block, 1, layer, :, offset, :] = d_v[s].
+ * d_k, d_v: [batch, num_kv_heads, head_dim] in in_dtype.  For a pool of
+ * kv_dtype f32/f16/bf16, in_dtype must equal kv_dtype and the bytes are copied.
+ * For an E4M3 pool ([UNLOCK] 3.2, per-tensor FP8) in_dtype is f32, f16 or bf16
+ * and each element is stored as e4m3(x / scale): IEEE fp32 division, round to
+ * nearest even, finite overflow and +-Inf saturate to +-448, NaN -> 0x7F;
+ * k_scale / v_scale (> 0) are used only for E4M3.  A negative position means
+ * "no token for this sequence" and is skipped (padding).  A position past the
+ * table, or a block id outside the pool, records PKV_EBOUNDS and skips that
+ * token. */
+PKV_API int kv_append(pkv_pool* pool, int layer, const void* d_k, const void* d_v,
+                      pkv_dtype in_dtype, const int32_t* d_block_tables, int max_blocks_per_seq,
+                      const int32_t* d_positions, int batch, float k_scale, float v_scale,
+                      cudaStream_t stream);
+
+/* The same store for num_tokens tokens: token i belongs to sequence
+ * d_seq_ids[i] (< batch) at position d_positions[i] (a prefill or bulk fill).
+ * Several tokens may target one sequence; two tokens must not target one slot
+ * unless their values are equal. */
+PKV_API int kv_append_tokens(pkv_pool* pool, int layer, const void* d_k, const void* d_v,
+                             pkv_dtype in_dtype, const int32_t* d_block_tables,
+                             int max_blocks_per_seq, int batch, const int32_t* d_seq_ids,
+                             const int32_t* d_positions, int64_t num_tokens, float k_scale,
+                             float v_scale, cudaStream_t stream);
+
+/* Largest |x| over n elements of d_x (f32/f16/bf16; NaN ignored), written to
+ * *d_amax (device float) on `stream`.  The per-tensor FP8 scale is amax / 448
+ * (amax = 0 -> scale 1). */
+PKV_API int kv_absmax(const void* d_x, pkv_dtype dtype, int64_t n, float* d_amax,
+                      cudaStream_t stream);
+
+/* ---------------------------------------------------------------- decode attention */
+
+/* Workspace bytes paged_decode_attention needs on the current device for this
+ * geometry, batch and num_splits (0 = automatic).  max_seq_len is the largest
+ * seq_len the call will see. */
+PKV_API size_t paged_decode_workspace_bytes(const pkv_geometry* geom, int batch, int max_seq_len,
+                                            int num_splits);
+
+/* Decode attention over the paged pool ([UNLOCK] 4.1 and 5.1, [MHPN] 1.1, 3.2):
+ * for each sequence s < batch and query head h < num_q_heads, with
+ * n = d_seq_lens[s] >= 0 tokens and kv head h / G,
+ *   s_j = scale * <q[s,h,:], K_s[j,:]>,  w = softmax(s),  out[s,h,:] = sum_j w_j V_s[j,:]
+ * where token j of sequence s is read from pool[table[s][j / bs], *, layer, kv, j % bs, :]
+ * and E4M3 elements are dequantised as value x k_scale (K) or x v_scale (V).
+ * A sequence with n = 0 gets out = 0.
+ * The key range of each sequence is cut into partitions whose partial results
+ * are merged by log-sum-exp ([SEQPAR] incremental softmax, [ENG26] 3.1):
+ *   num_splits = 0: automatic.  The token stream of all sequences is cut into
+ *     equal contiguous runs of blocks, one per resident CTA, so every SM reads
+ *     the same number of bytes; sequences spanning several runs are merged.
+ *   num_splits = S >= 1: every sequence is cut into S block-aligned partitions
+ *     (partials in the workspace as [batch, num_q_heads, S, head_dim] fp32 plus
+ *     [batch, num_q_heads, S] log-sum-exp, then merge_partials); S = 1 writes
+ *     out directly.
+ * d_q: [batch, num_q_heads, head_dim] in q_dtype; d_out same shape in out_dtype
+ * (f32, f16 or bf16).  scale is the softmax scale (the pages use 1/sqrt(head_dim)).
+ * d_workspace: at least paged_decode_workspace_bytes(...) bytes, 16-byte
+ * aligned, device memory; it is scratch and needs no initialisation.
+ * Errors: PKV_EINVAL (shapes, dtypes, batch < 0, max_seq_len < 0),
+ * PKV_ENOMEM (workspace too small), PKV_EUNSUPPORTED, PKV_ECUDA. */
+PKV_API int paged_decode_attention(void* d_out, pkv_dtype out_dtype, const void* d_q,
+                                   pkv_dtype q_dtype, const pkv_pool* pool, int layer,
+                                   const int32_t* d_block_tables, int max_blocks_per_seq,
+                                   const int32_t* d_seq_lens, int batch, int max_seq_len,
+                                   float scale, float k_scale, float v_scale, int num_splits,
+                                   void* d_workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* Launch choices a caller may force (tests, ablations, benchmarks).  Zero-filled
+ * means "automatic" for every field. */
+typedef struct {
+  int32_t kernel;          /* 0 auto, 1 the SIMT kernel, 2 the tensor-core (mma) kernel */
+  int32_t ctas_per_sm;     /* 0 auto; the persistent grid is SMs x this */
+  int32_t kv_heads_per_cta;/* 0 auto */
+  int32_t stages;          /* 0 auto; shared-memory pipeline depth */
+  int32_t phase;           /* 0 attention then merge, 1 attention only, 2 merge only */
+  int32_t reserved[3];
+} pkv_launch_opts;
+
+/* paged_decode_attention with forced launch choices.  phase 1 and 2 split the
+ * call into its two kernels so a caller can time them apart; the workspace
+ * carries the partial results from phase 1 to phase 2. */
+PKV_API int paged_decode_attention_ex(void* d_out, pkv_dtype out_dtype, const void* d_q,
+                                      pkv_dtype q_dtype, const pkv_pool* pool, int layer,
+                                      const int32_t* d_block_tables, int max_blocks_per_seq,
+                                      const int32_t* d_seq_lens, int batch, int max_seq_len,
+                                      float scale, float k_scale, float v_scale, int num_splits,
+                                      void* d_workspace, size_t ws_bytes,
+                                      const pkv_launch_opts* opts, cudaStream_t stream);
+
+/* Log-sum-exp merge of partial results ([SEQPAR] incremental softmax,
+ * [ENG26] 3.1): for each row r = (s, h) of batch x num_q_heads,
+ *   M = max_p lse[r,p],  w_p = exp(lse[r,p] - M),
+ *   out[r,:] = sum_p w_p O[r,p,:] / sum_p w_p.
+ * d_part_o: fp32 [batch, num_q_heads, num_splits, head_dim], each partial
+ * already normalised; d_part_lse: fp32 [batch, num_q_heads, num_splits],
+ * natural log-sum-exp of that partition's scores.  A partial with lse = -inf
+ * has weight 0; a row whose partials are all -inf gets out = 0.
+ * d_out: [batch, num_q_heads, head_dim] in out_dtype (f32, f16, bf16). */
+PKV_API int merge_partials(void* d_out, pkv_dtype out_dtype, const float* d_part_o,
+                           const float* d_part_lse, int batch, int num_q_heads, int head_dim,
+                           int num_splits, cudaStream_t stream);
+
+/* ---------------------------------------------------------------- status */
+
+/* Synchronise `stream`, read and clear the pool's device status word and
+ * return the first error recorded since the last check (PKV_OK if none;
+ * PKV_OK too if the pool has no status word). */
+PKV_API int pkv_check_status(const pkv_pool* pool, cudaStream_t stream);
+/* A static string naming a pkv_status. */
+PKV_API const char* pkv_strerror(int status);
+/* Number of kernel launches this library has issued in this process (a
+ * counter the benchmark reads to report its launches). */
+PKV_API uint64_t pkv_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H_ */

@@ -180,6 +180,7 @@ static void or_store_token(void* pool, int kv_dtype, int L, int Hkv, int bs, int
  * block_id = pos // bs, offset = pos % bs, and
  * pool[table[s][block_id], 0/1, layer, :, offset, :] = k[s], v[s].
  * Block allocation is the caller's job (the table must already hold the block).
+ * A negative position means the sequence has no token to append (skipped).
  * Returns 0, or -1 on an invalid dtype pair, -2 on an out-of-range position or block id.
  */
 int or_append(void* pool, int kv_dtype, int NB, int L, int Hkv, int bs, int D, int layer,
@@ -188,7 +189,8 @@ int or_append(void* pool, int kv_dtype, int NB, int L, int Hkv, int bs, int D, i
   if (kv_dtype != OR_E4M3 && in_dtype != kv_dtype) return -1;
   for (int s = 0; s < B; ++s) {
     int pos = positions[s];
-    if (pos < 0 || pos / bs >= max_blocks) return -2;
+    if (pos < 0) continue;
+    if (pos / bs >= max_blocks) return -2;
     int blk = tables[(size_t)s * max_blocks + pos / bs];
     if (blk < 0 || blk >= NB) return -2;
     or_store_token(pool, kv_dtype, L, Hkv, bs, D, layer, 0, blk, pos % bs, k, (size_t)s, in_dtype, k_scale);
@@ -210,7 +212,8 @@ int or_append_tokens(void* pool, int kv_dtype, int NB, int L, int Hkv, int bs, i
   if (kv_dtype != OR_E4M3 && in_dtype != kv_dtype) return -1;
   for (long long i = 0; i < n; ++i) {
     int s = seq_ids[i], pos = positions[i];
-    if (s < 0 || s >= B || pos < 0 || pos / bs >= max_blocks) return -2;
+    if (pos < 0) continue;
+    if (s < 0 || s >= B || pos / bs >= max_blocks) return -2;
     int blk = tables[(size_t)s * max_blocks + pos / bs];
     if (blk < 0 || blk >= NB) return -2;
     or_store_token(pool, kv_dtype, L, Hkv, bs, D, layer, 0, blk, pos % bs, k, (size_t)i, in_dtype, k_scale);

@@ -1,0 +1,69 @@
+// launch.h -- internal interface between the host library (pkv.cpp) and the
+// kernels (*.cu).  Not installed; the public ABI is include/pkv.h.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+// Decode attention arguments, shared by the tensor-core kernel, the SIMT kernel
+// and the merge kernels.
+struct DecodeArgs {
+  const void* q;             // [B, Hq, D] q_dtype
+  void* out;                 // [B, Hq, D] out_dtype
+  const void* pool;          // [NB, 2, L, Hkv, BS, D] kv_dtype
+  const int32_t* tables;     // [B, max_blocks]
+  const int32_t* seq_lens;   // [B]
+  float* part_o;             // partial outputs (layout depends on mode)
+  float* part_lse;           // partial natural log-sum-exp
+  int2* unit_info;           // balanced mode: per unit (first slot, piece count)
+  int32_t* status;           // device error word or nullptr
+  int B, Hq, Hkv, G, D, BS, L, layer, max_blocks, num_blocks;
+  int q_dtype, out_dtype, kv_dtype;
+  int HG;                    // kv heads per CTA (tensor-core kernel)
+  int NHG;                   // Hkv / HG
+  int stages;                // shared-memory pipeline depth
+  int mode;                  // 0 balanced token stream, 1 fixed S partitions per sequence
+  int S;                     // partitions per sequence in mode 1
+  float qk_scale_log2;       // softmax scale * log2(e) (* k_scale for E4M3)
+  float v_scale;             // v_scale for E4M3, else 1
+};
+
+// Shared memory the tensor-core kernel needs for one CTA.
+size_t mma_stage_bytes(int kv_dtype, int BS, int HG);
+size_t mma_smem_bytes(int kv_dtype, int BS, int HG, int stages);
+bool mma_supported(int kv_dtype, int BS, int D, int G);
+
+cudaError_t launch_decode_mma(const CUtensorMap* map, const DecodeArgs& a, int grid_x, int grid_y,
+                              cudaStream_t stream);
+cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t stream);
+// Merge of the balanced-mode partials, one CTA per (unit, head in the unit).
+cudaError_t launch_merge_units(const DecodeArgs& a, bool pdl, cudaStream_t stream);
+// Merge of [rows, S, D] partials (the public merge_partials layout).
+cudaError_t launch_merge_rows(void* out, int out_dtype, const float* part_o, const float* part_lse,
+                              int rows, int S, int D, bool pdl, cudaStream_t stream);
+
+struct AppendArgs {
+  void* pool;
+  const void* k;
+  const void* v;
+  const int32_t* tables;
+  const int32_t* seq_ids;    // nullptr: token i belongs to sequence i
+  const int32_t* positions;
+  int32_t* status;
+  int64_t num_tokens;
+  int B, Hkv, D, BS, L, layer, max_blocks, num_blocks;
+  int in_dtype, kv_dtype;
+  float k_scale, v_scale;
+};
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
+cudaError_t launch_absmax(const void* x, int dtype, int64_t n, float* amax, cudaStream_t stream);
+
+// Launch counter shared by every launcher.
+void count_launch();
+
+}  // namespace pkv

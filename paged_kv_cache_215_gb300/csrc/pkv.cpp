@@ -1,0 +1,624 @@
+// pkv.cpp -- host side of the C ABI declared in include/pkv.h: argument
+// validation, the host block allocator, TMA descriptors, launch heuristics and
+// workspace layout.  Every step of the computation runs in the CUDA kernels;
+// nothing here touches K, V, q or out.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "launch.h"
+#include "pkv.h"
+
+namespace pkv {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+static int elem_bytes(int dtype) {
+  switch (dtype) {
+    case PKV_F32: return 4;
+    case PKV_F16: return 2;
+    case PKV_BF16: return 2;
+    case PKV_FP8_E4M3: return 1;
+    default: return 0;
+  }
+}
+
+static bool act_dtype(int dtype) { return dtype == PKV_F32 || dtype == PKV_F16 || dtype == PKV_BF16; }
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DeviceInfo {
+  int sms = 0, smem_optin = 0, smem_per_sm = 0;
+};
+
+static bool device_info(DeviceInfo* out) {
+  static std::mutex mu;
+  static std::map<int, DeviceInfo> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cache.find(dev);
+  if (it == cache.end()) {
+    DeviceInfo d;
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+            cudaSuccess)
+      return false;
+    it = cache.emplace(dev, d).first;
+  }
+  *out = it->second;
+  return true;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// ---------------------------------------------------------------- launch plans
+
+struct MmaPlan {
+  int HG = 0, NHG = 0, stages = 0, ctas_per_sm = 1, grid = 0;
+  size_t smem = 0;
+};
+
+static bool hg_ok(const pkv_geometry& g, int hg) {
+  return hg >= 1 && hg <= 8 && g.num_kv_heads % hg == 0 && hg * g.block_size <= 256;
+}
+
+// Tensor-core kernel: KV heads per CTA, pipeline depth and persistent grid.
+static bool plan_mma(const pkv_geometry& g, const DeviceInfo& dev, const pkv_launch_opts* o,
+                     MmaPlan* p) {
+  const int ctas = (o && o->ctas_per_sm > 0) ? o->ctas_per_sm : 1;
+  if (ctas > 8) return false;
+  int hg = (o && o->kv_heads_per_cta > 0) ? o->kv_heads_per_cta : 0;
+  if (hg) {
+    if (!hg_ok(g, hg)) return false;
+  } else {
+    for (int c = 8; c >= 1; --c)
+      if (hg_ok(g, c) && mma_stage_bytes(g.kv_dtype, g.block_size, c) <= 64 * 1024) {
+        hg = c;
+        break;
+      }
+    if (!hg) return false;
+  }
+  const size_t stage = mma_stage_bytes(g.kv_dtype, g.block_size, hg);
+  const size_t per_cta = std::min<size_t>((size_t)dev.smem_optin,
+                                          (size_t)dev.smem_per_sm / ctas - 1024);
+  int stages = (o && o->stages > 0) ? o->stages : 0;
+  if (!stages) {
+    const size_t fixed = mma_smem_bytes(g.kv_dtype, g.block_size, hg, 0);
+    stages = per_cta > fixed ? (int)((per_cta - fixed) / stage) : 0;
+    stages = std::min(stages, 8);
+  }
+  if (stages < 2 || stages > 16) return false;
+  p->HG = hg;
+  p->NHG = g.num_kv_heads / hg;
+  p->stages = stages;
+  p->ctas_per_sm = ctas;
+  p->grid = dev.sms * ctas;
+  p->smem = mma_smem_bytes(g.kv_dtype, g.block_size, hg, stages);
+  return p->smem <= (size_t)dev.smem_optin;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Balanced-mode workspace: partial O and lse per (slot, head of the group), and
+// per-unit (first slot, count).
+struct BalancedWs {
+  size_t o_off, lse_off, info_off, bytes;
+};
+static BalancedWs balanced_ws(const pkv_geometry& g, int batch, const MmaPlan& p) {
+  const size_t units = (size_t)batch * p.NHG;
+  const size_t slots = (size_t)p.grid + units;
+  const size_t hgg = (size_t)p.HG * (g.num_q_heads / g.num_kv_heads);
+  BalancedWs w;
+  w.o_off = 0;
+  w.lse_off = align256(slots * hgg * g.head_dim * sizeof(float));
+  w.info_off = w.lse_off + align256(slots * hgg * sizeof(float));
+  w.bytes = w.info_off + align256(units * sizeof(int2));
+  return w;
+}
+
+// Fixed-split workspace: [B, Hq, S, D] and [B, Hq, S].
+static size_t fixed_ws(const pkv_geometry& g, int batch, int S, size_t* lse_off) {
+  const size_t rows = (size_t)batch * g.num_q_heads * S;
+  const size_t o = align256(rows * g.head_dim * sizeof(float));
+  if (lse_off) *lse_off = o;
+  return S > 1 ? o + align256(rows * sizeof(float)) : 0;
+}
+
+static int simt_auto_splits(const pkv_geometry& g, int batch, int max_seq_len, int sms) {
+  const long long units = std::max<long long>(1, (long long)batch * g.num_kv_heads);
+  long long s = (8LL * sms + units - 1) / units;
+  const long long nb = std::max<long long>(1, ((long long)max_seq_len + g.block_size - 1) / g.block_size);
+  s = std::min<long long>(s, nb);
+  s = std::min<long long>(s, 1024);
+  return (int)std::max<long long>(s, 1);
+}
+
+static bool geometry_ok(const pkv_geometry* g) {
+  if (!g) return false;
+  if (g->num_layers < 1 || g->num_kv_heads < 1 || g->num_q_heads < 1 || g->head_dim < 8 ||
+      g->head_dim > 256 || g->head_dim % 8 != 0 || g->block_size < 1 || g->block_size > 256 ||
+      g->num_blocks < 1 || g->num_q_heads % g->num_kv_heads != 0 || elem_bytes(g->kv_dtype) == 0)
+    return false;
+  if (g->kv_dtype == PKV_FP8_E4M3 && g->head_dim % 16 != 0) return false;
+  // the tensor map addresses (block, k|v, layer) slabs with a 32-bit coordinate
+  if ((long long)g->num_blocks * 2 * g->num_layers >= (1LL << 31)) return false;
+  return true;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+struct pkv_pool {
+  pkv_geometry g;
+  void* d_pool = nullptr;
+  size_t bytes = 0;
+  int32_t* d_status = nullptr;
+  std::vector<int32_t> ref;        // reference count per block, 0 = free
+  std::vector<int32_t> free_ids;   // stack of free ids
+  std::vector<int32_t> free_pos;   // position of an id in free_ids, -1 if taken
+  std::map<int, CUtensorMap> tmaps;
+  std::mutex mu;
+
+  void take(int32_t id) {
+    const int32_t pos = free_pos[id];
+    const int32_t last = free_ids.back();
+    free_ids[pos] = last;
+    free_pos[last] = pos;
+    free_ids.pop_back();
+    free_pos[id] = -1;
+  }
+  void give(int32_t id) {
+    free_pos[id] = (int32_t)free_ids.size();
+    free_ids.push_back(id);
+  }
+  size_t block_bytes() const {
+    return (size_t)2 * g.num_layers * g.num_kv_heads * g.block_size * g.head_dim *
+           elem_bytes(g.kv_dtype);
+  }
+  // TMA descriptor over the pool viewed as [NB*2*L, Hkv*bs, D] with a box of
+  // HG*bs rows by one 128-byte line, swizzled 128B.
+  const CUtensorMap* tmap(int hg) {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = tmaps.find(hg);
+    if (it != tmaps.end()) return &it->second;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return nullptr;
+    const int eb = elem_bytes(g.kv_dtype);
+    CUtensorMapDataType dt = g.kv_dtype == PKV_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                             : g.kv_dtype == PKV_F16  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                      : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    cuuint64_t dims[3] = {(cuuint64_t)g.head_dim, (cuuint64_t)g.num_kv_heads * g.block_size,
+                          (cuuint64_t)g.num_blocks * 2 * g.num_layers};
+    cuuint64_t strides[2] = {(cuuint64_t)g.head_dim * eb,
+                             (cuuint64_t)g.num_kv_heads * g.block_size * g.head_dim * eb};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / eb), (cuuint32_t)(hg * g.block_size), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUtensorMap m;
+    CUresult r = enc(&m, dt, 3, d_pool, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return nullptr;
+    return &tmaps.emplace(hg, m).first->second;
+  }
+};
+
+extern "C" {
+
+size_t kv_pool_bytes(const pkv_geometry* g) {
+  if (!geometry_ok(g)) return 0;
+  return (size_t)2 * g->num_layers * g->num_kv_heads * g->head_dim *
+         ((size_t)g->num_blocks * g->block_size) * elem_bytes(g->kv_dtype);
+}
+
+int kv_pool_create(const pkv_geometry* g, void* d_pool, size_t pool_bytes, int32_t* d_status,
+                   pkv_pool** out) {
+  if (!out || !geometry_ok(g) || !d_pool || !aligned16(d_pool) || pool_bytes < kv_pool_bytes(g))
+    return PKV_EINVAL;
+  pkv_pool* p = new (std::nothrow) pkv_pool();
+  if (!p) return PKV_ENOMEM;
+  p->g = *g;
+  p->d_pool = d_pool;
+  p->bytes = pool_bytes;
+  p->d_status = d_status;
+  p->ref.assign(g->num_blocks, 0);
+  p->free_pos.assign(g->num_blocks, -1);
+  p->free_ids.reserve(g->num_blocks);
+  for (int32_t i = g->num_blocks - 1; i >= 0; --i) p->give(i);
+  if (d_status && cudaMemset(d_status, 0, PKV_STATUS_BYTES) != cudaSuccess) {
+    delete p;
+    return PKV_ECUDA;
+  }
+  *out = p;
+  return PKV_OK;
+}
+
+int kv_pool_destroy(pkv_pool* p) {
+  delete p;
+  return PKV_OK;
+}
+
+int kv_pool_geometry(const pkv_pool* p, pkv_geometry* out) {
+  if (!p || !out) return PKV_EINVAL;
+  *out = p->g;
+  return PKV_OK;
+}
+
+int kv_pool_alloc(pkv_pool* p, int n, int32_t* ids) {
+  if (!p || n < 0 || (n > 0 && !ids)) return PKV_EINVAL;
+  std::lock_guard<std::mutex> lk(p->mu);
+  if ((size_t)n > p->free_ids.size()) return PKV_ENOMEM;
+  for (int i = 0; i < n; ++i) {
+    const int32_t id = p->free_ids.back();
+    p->take(id);
+    p->ref[id] = 1;
+    ids[i] = id;
+  }
+  return PKV_OK;
+}
+
+int kv_pool_reserve(pkv_pool* p, int n, const int32_t* ids) {
+  if (!p || n < 0 || (n > 0 && !ids)) return PKV_EINVAL;
+  std::lock_guard<std::mutex> lk(p->mu);
+  std::vector<char> seen;
+  for (int i = 0; i < n; ++i) {
+    const int32_t id = ids[i];
+    if (id < 0 || id >= p->g.num_blocks || p->ref[id] != 0) return PKV_EINVAL;
+  }
+  seen.assign(p->g.num_blocks, 0);
+  for (int i = 0; i < n; ++i) {
+    if (seen[ids[i]]) return PKV_EINVAL;
+    seen[ids[i]] = 1;
+  }
+  for (int i = 0; i < n; ++i) {
+    p->take(ids[i]);
+    p->ref[ids[i]] = 1;
+  }
+  return PKV_OK;
+}
+
+int kv_pool_free(pkv_pool* p, int n, const int32_t* ids) {
+  if (!p || n < 0 || (n > 0 && !ids)) return PKV_EINVAL;
+  std::lock_guard<std::mutex> lk(p->mu);
+  std::map<int32_t, int> drops;
+  for (int i = 0; i < n; ++i) {
+    const int32_t id = ids[i];
+    if (id < 0 || id >= p->g.num_blocks) return PKV_EINVAL;
+    if (++drops[id] > p->ref[id]) return PKV_EINVAL;
+  }
+  for (int i = 0; i < n; ++i)
+    if (--p->ref[ids[i]] == 0) p->give(ids[i]);
+  return PKV_OK;
+}
+
+int kv_pool_share(pkv_pool* p, int n, const int32_t* ids) {
+  if (!p || n < 0 || (n > 0 && !ids)) return PKV_EINVAL;
+  std::lock_guard<std::mutex> lk(p->mu);
+  for (int i = 0; i < n; ++i)
+    if (ids[i] < 0 || ids[i] >= p->g.num_blocks || p->ref[ids[i]] == 0) return PKV_EINVAL;
+  for (int i = 0; i < n; ++i) ++p->ref[ids[i]];
+  return PKV_OK;
+}
+
+int kv_pool_refcount(const pkv_pool* p, int32_t id) {
+  if (!p || id < 0 || id >= p->g.num_blocks) return PKV_EINVAL;
+  return p->ref[id];
+}
+
+int kv_pool_num_free(const pkv_pool* p) {
+  if (!p) return PKV_EINVAL;
+  return (int)p->free_ids.size();
+}
+
+int kv_pool_cow(pkv_pool* p, int32_t id, int32_t* out_id, cudaStream_t stream) {
+  if (!p || !out_id || id < 0 || id >= p->g.num_blocks) return PKV_EINVAL;
+  std::lock_guard<std::mutex> lk(p->mu);
+  if (p->ref[id] <= 0) return PKV_EINVAL;
+  if (p->ref[id] == 1) {
+    *out_id = id;
+    return PKV_OK;
+  }
+  if (p->free_ids.empty()) return PKV_ENOMEM;
+  const int32_t nid = p->free_ids.back();
+  const size_t bb = p->block_bytes();
+  char* base = static_cast<char*>(p->d_pool);
+  if (cudaMemcpyAsync(base + (size_t)nid * bb, base + (size_t)id * bb, bb,
+                      cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+    return PKV_ECUDA;
+  p->take(nid);
+  p->ref[nid] = 1;
+  --p->ref[id];
+  *out_id = nid;
+  return PKV_OK;
+}
+
+static int append_common(pkv_pool* p, int layer, const void* k, const void* v, pkv_dtype in_dtype,
+                         const int32_t* tables, int max_blocks, int batch, const int32_t* seq_ids,
+                         const int32_t* positions, int64_t num_tokens, float k_scale,
+                         float v_scale, cudaStream_t stream) {
+  if (!p || layer < 0 || layer >= p->g.num_layers || batch < 0 || num_tokens < 0)
+    return PKV_EINVAL;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !tables || !positions || max_blocks < 1 || batch < 1) return PKV_EINVAL;
+  if (!aligned16(k) || !aligned16(v)) return PKV_EINVAL;
+  const bool fp8 = p->g.kv_dtype == PKV_FP8_E4M3;
+  if (fp8) {
+    if (!act_dtype(in_dtype)) return PKV_EINVAL;
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+      return PKV_EINVAL;
+  } else if ((int)in_dtype != p->g.kv_dtype) {
+    return PKV_EINVAL;
+  }
+  AppendArgs a{};
+  a.pool = p->d_pool;
+  a.k = k;
+  a.v = v;
+  a.tables = tables;
+  a.seq_ids = seq_ids;
+  a.positions = positions;
+  a.status = p->d_status;
+  a.num_tokens = num_tokens;
+  a.B = batch;
+  a.Hkv = p->g.num_kv_heads;
+  a.D = p->g.head_dim;
+  a.BS = p->g.block_size;
+  a.L = p->g.num_layers;
+  a.layer = layer;
+  a.max_blocks = max_blocks;
+  a.num_blocks = p->g.num_blocks;
+  a.in_dtype = in_dtype;
+  a.kv_dtype = p->g.kv_dtype;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  return launch_append(a, stream) == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+int kv_append(pkv_pool* p, int layer, const void* d_k, const void* d_v, pkv_dtype in_dtype,
+              const int32_t* d_block_tables, int max_blocks_per_seq, const int32_t* d_positions,
+              int batch, float k_scale, float v_scale, cudaStream_t stream) {
+  return append_common(p, layer, d_k, d_v, in_dtype, d_block_tables, max_blocks_per_seq, batch,
+                       nullptr, d_positions, batch, k_scale, v_scale, stream);
+}
+
+int kv_append_tokens(pkv_pool* p, int layer, const void* d_k, const void* d_v, pkv_dtype in_dtype,
+                     const int32_t* d_block_tables, int max_blocks_per_seq, int batch,
+                     const int32_t* d_seq_ids, const int32_t* d_positions, int64_t num_tokens,
+                     float k_scale, float v_scale, cudaStream_t stream) {
+  if (num_tokens > 0 && !d_seq_ids) return PKV_EINVAL;
+  return append_common(p, layer, d_k, d_v, in_dtype, d_block_tables, max_blocks_per_seq, batch,
+                       d_seq_ids, d_positions, num_tokens, k_scale, v_scale, stream);
+}
+
+int kv_absmax(const void* d_x, pkv_dtype dtype, int64_t n, float* d_amax, cudaStream_t stream) {
+  if (!d_amax || n < 0 || (n > 0 && !d_x) || !act_dtype(dtype)) return PKV_EINVAL;
+  return launch_absmax(d_x, dtype, n, d_amax, stream) == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+size_t paged_decode_workspace_bytes(const pkv_geometry* g, int batch, int max_seq_len,
+                                    int num_splits) {
+  if (!geometry_ok(g) || batch < 0 || max_seq_len < 0 || num_splits < 0) return 0;
+  DeviceInfo dev;
+  if (!device_info(&dev)) return 0;
+  if (num_splits > 0) return fixed_ws(*g, batch, num_splits, nullptr) + 256;
+  size_t need = fixed_ws(*g, batch, simt_auto_splits(*g, batch, max_seq_len, dev.sms), nullptr);
+  for (int hg = 1; hg <= 8; ++hg) {
+    if (!hg_ok(*g, hg)) continue;
+    for (int c = 1; c <= 4; ++c) {
+      MmaPlan p;
+      p.HG = hg;
+      p.NHG = g->num_kv_heads / hg;
+      p.grid = dev.sms * c;
+      need = std::max(need, balanced_ws(*g, batch, p).bytes);
+    }
+  }
+  return need + 256;
+}
+
+int paged_decode_attention_ex(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_dtype q_dtype,
+                              const pkv_pool* pool, int layer, const int32_t* d_block_tables,
+                              int max_blocks_per_seq, const int32_t* d_seq_lens, int batch,
+                              int max_seq_len, float scale, float k_scale, float v_scale,
+                              int num_splits, void* d_workspace, size_t ws_bytes,
+                              const pkv_launch_opts* opts, cudaStream_t stream) {
+  pkv_pool* p = const_cast<pkv_pool*>(pool);
+  if (!p || batch < 0 || max_seq_len < 0 || num_splits < 0 || layer < 0 ||
+      layer >= p->g.num_layers)
+    return PKV_EINVAL;
+  if (batch == 0) return PKV_OK;
+  const pkv_geometry& g = p->g;
+  if (!d_out || !d_q || !d_block_tables || !d_seq_lens || max_blocks_per_seq < 1)
+    return PKV_EINVAL;
+  if (!act_dtype(out_dtype) || !act_dtype(q_dtype) || !aligned16(d_q) || !aligned16(d_out))
+    return PKV_EINVAL;
+  if ((long long)max_seq_len > (long long)max_blocks_per_seq * g.block_size) return PKV_EINVAL;
+  if (!std::isfinite(scale)) return PKV_EINVAL;
+  const bool fp8 = g.kv_dtype == PKV_FP8_E4M3;
+  if (fp8 && (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) ||
+              !std::isfinite(v_scale)))
+    return PKV_EINVAL;
+  const int phase = opts ? opts->phase : 0;
+  const int kernel = opts ? opts->kernel : 0;
+  if (phase < 0 || phase > 2 || kernel < 0 || kernel > 2) return PKV_EINVAL;
+  DeviceInfo dev;
+  if (!device_info(&dev)) return PKV_ECUDA;
+
+  const int G = g.num_q_heads / g.num_kv_heads;
+  const bool q_ok_mma = fp8 ? true
+                            : (g.kv_dtype == PKV_BF16 ? q_dtype == PKV_BF16 : q_dtype == PKV_F16);
+  const bool mma_ok = mma_supported(g.kv_dtype, g.block_size, g.head_dim, G) && q_ok_mma;
+  const bool simt_ok = g.head_dim % 32 == 0 && g.head_dim <= 256 && G <= 16;
+  bool use_mma;
+  if (kernel == 2) {
+    if (!mma_ok) return PKV_EUNSUPPORTED;
+    use_mma = true;
+  } else if (kernel == 1) {
+    if (!simt_ok) return PKV_EUNSUPPORTED;
+    use_mma = false;
+  } else {
+    if (!mma_ok && !simt_ok) return PKV_EUNSUPPORTED;
+    use_mma = mma_ok;
+  }
+
+  DecodeArgs a{};
+  a.q = d_q;
+  a.out = d_out;
+  a.pool = p->d_pool;
+  a.tables = d_block_tables;
+  a.seq_lens = d_seq_lens;
+  a.status = p->d_status;
+  a.B = batch;
+  a.Hq = g.num_q_heads;
+  a.Hkv = g.num_kv_heads;
+  a.G = G;
+  a.D = g.head_dim;
+  a.BS = g.block_size;
+  a.L = g.num_layers;
+  a.layer = layer;
+  a.max_blocks = max_blocks_per_seq;
+  a.num_blocks = g.num_blocks;
+  a.q_dtype = q_dtype;
+  a.out_dtype = out_dtype;
+  a.kv_dtype = g.kv_dtype;
+  a.qk_scale_log2 = (float)((double)scale * 1.4426950408889634 * (fp8 ? (double)k_scale : 1.0));
+  a.v_scale = fp8 ? v_scale : 1.f;
+  if (d_workspace && !aligned16(d_workspace)) return PKV_EINVAL;
+  char* ws = static_cast<char*>(d_workspace);
+
+  if (use_mma) {
+    MmaPlan plan;
+    if (!plan_mma(g, dev, opts, &plan)) return PKV_EUNSUPPORTED;
+    a.HG = plan.HG;
+    a.NHG = plan.NHG;
+    a.stages = plan.stages;
+    const CUtensorMap* map = p->tmap(plan.HG);
+    if (!map) return PKV_ECUDA;
+    if (num_splits == 0) {
+      const BalancedWs w = balanced_ws(g, batch, plan);
+      if (!ws || ws_bytes < w.bytes) return PKV_ENOMEM;
+      a.mode = 0;
+      a.S = 0;
+      a.part_o = reinterpret_cast<float*>(ws + w.o_off);
+      a.part_lse = reinterpret_cast<float*>(ws + w.lse_off);
+      a.unit_info = reinterpret_cast<int2*>(ws + w.info_off);
+      if (phase != 2 && launch_decode_mma(map, a, plan.grid, 1, stream) != cudaSuccess)
+        return PKV_ECUDA;
+      if (phase != 1 && launch_merge_units(a, phase == 0, stream) != cudaSuccess) return PKV_ECUDA;
+      return PKV_OK;
+    }
+    size_t lse_off = 0;
+    const size_t need = fixed_ws(g, batch, num_splits, &lse_off);
+    if (num_splits > 1 && (!ws || ws_bytes < need)) return PKV_ENOMEM;
+    a.mode = 1;
+    a.S = num_splits;
+    a.part_o = num_splits > 1 ? reinterpret_cast<float*>(ws) : nullptr;
+    a.part_lse = num_splits > 1 ? reinterpret_cast<float*>(ws + lse_off) : nullptr;
+    const long long units = (long long)batch * plan.NHG;
+    if (units > 65535) return PKV_EUNSUPPORTED;
+    if (phase != 2 && launch_decode_mma(map, a, num_splits, (int)units, stream) != cudaSuccess)
+      return PKV_ECUDA;
+    if (num_splits > 1 && phase != 1 &&
+        launch_merge_rows(d_out, out_dtype, a.part_o, a.part_lse, batch * g.num_q_heads,
+                          num_splits, g.head_dim, phase == 0, stream) != cudaSuccess)
+      return PKV_ECUDA;
+    return PKV_OK;
+  }
+
+  // SIMT kernel: fixed partitions (automatic count when num_splits == 0)
+  const int S = num_splits > 0 ? num_splits : simt_auto_splits(g, batch, max_seq_len, dev.sms);
+  if (batch > 65535 || g.num_kv_heads > 65535) return PKV_EUNSUPPORTED;
+  size_t lse_off = 0;
+  const size_t need = fixed_ws(g, batch, S, &lse_off);
+  if (S > 1 && (!ws || ws_bytes < need)) return PKV_ENOMEM;
+  a.mode = 1;
+  a.S = S;
+  a.part_o = S > 1 ? reinterpret_cast<float*>(ws) : nullptr;
+  a.part_lse = S > 1 ? reinterpret_cast<float*>(ws + lse_off) : nullptr;
+  if (phase != 2 && launch_decode_simt(a, stream) != cudaSuccess) return PKV_ECUDA;
+  if (S > 1 && phase != 1 &&
+      launch_merge_rows(d_out, out_dtype, a.part_o, a.part_lse, batch * g.num_q_heads, S,
+                        g.head_dim, phase == 0, stream) != cudaSuccess)
+    return PKV_ECUDA;
+  return PKV_OK;
+}
+
+int paged_decode_attention(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_dtype q_dtype,
+                           const pkv_pool* pool, int layer, const int32_t* d_block_tables,
+                           int max_blocks_per_seq, const int32_t* d_seq_lens, int batch,
+                           int max_seq_len, float scale, float k_scale, float v_scale,
+                           int num_splits, void* d_workspace, size_t ws_bytes,
+                           cudaStream_t stream) {
+  return paged_decode_attention_ex(d_out, out_dtype, d_q, q_dtype, pool, layer, d_block_tables,
+                                   max_blocks_per_seq, d_seq_lens, batch, max_seq_len, scale,
+                                   k_scale, v_scale, num_splits, d_workspace, ws_bytes, nullptr,
+                                   stream);
+}
+
+int merge_partials(void* d_out, pkv_dtype out_dtype, const float* d_part_o,
+                   const float* d_part_lse, int batch, int num_q_heads, int head_dim,
+                   int num_splits, cudaStream_t stream) {
+  if (batch < 0 || num_q_heads < 1 || head_dim < 1 || head_dim > 256 || num_splits < 1 ||
+      !act_dtype(out_dtype))
+    return PKV_EINVAL;
+  if (batch == 0) return PKV_OK;
+  if (!d_out || !d_part_o || !d_part_lse) return PKV_EINVAL;
+  const long long rows = (long long)batch * num_q_heads;
+  if (rows > 0x7fffffffLL) return PKV_EINVAL;
+  return launch_merge_rows(d_out, out_dtype, d_part_o, d_part_lse, (int)rows, num_splits,
+                           head_dim, false, stream) == cudaSuccess
+             ? PKV_OK
+             : PKV_ECUDA;
+}
+
+int pkv_check_status(const pkv_pool* p, cudaStream_t stream) {
+  if (!p) return PKV_EINVAL;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return PKV_ECUDA;
+  if (!p->d_status) return PKV_OK;
+  int32_t w[PKV_STATUS_BYTES / 4] = {0};
+  if (cudaMemcpy(w, p->d_status, PKV_STATUS_BYTES, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return PKV_ECUDA;
+  if (w[0] != 0 && cudaMemset(p->d_status, 0, PKV_STATUS_BYTES) != cudaSuccess) return PKV_ECUDA;
+  return w[0];
+}
+
+const char* pkv_strerror(int s) {
+  switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_EINVAL: return "invalid argument";
+    case PKV_ENOMEM: return "out of blocks or workspace";
+    case PKV_ECUDA: return "CUDA runtime error";
+    case PKV_EBOUNDS: return "block id or position out of range (device)";
+    case PKV_ETIMEOUT: return "bounded wait ran out (device)";
+    case PKV_EUNSUPPORTED: return "no kernel for this combination";
+    default: return "unknown status";
+  }
+}
+
+uint64_t pkv_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

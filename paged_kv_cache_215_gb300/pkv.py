@@ -1,0 +1,269 @@
+"""Thin Python binding of the C ABI in include/pkv.h (argument marshalling only).
+
+Torch tensors provide device memory and the current CUDA stream; every step of
+the computation runs in the library's CUDA kernels.  The library must have been
+built (``paged_kv_cache_215_gb300.build.build()``); importing this module
+without it raises -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import torch
+
+from . import build as _build
+
+PKV_OK, PKV_EINVAL, PKV_ENOMEM, PKV_ECUDA, PKV_EBOUNDS, PKV_ETIMEOUT, PKV_EUNSUPPORTED = \
+    0, -1, -2, -3, -4, -5, -6
+PKV_F32, PKV_F16, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2, 3
+STATUS_BYTES = 16
+
+DTYPE_CODE = {"f32": PKV_F32, "f16": PKV_F16, "bf16": PKV_BF16, "e4m3": PKV_FP8_E4M3}
+TORCH_CODE = {torch.float32: PKV_F32, torch.float16: PKV_F16, torch.bfloat16: PKV_BF16}
+ELEM_BYTES = {PKV_F32: 4, PKV_F16: 2, PKV_BF16: 2, PKV_FP8_E4M3: 1}
+
+
+class PkvError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {strerror(code)} ({code})")
+
+
+class Geometry(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32)]
+
+
+class LaunchOpts(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
+                ("kv_heads_per_cta", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("phase", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+
+
+def _load() -> ctypes.CDLL:
+    path = _build.SO
+    if not os.path.exists(path):
+        raise ImportError(f"the CUDA library {path} is not built; run "
+                          "paged_kv_cache_215_gb300.build.build() (no CPU fallback exists)")
+    lib = ctypes.CDLL(path)
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    I64 = ctypes.c_int64
+    G = ctypes.POINTER(Geometry)
+    sig = {
+        "kv_pool_bytes": (Z, [G]),
+        "kv_pool_create": (I, [G, P, Z, P, ctypes.POINTER(P)]),
+        "kv_pool_destroy": (I, [P]),
+        "kv_pool_geometry": (I, [P, G]),
+        "kv_pool_alloc": (I, [P, I, P]),
+        "kv_pool_reserve": (I, [P, I, P]),
+        "kv_pool_free": (I, [P, I, P]),
+        "kv_pool_share": (I, [P, I, P]),
+        "kv_pool_refcount": (I, [P, ctypes.c_int32]),
+        "kv_pool_num_free": (I, [P]),
+        "kv_pool_cow": (I, [P, ctypes.c_int32, P, P]),
+        "kv_append": (I, [P, I, P, P, I, P, I, P, I, F, F, P]),
+        "kv_append_tokens": (I, [P, I, P, P, I, P, I, I, P, P, I64, F, F, P]),
+        "kv_absmax": (I, [P, I, I64, P, P]),
+        "paged_decode_workspace_bytes": (Z, [G, I, I, I]),
+        "paged_decode_attention": (I, [P, I, P, I, P, I, P, I, P, I, I, F, F, F, I, P, Z, P]),
+        "paged_decode_attention_ex": (I, [P, I, P, I, P, I, P, I, P, I, I, F, F, F, I, P, Z,
+                                          ctypes.POINTER(LaunchOpts), P]),
+        "merge_partials": (I, [P, I, P, P, I, I, I, I, P]),
+        "pkv_check_status": (I, [P, P]),
+        "pkv_strerror": (ctypes.c_char_p, [I]),
+        "pkv_launch_count": (ctypes.c_uint64, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+EXPORTS = ("kv_pool_bytes", "kv_pool_create", "kv_pool_destroy", "kv_pool_geometry",
+           "kv_pool_alloc", "kv_pool_reserve", "kv_pool_free", "kv_pool_share",
+           "kv_pool_refcount", "kv_pool_num_free", "kv_pool_cow", "kv_append",
+           "kv_append_tokens", "kv_absmax", "paged_decode_workspace_bytes",
+           "paged_decode_attention", "paged_decode_attention_ex", "merge_partials",
+           "pkv_check_status", "pkv_strerror", "pkv_launch_count")
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return _lib.pkv_strerror(code).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != PKV_OK:
+        raise PkvError(rc, what)
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    assert t.is_contiguous(), "tensors passed to the library must be contiguous"
+    return t.data_ptr()
+
+
+def _i32(x: Sequence[int]):
+    arr = (ctypes.c_int32 * len(x))(*[int(v) for v in x])
+    return arr
+
+
+def geometry(num_layers, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+             kv_dtype) -> Geometry:
+    code = DTYPE_CODE[kv_dtype] if isinstance(kv_dtype, str) else int(kv_dtype)
+    return Geometry(num_layers, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, code)
+
+
+def kv_pool_bytes(geom: Geometry) -> int:
+    return int(_lib.kv_pool_bytes(ctypes.byref(geom)))
+
+
+def launch_count() -> int:
+    return int(_lib.pkv_launch_count())
+
+
+def launch_opts(kernel=0, ctas_per_sm=0, kv_heads_per_cta=0, stages=0, phase=0) -> LaunchOpts:
+    o = LaunchOpts()
+    o.kernel, o.ctas_per_sm, o.kv_heads_per_cta, o.stages, o.phase = \
+        kernel, ctas_per_sm, kv_heads_per_cta, stages, phase
+    return o
+
+
+class KVPool:
+    """A paged KV pool: caller-owned device storage [NB, 2, L, Hkv, bs, D] plus the
+    library's host state (block allocator, TMA descriptors)."""
+
+    def __init__(self, geom: Geometry, device="cuda", storage: Optional[torch.Tensor] = None):
+        self.geom = geom
+        self.nbytes = kv_pool_bytes(geom)
+        if self.nbytes == 0:
+            raise PkvError(PKV_EINVAL, "kv_pool_bytes")
+        self.storage = storage if storage is not None else \
+            torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+        self.status = torch.zeros(STATUS_BYTES // 4, dtype=torch.int32, device=self.storage.device)
+        h = ctypes.c_void_p()
+        _check(_lib.kv_pool_create(ctypes.byref(geom), _ptr(self.storage), self.storage.numel(),
+                                   _ptr(self.status), ctypes.byref(h)), "kv_pool_create")
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None):
+            _lib.kv_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def kv_dtype(self) -> int:
+        return self.geom.kv_dtype
+
+    def view(self) -> torch.Tensor:
+        """The storage as [NB, 2, L, Hkv, bs, D] elements (uint8 for E4M3)."""
+        g = self.geom
+        dt = {PKV_F32: torch.float32, PKV_F16: torch.float16, PKV_BF16: torch.bfloat16,
+              PKV_FP8_E4M3: torch.uint8}[g.kv_dtype]
+        return self.storage.view(dt).view(g.num_blocks, 2, g.num_layers, g.num_kv_heads,
+                                          g.block_size, g.head_dim)
+
+    # ---- host block allocator
+    def alloc(self, n: int):
+        out = (ctypes.c_int32 * max(n, 1))()
+        _check(_lib.kv_pool_alloc(self.handle, n, out), "kv_pool_alloc")
+        return list(out[:n])
+
+    def reserve(self, ids):
+        _check(_lib.kv_pool_reserve(self.handle, len(ids), _i32(ids)), "kv_pool_reserve")
+
+    def free(self, ids):
+        _check(_lib.kv_pool_free(self.handle, len(ids), _i32(ids)), "kv_pool_free")
+
+    def share(self, ids):
+        _check(_lib.kv_pool_share(self.handle, len(ids), _i32(ids)), "kv_pool_share")
+
+    def refcount(self, block_id: int) -> int:
+        return int(_lib.kv_pool_refcount(self.handle, block_id))
+
+    def num_free(self) -> int:
+        return int(_lib.kv_pool_num_free(self.handle))
+
+    def cow(self, block_id: int, stream=None) -> int:
+        out = ctypes.c_int32()
+        _check(_lib.kv_pool_cow(self.handle, block_id, ctypes.byref(out), _stream(stream)),
+               "kv_pool_cow")
+        return out.value
+
+    # ---- append (reshape_and_cache)
+    def append(self, layer, k, v, tables, positions, k_scale=1.0, v_scale=1.0, stream=None):
+        _check(_lib.kv_append(self.handle, layer, _ptr(k), _ptr(v), TORCH_CODE[k.dtype],
+                              _ptr(tables), tables.shape[1], _ptr(positions), positions.shape[0],
+                              k_scale, v_scale, _stream(stream)), "kv_append")
+
+    def append_tokens(self, layer, k, v, tables, seq_ids, positions, k_scale=1.0, v_scale=1.0,
+                      stream=None):
+        _check(_lib.kv_append_tokens(self.handle, layer, _ptr(k), _ptr(v), TORCH_CODE[k.dtype],
+                                     _ptr(tables), tables.shape[1], tables.shape[0],
+                                     _ptr(seq_ids), _ptr(positions), seq_ids.shape[0], k_scale,
+                                     v_scale, _stream(stream)), "kv_append_tokens")
+
+    def check_status(self, stream=None) -> int:
+        return int(_lib.pkv_check_status(self.handle, _stream(stream)))
+
+
+def kv_absmax(x: torch.Tensor, out: torch.Tensor, stream=None):
+    _check(_lib.kv_absmax(_ptr(x), TORCH_CODE[x.dtype], x.numel(), _ptr(out), _stream(stream)),
+           "kv_absmax")
+
+
+def fp8_scale(amax: float) -> float:
+    """Per-tensor E4M3 scale: amax / 448 in fp32 (amax = 0 gives 1)."""
+    import numpy as np
+    return float(np.float32(amax) / np.float32(448.0)) if amax > 0 else 1.0
+
+
+def workspace_bytes(geom: Geometry, batch: int, max_seq_len: int, num_splits: int = 0) -> int:
+    return int(_lib.paged_decode_workspace_bytes(ctypes.byref(geom), batch, max_seq_len,
+                                                 num_splits))
+
+
+def paged_decode_attention(out, q, pool: KVPool, layer, tables, seq_lens, max_seq_len, scale,
+                           k_scale=1.0, v_scale=1.0, num_splits=0, workspace=None, opts=None,
+                           stream=None):
+    if workspace is None:
+        nb = workspace_bytes(pool.geom, q.shape[0], max_seq_len, num_splits)
+        workspace = torch.empty(max(nb, 16), dtype=torch.uint8, device=q.device)
+    args = (_ptr(out), TORCH_CODE[out.dtype], _ptr(q), TORCH_CODE[q.dtype], pool.handle, layer,
+            _ptr(tables), tables.shape[1], _ptr(seq_lens), q.shape[0], max_seq_len, scale,
+            k_scale, v_scale, num_splits, _ptr(workspace), workspace.numel())
+    if opts is None:
+        rc = _lib.paged_decode_attention(*args, _stream(stream))
+    else:
+        rc = _lib.paged_decode_attention_ex(*args, ctypes.byref(opts), _stream(stream))
+    _check(rc, "paged_decode_attention")
+    return out
+
+
+def merge_partials(out, part_o, part_lse, stream=None):
+    B, H, S, D = part_o.shape
+    _check(_lib.merge_partials(_ptr(out), TORCH_CODE[out.dtype], _ptr(part_o), _ptr(part_lse),
+                               B, H, D, S, _stream(stream)), "merge_partials")
+    return out

@@ -193,7 +193,7 @@ class Tensors:
     q: torch.Tensor             # [B, Hq, D]
     k_new: torch.Tensor         # [B, Hkv, D] the last token of every sequence
     v_new: torch.Tensor
-    new_pos: torch.Tensor       # [B] int32 = seq_lens - 1
+    new_pos: torch.Tensor       # [B] int32 = seq_lens - 1 (-1: an empty sequence, nothing to append)
 
 
 def make_tensors(case: Case, device="cpu") -> Tensors:
@@ -233,14 +233,20 @@ def make_tensors(case: Case, device="cpu") -> Tensors:
     v_all = v_all.to(store)
     qdt = TORCH_DT[case.q_dtype]
     q = torch.randn((B, Hq, D), generator=g, device=dev).to(qdt)
-    last = (starts[1:] - 1).to(dev)
+    nonempty = lens > 0
+    last = (starts[1:] - 1).clamp(min=0).to(dev)
     keep = torch.ones(T_all, dtype=torch.bool, device=dev)
-    keep[last] = False
+    keep[last[nonempty.to(dev)]] = False
+    k_new = torch.zeros((B, Hkv, D), dtype=store, device=dev)
+    v_new = torch.zeros((B, Hkv, D), dtype=store, device=dev)
+    if T_all:
+        ne = nonempty.to(dev)
+        k_new[ne] = k_all[last[ne]]
+        v_new[ne] = v_all[last[ne]]
     return Tensors(k_tokens=k_all[keep].contiguous(), v_tokens=v_all[keep].contiguous(),
                    tok_seq=seq_of[keep].to(torch.int32).contiguous(),
                    tok_pos=pos_of[keep].to(torch.int32).contiguous(),
-                   q=q.contiguous(), k_new=k_all[last].contiguous(),
-                   v_new=v_all[last].contiguous(),
+                   q=q.contiguous(), k_new=k_new.contiguous(), v_new=v_new.contiguous(),
                    new_pos=(lens - 1).to(torch.int32).to(dev).contiguous())
 
 

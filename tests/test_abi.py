@@ -1,0 +1,151 @@
+"""C-ABI library checks that need no GPU: it builds, loads, exports every
+symbol include/pkv.h declares, sizes pools by the pages' formula, runs the host
+block allocator, and rejects bad arguments before any device work."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+from paged_kv_cache_215_gb300 import build as pkv_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    pkv_build.build()
+    from paged_kv_cache_215_gb300 import pkv as mod
+    return mod
+
+
+def test_library_exports_every_declared_symbol(pkv):
+    hdr = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    declared = set(re.findall(r"PKV_API\s+[\w\s\*]+?\b(\w+)\s*\(", hdr))
+    assert len(declared) >= 20
+    lib = ctypes.CDLL(pkv_build.SO)
+    for name in sorted(declared):
+        assert hasattr(lib, name), name
+    assert declared == set(pkv.EXPORTS)
+
+
+def test_pool_bytes_is_the_pages_formula(pkv):
+    for (L, hq, hkv, D, bs, nb, dt, eb) in [(1, 32, 8, 128, 16, 9012, "bf16", 2),
+                                            (80, 64, 8, 128, 32, 7, "f16", 2),
+                                            (2, 4, 2, 64, 16, 32, "f32", 4),
+                                            (1, 32, 8, 128, 16, 1000, "e4m3", 1)]:
+        g = pkv.geometry(L, hq, hkv, D, bs, nb, dt)
+        assert pkv.kv_pool_bytes(g) == oracle.kv_bytes(L, hkv, D, nb * bs, eb)
+    assert pkv.kv_pool_bytes(pkv.geometry(1, 3, 2, 128, 16, 10, "bf16")) == 0   # 3 % 2 != 0
+    assert pkv.kv_pool_bytes(pkv.geometry(1, 2, 2, 100, 16, 10, "bf16")) == 0   # D % 8 != 0
+
+
+class FakePool:
+    """A pool whose device pointer is never dereferenced (allocator only)."""
+
+    def __init__(self, pkv, nb=10):
+        self.pkv = pkv
+        self.g = pkv.geometry(1, 4, 2, 64, 16, nb, "bf16")
+        h = ctypes.c_void_p()
+        rc = pkv.lib().kv_pool_create(ctypes.byref(self.g), ctypes.c_void_p(1 << 20),
+                                      pkv.kv_pool_bytes(self.g), None, ctypes.byref(h))
+        assert rc == 0
+        self.h = h
+
+    def alloc(self, n):
+        out = (ctypes.c_int32 * max(n, 1))()
+        rc = self.pkv.lib().kv_pool_alloc(self.h, n, out)
+        return rc, list(out[:n])
+
+    def call(self, name, ids):
+        arr = (ctypes.c_int32 * max(len(ids), 1))(*ids)
+        return getattr(self.pkv.lib(), name)(self.h, len(ids), arr)
+
+    def ref(self, i):
+        return self.pkv.lib().kv_pool_refcount(self.h, i)
+
+    def nfree(self):
+        return self.pkv.lib().kv_pool_num_free(self.h)
+
+    def close(self):
+        self.pkv.lib().kv_pool_destroy(self.h)
+
+
+def test_allocator_all_or_nothing(pkv):
+    p = FakePool(pkv, nb=10)
+    rc, ids = p.alloc(4)
+    assert rc == 0 and len(set(ids)) == 4 and p.nfree() == 6
+    rc, _ = p.alloc(7)
+    assert rc == pkv.PKV_ENOMEM and p.nfree() == 6          # nothing taken
+    rc, more = p.alloc(6)
+    assert rc == 0 and p.nfree() == 0 and not set(more) & set(ids)
+    assert p.call("kv_pool_free", ids + more) == 0 and p.nfree() == 10
+    assert all(p.ref(i) == 0 for i in range(10))
+    p.close()
+
+
+def test_allocator_refcounts_share_and_free(pkv):
+    p = FakePool(pkv, nb=6)
+    _, ids = p.alloc(2)
+    assert p.call("kv_pool_share", ids) == 0 and p.call("kv_pool_share", ids[:1]) == 0
+    assert p.ref(ids[0]) == 3 and p.ref(ids[1]) == 2
+    assert p.call("kv_pool_free", ids) == 0
+    assert p.ref(ids[0]) == 2 and p.ref(ids[1]) == 1 and p.nfree() == 4
+    # freeing more references than exist fails and changes nothing
+    assert p.call("kv_pool_free", [ids[1], ids[1]]) == pkv.PKV_EINVAL and p.ref(ids[1]) == 1
+    assert p.call("kv_pool_free", [ids[1]]) == 0 and p.nfree() == 5
+    assert p.call("kv_pool_share", [ids[1]]) == pkv.PKV_EINVAL     # sharing a free block
+    p.close()
+
+
+def test_allocator_reserve(pkv):
+    p = FakePool(pkv, nb=8)
+    assert p.call("kv_pool_reserve", [5, 2, 7]) == 0
+    assert [p.ref(i) for i in range(8)] == [0, 0, 1, 0, 0, 1, 0, 1]
+    assert p.call("kv_pool_reserve", [1, 2]) == pkv.PKV_EINVAL      # 2 is taken
+    assert p.call("kv_pool_reserve", [1, 1]) == pkv.PKV_EINVAL      # repeated
+    assert p.call("kv_pool_reserve", [8]) == pkv.PKV_EINVAL         # out of range
+    assert p.ref(1) == 0 and p.nfree() == 5
+    rc, ids = p.alloc(5)
+    assert rc == 0 and sorted(ids) == [0, 1, 3, 4, 6]
+    p.close()
+
+
+def test_decode_rejects_bad_arguments_before_device_work(pkv):
+    p = FakePool(pkv, nb=8)
+    L = pkv.lib()
+    x = ctypes.c_void_p(1 << 20)
+    common = dict(out=x, od=pkv.PKV_BF16, q=x, qd=pkv.PKV_BF16, layer=0, tab=x, mb=4, lens=x,
+                  B=2, maxlen=64, scale=0.125, ks=1.0, vs=1.0, S=0, ws=x, wsb=1 << 20)
+
+    def call(**kw):
+        a = dict(common, **kw)
+        return L.paged_decode_attention(a["out"], a["od"], a["q"], a["qd"], p.h, a["layer"],
+                                        a["tab"], a["mb"], a["lens"], a["B"], a["maxlen"],
+                                        a["scale"], a["ks"], a["vs"], a["S"], a["ws"], a["wsb"],
+                                        None)
+    assert call(B=0) == 0                                  # empty batch: no-op
+    assert call(layer=1) == pkv.PKV_EINVAL                 # layer out of range
+    assert call(B=-1) == pkv.PKV_EINVAL
+    assert call(maxlen=65) == pkv.PKV_EINVAL               # longer than the table holds
+    assert call(od=pkv.PKV_FP8_E4M3) == pkv.PKV_EINVAL     # out dtype
+    assert call(q=ctypes.c_void_p((1 << 20) + 2)) == pkv.PKV_EINVAL   # misaligned q
+    assert call(tab=None) == pkv.PKV_EINVAL
+    assert call(S=-2) == pkv.PKV_EINVAL
+    p.close()
+
+
+def test_append_rejects_dtype_mismatch(pkv):
+    p = FakePool(pkv, nb=8)
+    x = ctypes.c_void_p(1 << 20)
+    rc = pkv.lib().kv_append(p.h, 0, x, x, pkv.PKV_F32, x, 4, x, 2, 1.0, 1.0, None)
+    assert rc == pkv.PKV_EINVAL                            # f32 into a bf16 pool
+    rc = pkv.lib().kv_append(p.h, 3, x, x, pkv.PKV_BF16, x, 4, x, 2, 1.0, 1.0, None)
+    assert rc == pkv.PKV_EINVAL                            # layer
+    p.close()
+
+
+def test_strerror_names_every_status(pkv):
+    names = {pkv.strerror(c) for c in range(-6, 1)}
+    assert len(names) == 7 and "unknown status" not in names
