@@ -1,0 +1,66 @@
+"""Parity at the full workload sizes the benchmark times (needs a GPU).
+
+The GPU runs the whole batch in the benchmark's launch configuration
+(automatic split, bf16 and fp32 output); the oracle builds its own pool for a
+sample of sequences (through its own append) and computes every query head of
+those sequences in fp64.  Bounds as in test_gpu_parity: max |err| <= 2e-3 x
+max|V| (bf16 KV), 5e-3 x max|V| (E4M3 KV), plus half an output ulp for bf16
+output; the sampled part of the pool must equal the oracle's byte for byte.
+"""
+import gc as _gc
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_215_gb300 import workloads as wl
+from tests.gpu_harness import GpuCase, assert_parity, oracle_side
+
+pytestmark = pytest.mark.gpu
+
+
+def _extremes(case, k=3):
+    order = np.argsort(case.seq_lens)
+    return sorted({int(order[0]), int(order[len(order) // 2]), int(order[-1])})[:k]
+
+
+SAMPLES = {
+    "llama8b_b32_8k": lambda c: [0, 13, 31],
+    "long_128k": lambda c: [0],
+    "long_1m": lambda c: [0],
+    "fp8_b8_32k": lambda c: [0, 7],
+    "llama70b_prefix_bs16": _extremes,
+    "llama70b_prefix_bs32": _extremes,
+}
+
+
+@pytest.mark.parametrize("name", list(SAMPLES))
+def test_full_size_sampled_parity(name):
+    case = wl.FULL[name]()
+    tens = wl.make_tensors(case, device="cuda")
+    g = GpuCase(case, tens)
+    out_lo = g.step(out_dtype=case.out_dtype)          # the benchmark's output dtype
+    out_32 = g.step(out_dtype="f32", append=False)
+    torch.cuda.synchronize()
+    assert g.status() == 0
+    seqs = SAMPLES[name](case)
+    pool, ref, seqs = oracle_side(case, tens, seqs, g.k_scale, g.v_scale)
+    # the sampled sequences' blocks hold exactly the oracle's bytes
+    gpu_pool = g.pool.view().cpu()
+    ora_pool = torch.from_numpy(pool).view(gpu_pool.dtype).view(gpu_pool.shape)
+    for s in seqs:
+        n = int(case.seq_lens[s])
+        blocks = torch.from_numpy(case.tables[s, :(n + case.block_size - 1) // case.block_size]
+                                  .astype(np.int64))
+        a, b = gpu_pool[blocks], ora_pool[blocks]          # [nb, 2, L, Hkv, bs, D]
+        # token order is (block, slot): only the n slots the sequence uses are compared
+        a = a.permute(0, 4, 1, 2, 3, 5).reshape(-1, *a.shape[1:4], a.shape[5])[:n].contiguous()
+        b = b.permute(0, 4, 1, 2, 3, 5).reshape(-1, *b.shape[1:4], b.shape[5])[:n].contiguous()
+        if a.element_size() == 2:
+            a, b = a.view(torch.int16), b.view(torch.int16)
+        assert torch.equal(a, b), f"pool bytes of sequence {s} differ"
+    assert_parity(case, out_32, ref, pool, seqs, g.v_scale, name)
+    assert_parity(case, out_lo, ref, pool, seqs, g.v_scale, name, out_dtype=case.out_dtype)
+    del g, tens, pool
+    _gc.collect()
+    torch.cuda.empty_cache()
