@@ -227,6 +227,36 @@ PKV_API int merge_partials(void* d_out, pkv_dtype out_dtype, const float* d_part
                            const float* d_part_lse, int batch, int num_q_heads, int head_dim,
                            int num_splits, cudaStream_t stream);
 
+/* ---------------------------------------------------------------- decode without a workspace */
+
+/* Size of the library's built-in scratch array used by
+ * paged_decode_attention_static (16 MiB per GPU that loads the library). */
+#define PKV_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/* paged_decode_attention for callers that cannot allocate device memory when
+ * they run it (an allocator frozen during graph capture, a plugin that only
+ * receives its input and output buffers, a loop that must not allocate after
+ * start-up).  The source pages have no counterpart: this is an interface
+ * convenience of this library.
+ * Same arguments and result as paged_decode_attention, minus the workspace:
+ * the partial results live in a fixed array inside the library
+ * (PKV_STATIC_SCRATCH_BYTES), so the call allocates nothing.
+ *   - Returns PKV_ENOMEM, launching nothing, if the workspace this call's
+ *     launch plan needs is larger than the array (paged_decode_workspace_bytes
+ *     is an upper bound of that need).
+ *   - Every call on a device shares the array and the array keeps what the last
+ *     call left; no part of it needs to start at zero.  Calls whose kernels may
+ *     overlap on the GPU (unordered streams) race on it and must be serialised.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture. */
+PKV_API int paged_decode_attention_static(void* d_out, pkv_dtype out_dtype, const void* d_q,
+                                          pkv_dtype q_dtype, const pkv_pool* pool, int layer,
+                                          const int32_t* d_block_tables, int max_blocks_per_seq,
+                                          const int32_t* d_seq_lens, int batch, int max_seq_len,
+                                          float scale, float k_scale, float v_scale,
+                                          int num_splits, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- status */
 
 /* Synchronise `stream`, read and clear the pool's device status word and

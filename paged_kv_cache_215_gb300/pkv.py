@@ -74,6 +74,7 @@ def _load() -> ctypes.CDLL:
         "paged_decode_attention_ex": (I, [P, I, P, I, P, I, P, I, P, I, I, F, F, F, I, P, Z,
                                           ctypes.POINTER(LaunchOpts), P]),
         "merge_partials": (I, [P, I, P, P, I, I, I, I, P]),
+        "paged_decode_attention_static": (I, [P, I, P, I, P, I, P, I, P, I, I, F, F, F, I, P]),
         "pkv_check_status": (I, [P, P]),
         "pkv_strerror": (ctypes.c_char_p, [I]),
         "pkv_launch_count": (ctypes.c_uint64, []),
@@ -91,6 +92,7 @@ EXPORTS = ("kv_pool_bytes", "kv_pool_create", "kv_pool_destroy", "kv_pool_geomet
            "kv_pool_refcount", "kv_pool_num_free", "kv_pool_cow", "kv_append",
            "kv_append_tokens", "kv_absmax", "paged_decode_workspace_bytes",
            "paged_decode_attention", "paged_decode_attention_ex", "merge_partials",
+           "paged_decode_attention_static",
            "pkv_check_status", "pkv_strerror", "pkv_launch_count")
 
 
@@ -259,6 +261,17 @@ def paged_decode_attention(out, q, pool: KVPool, layer, tables, seq_lens, max_se
     else:
         rc = _lib.paged_decode_attention_ex(*args, ctypes.byref(opts), _stream(stream))
     _check(rc, "paged_decode_attention")
+    return out
+
+
+def paged_decode_attention_static(out, q, pool: KVPool, layer, tables, seq_lens, max_seq_len,
+                                  scale, k_scale=1.0, v_scale=1.0, num_splits=0, stream=None):
+    """paged_decode_attention without a workspace argument: the library's built-in
+    scratch array holds the partial results (see include/pkv.h)."""
+    _check(_lib.paged_decode_attention_static(
+        _ptr(out), TORCH_CODE[out.dtype], _ptr(q), TORCH_CODE[q.dtype], pool.handle, layer,
+        _ptr(tables), tables.shape[1], _ptr(seq_lens), q.shape[0], max_seq_len, scale, k_scale,
+        v_scale, num_splits, _stream(stream)), "paged_decode_attention_static")
     return out
 
 
