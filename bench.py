@@ -139,12 +139,14 @@ def kv_bytes(case):
 
 
 def algorithmic_attn_bytes(case):
-    """What one attention launch must move: every cached K/V element once, q in,
-    out, and the table entries it follows."""
+    """What one decode-step attention launch must move: every cached K/V element
+    once, q in, out, the table entries it follows, and the new token's k/v in and
+    stored."""
     q = case.batch * case.num_q_heads * case.head_dim * 2
     out = case.batch * case.num_q_heads * case.head_dim * 2
     tables = sum((int(n) + case.block_size - 1) // case.block_size for n in case.seq_lens) * 4
-    return kv_bytes(case) + q + out + tables
+    new = case.batch * 2 * case.num_kv_heads * case.head_dim * (2 + case.kv_elem_bytes())
+    return kv_bytes(case) + q + out + tables + new
 
 
 def unique_kv_bytes(case):
@@ -199,55 +201,81 @@ class Workload:
         self.o_merge = pkv.launch_opts(phase=2)
         torch.cuda.synchronize()
 
-    def append(self, k=None, v=None, pos=None):
-        t = self.tens
-        self.pool.append(self.case.layer, t.k_new if k is None else k, t.v_new if v is None else v,
-                         self.tables, t.new_pos if pos is None else pos, self.ks, self.vs)
-
-    def attention(self, opts=None, q=None, seq_lens=None, out=None):
+    def step(self, opts=None, q=None, k=None, v=None, seq_lens=None):
+        """One decode step: store every sequence's new token and attend (one attention
+        launch with the store fused in, plus the merge)."""
         c = self.case
-        self.pkv.paged_decode_attention(self.out if out is None else out,
-                                        self.tens.q if q is None else q, self.pool, c.layer,
-                                        self.tables, self.seq_lens if seq_lens is None else seq_lens,
-                                        self.max_len, c.scale, self.ks, self.vs, 0, self.ws, opts)
+        t = self.tens
+        self.pkv.paged_decode_step(self.out, t.q if q is None else q, t.k_new if k is None else k,
+                                   t.v_new if v is None else v, self.pool, c.layer, self.tables,
+                                   self.seq_lens if seq_lens is None else seq_lens, self.max_len,
+                                   c.scale, self.ks, self.vs, 0, self.ws, opts)
 
     def close(self):
         self.pool.close()
 
 
-def time_steps(w, steps, warmup, split_phases):
-    """Run warm-up then `steps` timed steps; returns (total ms, per-step attention ms list)."""
+def time_steps(w, steps, warmup, split_phases=False, graph_chunk=0):
+    """Warm-up, then `steps` timed decode steps on the current stream.
+
+    split_phases: launch the attention kernel (phase 1) and the merge (phase 2)
+    separately, with events around each attention launch (for the roofline).
+    graph_chunk > 0: capture that many consecutive steps (chained with
+    programmatic dependent launch) in one CUDA graph and replay it.
+    Returns (total ms, per-step attention ms list, launches per step)."""
+    from paged_kv_cache_215_gb300 import pkv
     stream = torch.cuda.current_stream()
+    pdl = pkv.launch_opts(pdl=1)
     for _ in range(warmup):
-        w.append()
-        w.attention()
+        w.step(pdl)
     torch.cuda.synchronize()
+    n0 = pkv.launch_count()
+    w.step(pdl)
+    torch.cuda.synchronize()
+    per_step = pkv.launch_count() - n0
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps if split_phases else 0)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if graph_chunk:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            w.step(pdl)                     # first call outside capture (one-time set-up)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            for _ in range(graph_chunk):
+                w.step(pdl)
+        reps = max(1, steps // graph_chunk)
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(reps):
+            g.replay()
+        end.record(stream)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) * steps / (reps * graph_chunk), [], per_step
     start.record(stream)
     for i in range(steps):
-        w.append()
         if split_phases:
             ev[i][0].record(stream)
-            w.attention(w.o_attn)
+            w.step(w.o_attn)
             ev[i][1].record(stream)
-            w.attention(w.o_merge)
+            w.step(w.o_merge)
         else:
-            w.attention()
+            w.step(pdl)
     end.record(stream)
     torch.cuda.synchronize()
-    total = start.elapsed_time(end)
-    attn = [a.elapsed_time(b) for a, b in ev]
-    return total, attn
+    return start.elapsed_time(end), [a.elapsed_time(b) for a, b in ev], per_step
 
 
 def time_e2e(w, steps, warmup):
-    """Through the C ABI from pinned host buffers: per step copy q, k_new, v_new,
-    positions and lengths host->device, append, attend, copy out device->host."""
+    """Through the C ABI from pinned host buffers: per step copy q, the new k and v
+    and the lengths host->device, run the decode step, copy out device->host."""
     c = w.case
     t = w.tens
-    host = {k: getattr(t, k).cpu().pin_memory() for k in ("q", "k_new", "v_new", "new_pos")}
+    host = {k: getattr(t, k).cpu().pin_memory() for k in ("q", "k_new", "v_new")}
     host["seq_lens"] = torch.from_numpy(c.seq_lens).pin_memory()
     dev = {k: torch.empty_like(v, device="cuda") for k, v in host.items()}
     out_h = torch.empty(w.out.shape, dtype=w.out.dtype).pin_memory()
@@ -258,8 +286,7 @@ def time_e2e(w, steps, warmup):
     def step():
         for k in host:
             dev[k].copy_(host[k], non_blocking=True)
-        w.append(dev["k_new"], dev["v_new"], dev["new_pos"])
-        w.attention(q=dev["q"], seq_lens=dev["seq_lens"])
+        w.step(None, q=dev["q"], k=dev["k_new"], v=dev["v_new"], seq_lens=dev["seq_lens"])
         out_h.copy_(w.out, non_blocking=True)
 
     for _ in range(warmup):
@@ -293,8 +320,8 @@ def cpu_baseline(w, budget_s=15.0):
     rows_all = c.batch * c.num_q_heads
     per_row_bytes = kv_bytes(c) / rows_all
     done_rows, spent, n = 0, 0.0, max(1, oracle.num_threads())
-    while spent < budget_s and done_rows < rows_all:
-        rows = np.arange(done_rows, min(rows_all, done_rows + n), dtype=np.int32)
+    while spent < budget_s:
+        rows = (np.arange(done_rows, done_rows + n) % rows_all).astype(np.int32)
         t0 = time.perf_counter()
         oracle.decode(q, c.q_dtype, pool, c.kv_dtype, c.geometry, c.layer, c.tables, c.seq_lens,
                       c.scale, w.ks, w.vs, rows=rows)
@@ -302,48 +329,54 @@ def cpu_baseline(w, budget_s=15.0):
         done_rows += rows.size
     gbs = done_rows * per_row_bytes / spent / 1e9
     return {"value": gbs, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{done_rows} of {rows_all} (sequence, query head) rows of the same "
-                      f"workload, fp64, {spent:.1f} s; GB/s counts each row's share of the "
-                      f"KV bytes"}
+            "sample": f"{done_rows} (sequence, query head) rows (the workload has {rows_all}), "
+                      f"fp64, {spent:.1f} s; GB/s counts each row's share of the KV bytes"}
 
 
-def measure(name, steps, warmup, device, with_clocks=False, gpu_index=0, e2e=True):
-    from paged_kv_cache_215_gb300 import pkv
+def measure(name, steps, warmup, device, with_clocks=False, gpu_index=0, e2e=True, graph=True):
     w = Workload(name, device)
     c = w.case
     peak, peak_kind = peaks()
     sampler = ClockSampler(gpu_index) if with_clocks else None
-    # headline: the production path (attention + merge chained with PDL)
+    # headline: the production step -- fused store + attention, then the merge,
+    # consecutive steps chained with programmatic dependent launch
     if sampler:
         sampler.start()
-    n0 = pkv.launch_count()
-    total_ms, _ = time_steps(w, steps, warmup, split_phases=False)
-    launches = pkv.launch_count() - n0 - 3 * warmup
+    eager_ms, _, per_step = time_steps(w, steps, warmup)
+    graph_ms = time_steps(w, steps, 3, graph_chunk=10)[0] if graph else None
     clocks = sampler.stop() if sampler else None
     # the attention kernel alone, timed per launch with events on its stream
-    _, attn = time_steps(w, steps, 3, split_phases=True)
-    ms = total_ms / steps
+    _, attn, _ = time_steps(w, steps, 3, split_phases=True)
+    eager = eager_ms / steps
+    gstep = graph_ms / steps if graph_ms else None
+    ms = min(eager, gstep) if gstep else eager
     attn_ms = float(np.mean(attn))
+    alg = algorithmic_attn_bytes(c)
     res = {
         "ms_per_step": ms,
+        "ms_per_step_eager": eager,
+        "ms_per_step_graph": gstep,
+        "timing": "cuda-graph replay of 10-step chunks" if (gstep and gstep <= eager)
+                  else "eager launches",
         "kv_bytes": kv_bytes(c),
         "kv_gbs": kv_bytes(c) / (ms * 1e-3) / 1e9,
         "attn_kernel_us": attn_ms * 1e3,
         "attn_kernel_p10_p90_us": [float(np.percentile(attn, 10)) * 1e3,
                                    float(np.percentile(attn, 90)) * 1e3],
-        "algorithmic_bytes": algorithmic_attn_bytes(c),
+        "algorithmic_bytes": alg,
         "roofline": {
             "bound": "hbm",
-            "achieved": algorithmic_attn_bytes(c) / (attn_ms * 1e-3) / 1e9,
+            "achieved": alg / (attn_ms * 1e-3) / 1e9,
             "peak": peak, "unit": "GB/s",
-            "frac": algorithmic_attn_bytes(c) / (attn_ms * 1e-3) / 1e9 / peak,
+            "frac": alg / (attn_ms * 1e-3) / 1e9 / peak,
             "traffic": profiled_traffic(name),
             "peak_kind": peak_kind,
         },
         "tokens_per_s_per_layer": c.batch / (ms * 1e-3),
         "decode_tokens_per_s_model": c.batch / (ms * 1e-3 * MODEL_LAYERS[name]),
         "model_layers": MODEL_LAYERS[name],
-        "gpu_launches": launches,
+        "gpu_launches": per_step * steps,
+        "launches_per_step": per_step,
         "clocks": clocks,
         "batch": c.batch,
         "seq_len_max": int(c.seq_lens.max()),
@@ -394,7 +427,8 @@ def run_ours(args):
             ow.close()
             del ow
             torch.cuda.empty_cache()
-            others[other] = {k: ores[k] for k in ("ms_per_step", "kv_gbs", "attn_kernel_us",
+            others[other] = {k: ores[k] for k in ("ms_per_step", "ms_per_step_eager",
+                                                  "ms_per_step_graph", "kv_gbs", "attn_kernel_us",
                                                   "tokens_per_s_per_layer",
                                                   "decode_tokens_per_s_model", "batch",
                                                   "block_waste")}
@@ -421,6 +455,10 @@ def run_ours(args):
         "decode_tokens_per_s_per_layer": res["tokens_per_s_per_layer"],
         "roofline": res["roofline"],
         "attn_kernel_us": res["attn_kernel_us"],
+        "ms_per_step_eager": res["ms_per_step_eager"],
+        "ms_per_step_graph": res["ms_per_step_graph"],
+        "timing": res["timing"],
+        "launches_per_step": res["launches_per_step"],
         "e2e": res["e2e"],
         "gpu_launches": res["gpu_launches"],
         "clocks": res["clocks"],

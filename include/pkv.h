@@ -200,7 +200,13 @@ typedef struct {
   int32_t kv_heads_per_cta;/* 0 auto */
   int32_t stages;          /* 0 auto; shared-memory pipeline depth */
   int32_t phase;           /* 0 attention then merge, 1 attention only, 2 merge only */
-  int32_t reserved[3];
+  int32_t pdl;             /* 1: launch the attention kernel with programmatic dependent
+                              launch, so its start-up overlaps the kernel before it in the
+                              stream.  Only valid when that kernel writes none of q, the
+                              block tables, seq_lens, the pool or k/v_new (for example the
+                              previous decode step's merge); every write to out, the
+                              workspace and the pool still waits for it. */
+  int32_t reserved[2];
 } pkv_launch_opts;
 
 /* paged_decode_attention with forced launch choices.  phase 1 and 2 split the
@@ -213,6 +219,24 @@ PKV_API int paged_decode_attention_ex(void* d_out, pkv_dtype out_dtype, const vo
                                       float scale, float k_scale, float v_scale, int num_splits,
                                       void* d_workspace, size_t ws_bytes,
                                       const pkv_launch_opts* opts, cudaStream_t stream);
+
+/* One decode step for one layer: for every sequence s with n = d_seq_lens[s] >= 1
+ * tokens (counting the new one), store the new token's d_k_new[s] / d_v_new[s]
+ * ([batch, num_kv_heads, head_dim] in new_dtype) at position n - 1 exactly as
+ * kv_append does ([ENG26] 2.2, [UNLOCK] 3.2), then compute
+ * paged_decode_attention over the n tokens.  On the tensor-core kernel the store
+ * is fused into the attention launch: the CTA that reads a sequence's last block
+ * writes the token into it just before loading it, so the step is one attention
+ * launch plus the merge.  The slot written must not be shared with another
+ * sequence (copy it with kv_pool_cow first).  Other arguments and errors as in
+ * paged_decode_attention_ex. */
+PKV_API int paged_decode_step(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_dtype q_dtype,
+                              const void* d_k_new, const void* d_v_new, pkv_dtype new_dtype,
+                              const pkv_pool* pool, int layer, const int32_t* d_block_tables,
+                              int max_blocks_per_seq, const int32_t* d_seq_lens, int batch,
+                              int max_seq_len, float scale, float k_scale, float v_scale,
+                              int num_splits, void* d_workspace, size_t ws_bytes,
+                              const pkv_launch_opts* opts, cudaStream_t stream);
 
 /* Log-sum-exp merge of partial results ([SEQPAR] incremental softmax,
  * [ENG26] 3.1): for each row r = (s, h) of batch x num_q_heads,

@@ -20,31 +20,6 @@
 namespace pkv {
 namespace {
 
-template <int IN>
-__device__ __forceinline__ void load8(const void* src, size_t idx, float (&x)[8]) {
-  if constexpr (IN == PKV_F32) {
-    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(src) + idx);
-    const float4 a = p[0], b = p[1];
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-  } else {
-    const uint4 r = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + idx);
-    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = unpack2<IN == PKV_BF16>(w[i]);
-      x[2 * i] = f.x;
-      x[2 * i + 1] = f.y;
-    }
-  }
-}
-
-__device__ __forceinline__ uint8_t encode_e4m3(float x, float scale) {
-  const float y = __fdiv_rn(x, scale);
-  if (isnan(y)) return 0x7F;
-  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3));
-}
-
 template <int IN, int KV>
 __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
   const int per_row = a.D / 8;
@@ -58,9 +33,13 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
     const int kv = (int)(r % 2);
     const long long tok = r / 2;
     const int s = a.seq_ids ? __ldg(a.seq_ids + tok) : (int)tok;
-    const int pos = __ldg(a.positions + tok);
+    if (s < 0 || s >= a.B) {
+      record_error(a.status, PKV_EBOUNDS);
+      continue;
+    }
+    const int pos = a.positions ? __ldg(a.positions + tok) : __ldg(a.seq_lens + s) - 1;
     if (pos < 0) continue;   // padding: no token for this sequence
-    if (s < 0 || s >= a.B || pos / a.BS >= a.max_blocks) {
+    if (pos / a.BS >= a.max_blocks) {
       record_error(a.status, PKV_EBOUNDS);
       continue;
     }
@@ -74,26 +53,7 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
         (((((size_t)blk * 2 + kv) * a.L + a.layer) * a.Hkv + h) * a.BS + pos % a.BS) * a.D +
         (size_t)d8 * 8;
     const void* in = kv ? a.v : a.k;
-    if constexpr (KV == PKV_FP8_E4M3) {
-      float x[8];
-      load8<IN>(in, src, x);
-      const float sc = kv ? a.v_scale : a.k_scale;
-      uint32_t lo = 0, hi = 0;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        lo |= static_cast<uint32_t>(encode_e4m3(x[e], sc)) << (8 * e);
-        hi |= static_cast<uint32_t>(encode_e4m3(x[4 + e], sc)) << (8 * e);
-      }
-      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(a.pool) + dst) = make_uint2(lo, hi);
-    } else if constexpr (KV == PKV_F32) {
-      const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(in) + src);
-      float4* q = reinterpret_cast<float4*>(static_cast<float*>(a.pool) + dst);
-      q[0] = p[0];
-      q[1] = p[1];
-    } else {
-      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.pool) + dst) =
-          *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(in) + src);
-    }
+    store8_to_pool(a.pool, dst, KV, in, src, IN, kv ? a.v_scale : a.k_scale);
   }
 }
 

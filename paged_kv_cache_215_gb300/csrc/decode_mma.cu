@@ -192,12 +192,13 @@ struct Consumer {
           const uint32_t addr = kbase + row * kLineBytes + ((chunk ^ sw) << 4);
           uint32_t r0, r1, r2, r3;
           ldsm_x4(addr, r0, r1, r2, r3);
-          mma_16816<false>(e, e4m3x2_to_f16x2(r0 & 0xffff), e4m3x2_to_f16x2(r1 & 0xffff),
-                           e4m3x2_to_f16x2(r0 >> 16), e4m3x2_to_f16x2(r1 >> 16),
-                           qf[2 * jp][0], qf[2 * jp][1]);
-          mma_16816<false>(o, e4m3x2_to_f16x2(r2 & 0xffff), e4m3x2_to_f16x2(r3 & 0xffff),
-                           e4m3x2_to_f16x2(r2 >> 16), e4m3x2_to_f16x2(r3 >> 16),
-                           qf[2 * jp + 1][0], qf[2 * jp + 1][1]);
+          uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+          e4m3x4_to_f16x2x2(r0, a0, a2);
+          e4m3x4_to_f16x2x2(r1, a1, a3);
+          e4m3x4_to_f16x2x2(r2, b0, b2);
+          e4m3x4_to_f16x2x2(r3, b1, b3);
+          mma_16816<false>(e, a0, a1, a2, a3, qf[2 * jp][0], qf[2 * jp][1]);
+          mma_16816<false>(o, b0, b1, b2, b3, qf[2 * jp + 1][0], qf[2 * jp + 1][1]);
         }
       }
 #pragma unroll
@@ -264,13 +265,18 @@ struct Consumer {
     }
 
     // ---- O^T += V^T P^T
+    // Rows of V past the sequence's end are unwritten slots: their lanes are
+    // zeroed (only in a tail block) so that 0 * NaN never reaches the sum.
+    const bool tail = valid < BS;
 #pragma unroll
     for (int mt = 0; mt < kTiles; ++mt) {
       // tokens of this thread in the A fragment: 2c, 2c+1 (regs 0,1) and 8+2c, 9+2c (regs 2,3)
-      const int tl = mt * 16 + 2 * c;
-      const uint32_t mk_lo = (tl < valid ? 0x0000ffffu : 0u) | (tl + 1 < valid ? 0xffff0000u : 0u);
-      const uint32_t mk_hi =
-          (tl + 8 < valid ? 0x0000ffffu : 0u) | (tl + 9 < valid ? 0xffff0000u : 0u);
+      uint32_t mk_lo = 0xffffffffu, mk_hi = 0xffffffffu;
+      if (tail) {
+        const int tl = mt * 16 + 2 * c;
+        mk_lo = (tl < valid ? 0x0000ffffu : 0u) | (tl + 1 < valid ? 0xffff0000u : 0u);
+        mk_hi = (tl + 8 < valid ? 0x0000ffffu : 0u) | (tl + 9 < valid ? 0xffff0000u : 0u);
+      }
       if constexpr (!T::kFp8) {
         const int q4 = lane >> 3;
         const int row = row0 + mt * 16 + ((q4 >> 1) << 3) + (lane & 7);
@@ -281,10 +287,12 @@ struct Consumer {
                                 ((chunk ^ sw) << 4);
           uint32_t a0, a1, a2, a3;
           ldsm_x4_t(addr, a0, a1, a2, a3);
-          a0 &= mk_lo;
-          a1 &= mk_lo;
-          a2 &= mk_hi;
-          a3 &= mk_hi;
+          if (tail) {
+            a0 &= mk_lo;
+            a1 &= mk_lo;
+            a2 &= mk_hi;
+            a3 &= mk_hi;
+          }
           mma_16816<T::kBf16Mma>(acc[dt], a0, a1, a2, a3, bh[mt][0], bh[mt][1]);
           if constexpr (kSplitP)
             mma_16816<T::kBf16Mma>(acc[dt], a0, a1, a2, a3, bl[mt][0], bl[mt][1]);
@@ -299,14 +307,23 @@ struct Consumer {
           uint32_t r0, r1, r2, r3;
           ldsm_x4_t(addr, r0, r1, r2, r3);
           // r = {V[2c][2i], V[2c][2i+1], V[2c+1][2i], V[2c+1][2i+1]} -> (d even, d odd) pairs
-          const uint32_t x0 = byte_perm(r0, 0, 0x3120), x1 = byte_perm(r1, 0, 0x3120);
-          const uint32_t x2 = byte_perm(r2, 0, 0x3120), x3 = byte_perm(r3, 0, 0x3120);
-          mma_16816<false>(acc[2 * dp], e4m3x2_to_f16x2(x0 & 0xffff) & mk_lo,
-                           e4m3x2_to_f16x2(x0 >> 16) & mk_lo, e4m3x2_to_f16x2(x1 & 0xffff) & mk_hi,
-                           e4m3x2_to_f16x2(x1 >> 16) & mk_hi, bh[mt][0], bh[mt][1]);
-          mma_16816<false>(acc[2 * dp + 1], e4m3x2_to_f16x2(x2 & 0xffff) & mk_lo,
-                           e4m3x2_to_f16x2(x2 >> 16) & mk_lo, e4m3x2_to_f16x2(x3 & 0xffff) & mk_hi,
-                           e4m3x2_to_f16x2(x3 >> 16) & mk_hi, bh[mt][0], bh[mt][1]);
+          uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+          e4m3x4_to_f16x2x2(byte_perm(r0, 0, 0x3120), a0, a1);
+          e4m3x4_to_f16x2x2(byte_perm(r1, 0, 0x3120), a2, a3);
+          e4m3x4_to_f16x2x2(byte_perm(r2, 0, 0x3120), b0, b1);
+          e4m3x4_to_f16x2x2(byte_perm(r3, 0, 0x3120), b2, b3);
+          if (tail) {
+            a0 &= mk_lo;
+            a1 &= mk_lo;
+            a2 &= mk_hi;
+            a3 &= mk_hi;
+            b0 &= mk_lo;
+            b1 &= mk_lo;
+            b2 &= mk_hi;
+            b3 &= mk_hi;
+          }
+          mma_16816<false>(acc[2 * dp], a0, a1, a2, a3, bh[mt][0], bh[mt][1]);
+          mma_16816<false>(acc[2 * dp + 1], b0, b1, b2, b3, bh[mt][0], bh[mt][1]);
         }
       }
     }
@@ -411,8 +428,11 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
       int nb = s < a.B ? blocks_of(clamp_len(a, s), BS) : 0;
       total += (long long)__reduce_add_sync(0xffffffffu, (unsigned)nb);
       // units of a sequence with no tokens get no piece: mark them once
-      if (blockIdx.x == 0 && s < a.B && nb == 0)
-        for (int hg = 0; hg < a.NHG; ++hg) a.unit_info[(size_t)s * a.NHG + hg] = make_int2(0, 0);
+      if (blockIdx.x == 0 && __any_sync(0xffffffffu, s < a.B && nb == 0)) {
+        if (a.pdl) grid_dependency_wait();
+        if (s < a.B && nb == 0)
+          for (int hg = 0; hg < a.NHG; ++hg) a.unit_info[(size_t)s * a.NHG + hg] = make_int2(0, 0);
+      }
     }
     total *= a.NHG;
     // Only min(grid, total) CTAs take part, so that every run holds at least one
@@ -491,6 +511,7 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
     uint32_t round = 0;
     long long issued = 0;
     int ids = 0, id_base = -1, id_unit_s = -1;
+    bool waited = false;
     while (cur.remaining > 0) {
       // refill 32 table entries of the current sequence when needed
       if (cur.s != id_unit_s || cur.j < id_base || cur.j >= id_base + 32) {
@@ -500,9 +521,35 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
         ids = jj < cur.nb ? __ldg(a.tables + (size_t)cur.s * a.max_blocks + jj) : 0;
       }
       int blk = __shfl_sync(0xffffffffu, ids, cur.j - id_base);
-      if (blk < 0 || blk >= a.num_blocks) {
+      const bool blk_ok = blk >= 0 && blk < a.num_blocks;
+      if (!blk_ok) {
         if (lane == 0) record_error(a.status, PKV_EBOUNDS);
         blk = 0;
+      }
+      if (a.k_new && cur.j == cur.nb - 1 && blk_ok) {
+        // decode step: store the sequence's new token (position n - 1) for this
+        // head group, then order those generic-proxy writes before the TMA read
+        if (a.pdl && !waited) {
+          grid_dependency_wait();
+          waited = true;
+        }
+        const int t = (cur.n - 1) % BS;
+        const int per_head = kD / 8;
+        const int total8 = 2 * a.HG * per_head;
+        for (int i = lane; i < total8; i += 32) {
+          const int kv = i / (a.HG * per_head);
+          const int r = i - kv * a.HG * per_head;
+          const int h = cur.hg * a.HG + r / per_head;
+          const int d8 = r % per_head;
+          const size_t src = ((size_t)cur.s * a.Hkv + h) * kD + (size_t)d8 * 8;
+          const size_t dst =
+              (((((size_t)blk * 2 + kv) * a.L + a.layer) * a.Hkv + h) * BS + t) * kD +
+              (size_t)d8 * 8;
+          store8_to_pool(const_cast<void*>(a.pool), dst, KVT, kv ? a.v_new : a.k_new, src,
+                         a.new_dtype, kv ? a.v_enc_scale : a.k_enc_scale);
+        }
+        fence_proxy_async_global();
+        __syncwarp();
       }
       if (lane == 0) {
         bool ok = mbar_wait_bounded(&hdr->empty[stage], (round & 1) ^ 1);
@@ -555,11 +602,13 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
   cons.qk_scale_log2_ = a.qk_scale_log2;
   cons.reset();
   const int w = warp;
+  bool waited = false;
   int hkv = cur.hg * a.HG + w;
   if (cur.remaining > 0) cons.load_q(a, cur.s, hkv, lane);
 
   // fixed mode, empty partition: an empty partial (or zero output when S == 1)
   if (a.mode == 1 && cur.remaining <= 0) {
+    if (a.pdl) grid_dependency_wait();
     size_t base;
     int stride;
     part_addr(a, cur.s, hkv, w, 0, part_p, base, stride);
@@ -599,6 +648,10 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
     const bool unit_end = cur.j == cur.nb - 1;
     const bool run_end = cur.remaining == 1;
     if (unit_end || run_end) {
+      if (a.pdl && !waited) {
+        grid_dependency_wait();
+        waited = true;
+      }
       const bool first = cur.j0 == 0;
       const long long u = (long long)cur.s * a.NHG + cur.hg;
       bool whole;
@@ -652,8 +705,17 @@ static cudaError_t launch_t(const CUtensorMap* map, const DecodeArgs& a, int gx,
   auto kern = decode_mma_kernel<KVT, BS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(gx, gy), 32 * (a.HG + 1), smem, stream>>>(*map, a);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(gx, gy);
+  cfg.blockDim = dim3(32 * (a.HG + 1));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.pdl ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, *map, a);
   if (e == cudaSuccess) count_launch();
   return e;
 }

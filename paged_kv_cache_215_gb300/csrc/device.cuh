@@ -157,6 +157,17 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t x) {
   return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
 
+// Four E4M3 codes in one register (byte 0 first) -> two f16x2: lo = bytes 0,1;
+// hi = bytes 2,3.  Exact.  The 16-bit halves are taken with a register unpack.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(x));
+}
+
 __device__ __forceinline__ uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t sel) {
   return __byte_perm(a, b, sel);
 }
@@ -177,6 +188,65 @@ __device__ __forceinline__ void store_from_float(void* base, size_t idx, int dty
     case PKV_F16: static_cast<__half*>(base)[idx] = __float2half_rn(v); break;
     case PKV_BF16: static_cast<__nv_bfloat16*>(base)[idx] = __float2bfloat16_rn(v); break;
     default: break;
+  }
+}
+
+// Generic-proxy writes to global memory made visible to later TMA (async-proxy) reads.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Eight consecutive elements of an f32 / f16 / bf16 array as floats (16-byte aligned).
+__device__ __forceinline__ void load8_as_float(const void* src, size_t idx, int dtype,
+                                               float (&x)[8]) {
+  if (dtype == PKV_F32) {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(src) + idx);
+    const float4 a = p[0], b = p[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  } else {
+    const uint4 r = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + idx);
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = dtype == PKV_BF16 ? unpack2<true>(w[i]) : unpack2<false>(w[i]);
+      x[2 * i] = f.x;
+      x[2 * i + 1] = f.y;
+    }
+  }
+}
+
+// Per-tensor E4M3 store rule: y = x / scale (IEEE fp32 division), round to
+// nearest even, finite overflow and +-Inf saturate to +-448, NaN -> 0x7F.
+__device__ __forceinline__ uint8_t encode_e4m3(float x, float scale) {
+  const float y = __fdiv_rn(x, scale);
+  if (isnan(y)) return 0x7F;
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3));
+}
+
+// Store 8 consecutive elements of one token row into the pool: a 16-byte copy
+// for a pool of the input's dtype, or E4M3 encoding into 8 bytes.
+__device__ __forceinline__ void store8_to_pool(void* pool, size_t dst, int kv_dtype,
+                                               const void* src, size_t sidx, int in_dtype,
+                                               float scale) {
+  if (kv_dtype == PKV_FP8_E4M3) {
+    float x[8];
+    load8_as_float(src, sidx, in_dtype, x);
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      lo |= static_cast<uint32_t>(encode_e4m3(x[e], scale)) << (8 * e);
+      hi |= static_cast<uint32_t>(encode_e4m3(x[4 + e], scale)) << (8 * e);
+    }
+    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(pool) + dst) = make_uint2(lo, hi);
+  } else if (kv_dtype == PKV_F32) {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(src) + sidx);
+    float4* q = reinterpret_cast<float4*>(static_cast<float*>(pool) + dst);
+    q[0] = p[0];
+    q[1] = p[1];
+  } else {
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(pool) + dst) =
+        *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + sidx);
   }
 }
 

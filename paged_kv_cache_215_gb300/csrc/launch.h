@@ -31,6 +31,16 @@ struct DecodeArgs {
   int S;                     // partitions per sequence in mode 1
   float qk_scale_log2;       // softmax scale * log2(e) (* k_scale for E4M3)
   float v_scale;             // v_scale for E4M3, else 1
+  // Fused append (decode step): when k_new is set, the new token of sequence s
+  // ([B, Hkv, D] in new_dtype) is stored at position seq_lens[s] - 1 before the
+  // block holding it is read; E4M3 pools encode with k_enc_scale / v_enc_scale.
+  const void* k_new;
+  const void* v_new;
+  int new_dtype;
+  float k_enc_scale, v_enc_scale;
+  // 1: launched with programmatic dependent launch; every write to out, the
+  // workspace or the pool waits for the preceding kernel (griddepcontrol.wait).
+  int pdl;
 };
 
 // Shared memory the tensor-core kernel needs for one CTA.
@@ -53,7 +63,8 @@ struct AppendArgs {
   const void* v;
   const int32_t* tables;
   const int32_t* seq_ids;    // nullptr: token i belongs to sequence i
-  const int32_t* positions;
+  const int32_t* positions;  // nullptr: position seq_lens[s] - 1 (the decode step's token)
+  const int32_t* seq_lens;
   int32_t* status;
   int64_t num_tokens;
   int B, Hkv, D, BS, L, layer, max_blocks, num_blocks;

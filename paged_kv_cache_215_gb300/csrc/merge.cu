@@ -10,24 +10,30 @@
 // sum_p w_p O_p / sum_p w_p.  A partial with lse_p = -inf (an empty key range)
 // has weight 0; a row with no finite partial is 0.
 //
-// One CTA of 256 threads merges one row: its eight warps take every eighth
-// partial, lanes split the head dimension, and the warps' sums meet in shared
-// memory.
+// One CTA of 512 threads merges one row: the partials' weights are computed
+// once into shared memory, each of the sixteen warps takes every sixteenth
+// partial with four rows in flight, lanes split the head dimension, and the
+// warps' sums meet in shared memory.
 #include "device.cuh"
 #include "launch.h"
 
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxDL = 8;   // head_dim <= 256
+constexpr int kMaxD = 256;
+constexpr int kChunk = 1024;   // partial weights staged in shared memory per pass
+constexpr int kUnroll = 4;     // partial rows in flight per warp
 
 // Partial i of the row: lse at lse[i * lse_stride], O at o[i * o_stride + d].
+// Vector path: D % 4 == 0 and 16-byte aligned rows; lane g holds columns 4g..4g+3
+// (and 4(g+32)..) of one partial row per load, so a warp reads a whole row.
 __device__ void merge_row(const float* __restrict__ lse, size_t lse_stride,
                           const float* __restrict__ o, size_t o_stride, int count, int D,
                           void* out, size_t out_off, int out_dtype) {
-  __shared__ float red[kWarps][32 * kMaxDL];
+  __shared__ float wts[kChunk];
+  __shared__ float red[kWarps][kMaxD];
   __shared__ float redw[kWarps];
   __shared__ float redm[kWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -38,30 +44,88 @@ __device__ void merge_row(const float* __restrict__ lse, size_t lse_stride,
   if (lane == 0) redm[warp] = M;
   __syncthreads();
   M = redm[0];
+#pragma unroll
   for (int w = 1; w < kWarps; ++w) M = fmaxf(M, redm[w]);
 
-  float acc[kMaxDL];
+  const bool vec = (D % 4) == 0 && (o_stride % 4) == 0 &&
+                   (reinterpret_cast<uintptr_t>(o) & 15u) == 0;
+  const int groups = vec ? D / 4 : 0;
+  float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+  float accs[kMaxD / 32];
 #pragma unroll
-  for (int k = 0; k < kMaxDL; ++k) acc[k] = 0.f;
+  for (int k = 0; k < kMaxD / 32; ++k) accs[k] = 0.f;
   float wsum = 0.f;
+
   if (M != -INFINITY) {
-#pragma unroll 4
-    for (int i = warp; i < count; i += kWarps) {
-      const float w = exp2f((lse[i * lse_stride] - M) * kLog2e);
-      wsum += w;
-      const float* op = o + i * o_stride;
+    for (int base = 0; base < count; base += kChunk) {
+      const int n = min(kChunk, count - base);
+      __syncthreads();
+      for (int i = threadIdx.x; i < n; i += kThreads)
+        wts[i] = exp2f((lse[(size_t)(base + i) * lse_stride] - M) * kLog2e);
+      __syncthreads();
+      for (int i0 = warp; i0 < n; i0 += kWarps * kUnroll) {
+        if (vec) {
+          float4 v[kUnroll][2];
 #pragma unroll
-      for (int k = 0; k < kMaxDL; ++k)
-        if (lane + 32 * k < D) acc[k] = fmaf(w, op[lane + 32 * k], acc[k]);
+          for (int u = 0; u < kUnroll; ++u) {
+            const int i = i0 + u * kWarps;
+            const float4* row = reinterpret_cast<const float4*>(o + (size_t)(base + i) * o_stride);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int g = lane + 32 * h;
+              v[u][h] = (i < n && g < groups) ? row[g] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < kUnroll; ++u) {
+            const int i = i0 + u * kWarps;
+            const float w = i < n ? wts[i] : 0.f;
+            wsum += w;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              acc[h].x = fmaf(w, v[u][h].x, acc[h].x);
+              acc[h].y = fmaf(w, v[u][h].y, acc[h].y);
+              acc[h].z = fmaf(w, v[u][h].z, acc[h].z);
+              acc[h].w = fmaf(w, v[u][h].w, acc[h].w);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < kUnroll; ++u) {
+            const int i = i0 + u * kWarps;
+            if (i >= n) break;
+            const float w = wts[i];
+            wsum += w;
+            const float* row = o + (size_t)(base + i) * o_stride;
+#pragma unroll
+            for (int k = 0; k < kMaxD / 32; ++k)
+              if (lane + 32 * k < D) accs[k] = fmaf(w, row[lane + 32 * k], accs[k]);
+          }
+        }
+      }
     }
   }
+  if (vec) {
 #pragma unroll
-  for (int k = 0; k < kMaxDL; ++k)
-    if (lane + 32 * k < D) red[warp][lane + 32 * k] = acc[k];
+    for (int h = 0; h < 2; ++h) {
+      const int g = lane + 32 * h;
+      if (g < groups) {
+        red[warp][4 * g + 0] = acc[h].x;
+        red[warp][4 * g + 1] = acc[h].y;
+        red[warp][4 * g + 2] = acc[h].z;
+        red[warp][4 * g + 3] = acc[h].w;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < kMaxD / 32; ++k)
+      if (lane + 32 * k < D) red[warp][lane + 32 * k] = accs[k];
+  }
   if (lane == 0) redw[warp] = wsum;
   __syncthreads();
   for (int d = threadIdx.x; d < D; d += kThreads) {
     float W = 0.f, v = 0.f;
+#pragma unroll
     for (int w = 0; w < kWarps; ++w) {
       W += redw[w];
       v += red[w][d];
@@ -75,6 +139,8 @@ __device__ void merge_row(const float* __restrict__ lse, size_t lse_stride,
 // kernel already wrote the output.
 __global__ void __launch_bounds__(kThreads) merge_units_kernel(const DecodeArgs a) {
   grid_dependency_wait();
+  // the next launch may begin now: this grid's inputs are complete
+  grid_launch_dependents();
   const int u = blockIdx.x, hl = blockIdx.y;
   const int2 info = a.unit_info[u];
   if (info.y == 1) return;
@@ -91,6 +157,7 @@ __global__ void __launch_bounds__(kThreads)
     merge_rows_kernel(void* out, int out_dtype, const float* part_o, const float* part_lse, int S,
                       int D) {
   grid_dependency_wait();
+  grid_launch_dependents();
   const size_t r = blockIdx.x;
   merge_row(part_lse + r * S, 1, part_o + r * S * D, D, S, D, out, r * D, out_dtype);
 }
@@ -115,7 +182,7 @@ static cudaError_t launch_pdl(const void* func, dim3 grid, void** args, bool pdl
 }
 
 cudaError_t launch_merge_units(const DecodeArgs& a, bool pdl, cudaStream_t stream) {
-  if (a.D > 32 * kMaxDL) return cudaErrorInvalidValue;
+  if (a.D > kMaxD) return cudaErrorInvalidValue;
   const int units = a.B * a.NHG;
   if (units == 0) return cudaSuccess;
   DecodeArgs copy = a;
@@ -126,7 +193,7 @@ cudaError_t launch_merge_units(const DecodeArgs& a, bool pdl, cudaStream_t strea
 
 cudaError_t launch_merge_rows(void* out, int out_dtype, const float* part_o, const float* part_lse,
                               int rows, int S, int D, bool pdl, cudaStream_t stream) {
-  if (D > 32 * kMaxDL) return cudaErrorInvalidValue;
+  if (D > kMaxD) return cudaErrorInvalidValue;
   if (rows == 0) return cudaSuccess;
   void* args[] = {&out, &out_dtype, &part_o, &part_lse, &S, &D};
   return launch_pdl(reinterpret_cast<const void*>(merge_rows_kernel), dim3(rows), args, pdl,

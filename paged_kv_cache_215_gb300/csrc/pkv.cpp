@@ -89,16 +89,21 @@ static bool hg_ok(const pkv_geometry& g, int hg) {
 }
 
 // Tensor-core kernel: KV heads per CTA, pipeline depth and persistent grid.
+// Defaults (measured on GB300 over the 8K x 32, 128K, 1M, 70B-shaped and FP8
+// workloads): two CTAs per SM; each CTA streams a head group of at most 4 KV
+// heads whose per-block K+V stage is at most 32 KB; the ring keeps about 128 KB
+// per SM in flight for 16-bit pools and 192 KB for E4M3 pools, whose
+// conversion work needs deeper buffering.  Deeper 16-bit rings measured slower.
 static bool plan_mma(const pkv_geometry& g, const DeviceInfo& dev, const pkv_launch_opts* o,
                      MmaPlan* p) {
-  const int ctas = (o && o->ctas_per_sm > 0) ? o->ctas_per_sm : 1;
+  const int ctas = (o && o->ctas_per_sm > 0) ? o->ctas_per_sm : 2;
   if (ctas > 8) return false;
   int hg = (o && o->kv_heads_per_cta > 0) ? o->kv_heads_per_cta : 0;
   if (hg) {
     if (!hg_ok(g, hg)) return false;
   } else {
-    for (int c = 8; c >= 1; --c)
-      if (hg_ok(g, c) && mma_stage_bytes(g.kv_dtype, g.block_size, c) <= 64 * 1024) {
+    for (int c = 4; c >= 1; --c)
+      if (hg_ok(g, c) && mma_stage_bytes(g.kv_dtype, g.block_size, c) <= 32 * 1024) {
         hg = c;
         break;
       }
@@ -107,13 +112,15 @@ static bool plan_mma(const pkv_geometry& g, const DeviceInfo& dev, const pkv_lau
   const size_t stage = mma_stage_bytes(g.kv_dtype, g.block_size, hg);
   const size_t per_cta = std::min<size_t>((size_t)dev.smem_optin,
                                           (size_t)dev.smem_per_sm / ctas - 1024);
+  const size_t fixed = mma_smem_bytes(g.kv_dtype, g.block_size, hg, 0);
+  const int fit = per_cta > fixed ? (int)((per_cta - fixed) / stage) : 0;
   int stages = (o && o->stages > 0) ? o->stages : 0;
   if (!stages) {
-    const size_t fixed = mma_smem_bytes(g.kv_dtype, g.block_size, hg, 0);
-    stages = per_cta > fixed ? (int)((per_cta - fixed) / stage) : 0;
-    stages = std::min(stages, 8);
+    const size_t inflight = (g.kv_dtype == PKV_FP8_E4M3 ? 192 : 128) * 1024;
+    stages = (int)(inflight / ((size_t)ctas * stage));
+    stages = std::max(2, std::min(stages, std::min(fit, 8)));
   }
-  if (stages < 2 || stages > 16) return false;
+  if (stages < 2 || stages > 16 || stages > fit) return false;
   p->HG = hg;
   p->NHG = g.num_kv_heads / hg;
   p->stages = stages;
@@ -382,6 +389,7 @@ static int append_common(pkv_pool* p, int layer, const void* k, const void* v, p
   a.tables = tables;
   a.seq_ids = seq_ids;
   a.positions = positions;
+  a.seq_lens = nullptr;
   a.status = p->d_status;
   a.num_tokens = num_tokens;
   a.B = batch;
@@ -440,12 +448,16 @@ size_t paged_decode_workspace_bytes(const pkv_geometry* g, int batch, int max_se
   return need + 256;
 }
 
-int paged_decode_attention_ex(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_dtype q_dtype,
-                              const pkv_pool* pool, int layer, const int32_t* d_block_tables,
-                              int max_blocks_per_seq, const int32_t* d_seq_lens, int batch,
-                              int max_seq_len, float scale, float k_scale, float v_scale,
-                              int num_splits, void* d_workspace, size_t ws_bytes,
-                              const pkv_launch_opts* opts, cudaStream_t stream) {
+// Shared body of paged_decode_attention_ex and paged_decode_step.  With k_new
+// set, every sequence's new token is first stored at position seq_lens[s] - 1
+// (fused into the tensor-core kernel, or a separate append launch otherwise).
+static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_dtype q_dtype,
+                         const void* d_k_new, const void* d_v_new, int new_dtype,
+                         const pkv_pool* pool, int layer, const int32_t* d_block_tables,
+                         int max_blocks_per_seq, const int32_t* d_seq_lens, int batch,
+                         int max_seq_len, float scale, float k_scale, float v_scale,
+                         int num_splits, void* d_workspace, size_t ws_bytes,
+                         const pkv_launch_opts* opts, cudaStream_t stream) {
   pkv_pool* p = const_cast<pkv_pool*>(pool);
   if (!p || batch < 0 || max_seq_len < 0 || num_splits < 0 || layer < 0 ||
       layer >= p->g.num_layers)
@@ -462,9 +474,16 @@ int paged_decode_attention_ex(void* d_out, pkv_dtype out_dtype, const void* d_q,
   if (fp8 && (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) ||
               !std::isfinite(v_scale)))
     return PKV_EINVAL;
+  const bool fused_append = d_k_new != nullptr;
+  if (fused_append) {
+    if (!d_v_new || !aligned16(d_k_new) || !aligned16(d_v_new)) return PKV_EINVAL;
+    if (fp8 ? !act_dtype(new_dtype) : new_dtype != g.kv_dtype) return PKV_EINVAL;
+  }
   const int phase = opts ? opts->phase : 0;
   const int kernel = opts ? opts->kernel : 0;
-  if (phase < 0 || phase > 2 || kernel < 0 || kernel > 2) return PKV_EINVAL;
+  const int pdl = opts ? opts->pdl : 0;
+  if (phase < 0 || phase > 2 || kernel < 0 || kernel > 2 || pdl < 0 || pdl > 1)
+    return PKV_EINVAL;
   DeviceInfo dev;
   if (!device_info(&dev)) return PKV_ECUDA;
 
@@ -507,8 +526,39 @@ int paged_decode_attention_ex(void* d_out, pkv_dtype out_dtype, const void* d_q,
   a.kv_dtype = g.kv_dtype;
   a.qk_scale_log2 = (float)((double)scale * 1.4426950408889634 * (fp8 ? (double)k_scale : 1.0));
   a.v_scale = fp8 ? v_scale : 1.f;
+  a.k_enc_scale = k_scale;
+  a.v_enc_scale = v_scale;
+  a.new_dtype = new_dtype;
   if (d_workspace && !aligned16(d_workspace)) return PKV_EINVAL;
   char* ws = static_cast<char*>(d_workspace);
+
+  // without the fused path the new tokens go in through the append kernel first
+  auto append_first = [&]() -> int {
+    if (!fused_append || phase == 2) return PKV_OK;
+    AppendArgs ap{};
+    ap.pool = p->d_pool;
+    ap.k = d_k_new;
+    ap.v = d_v_new;
+    ap.tables = d_block_tables;
+    ap.seq_ids = nullptr;
+    ap.positions = nullptr;
+    ap.seq_lens = d_seq_lens;
+    ap.status = p->d_status;
+    ap.num_tokens = batch;
+    ap.B = batch;
+    ap.Hkv = g.num_kv_heads;
+    ap.D = g.head_dim;
+    ap.BS = g.block_size;
+    ap.L = g.num_layers;
+    ap.layer = layer;
+    ap.max_blocks = max_blocks_per_seq;
+    ap.num_blocks = g.num_blocks;
+    ap.in_dtype = new_dtype;
+    ap.kv_dtype = g.kv_dtype;
+    ap.k_scale = k_scale;
+    ap.v_scale = v_scale;
+    return launch_append(ap, stream) == cudaSuccess ? PKV_OK : PKV_ECUDA;
+  };
 
   if (use_mma) {
     MmaPlan plan;
@@ -516,6 +566,11 @@ int paged_decode_attention_ex(void* d_out, pkv_dtype out_dtype, const void* d_q,
     a.HG = plan.HG;
     a.NHG = plan.NHG;
     a.stages = plan.stages;
+    a.pdl = pdl;
+    if (fused_append) {
+      a.k_new = d_k_new;
+      a.v_new = d_v_new;
+    }
     const CUtensorMap* map = p->tmap(plan.HG);
     if (!map) return PKV_ECUDA;
     if (num_splits == 0) {
@@ -559,12 +614,38 @@ int paged_decode_attention_ex(void* d_out, pkv_dtype out_dtype, const void* d_q,
   a.S = S;
   a.part_o = S > 1 ? reinterpret_cast<float*>(ws) : nullptr;
   a.part_lse = S > 1 ? reinterpret_cast<float*>(ws + lse_off) : nullptr;
+  const int rc = append_first();
+  if (rc != PKV_OK) return rc;
   if (phase != 2 && launch_decode_simt(a, stream) != cudaSuccess) return PKV_ECUDA;
   if (S > 1 && phase != 1 &&
       launch_merge_rows(d_out, out_dtype, a.part_o, a.part_lse, batch * g.num_q_heads, S,
                         g.head_dim, phase == 0, stream) != cudaSuccess)
     return PKV_ECUDA;
   return PKV_OK;
+}
+
+int paged_decode_attention_ex(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_dtype q_dtype,
+                              const pkv_pool* pool, int layer, const int32_t* d_block_tables,
+                              int max_blocks_per_seq, const int32_t* d_seq_lens, int batch,
+                              int max_seq_len, float scale, float k_scale, float v_scale,
+                              int num_splits, void* d_workspace, size_t ws_bytes,
+                              const pkv_launch_opts* opts, cudaStream_t stream) {
+  return decode_common(d_out, out_dtype, d_q, q_dtype, nullptr, nullptr, 0, pool, layer,
+                       d_block_tables, max_blocks_per_seq, d_seq_lens, batch, max_seq_len, scale,
+                       k_scale, v_scale, num_splits, d_workspace, ws_bytes, opts, stream);
+}
+
+int paged_decode_step(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_dtype q_dtype,
+                      const void* d_k_new, const void* d_v_new, pkv_dtype new_dtype,
+                      const pkv_pool* pool, int layer, const int32_t* d_block_tables,
+                      int max_blocks_per_seq, const int32_t* d_seq_lens, int batch,
+                      int max_seq_len, float scale, float k_scale, float v_scale, int num_splits,
+                      void* d_workspace, size_t ws_bytes, const pkv_launch_opts* opts,
+                      cudaStream_t stream) {
+  if (!d_k_new) return PKV_EINVAL;
+  return decode_common(d_out, out_dtype, d_q, q_dtype, d_k_new, d_v_new, new_dtype, pool, layer,
+                       d_block_tables, max_blocks_per_seq, d_seq_lens, batch, max_seq_len, scale,
+                       k_scale, v_scale, num_splits, d_workspace, ws_bytes, opts, stream);
 }
 
 int paged_decode_attention(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_dtype q_dtype,

@@ -42,7 +42,8 @@ class Geometry(ctypes.Structure):
 class LaunchOpts(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
                 ("kv_heads_per_cta", ctypes.c_int32), ("stages", ctypes.c_int32),
-                ("phase", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("phase", ctypes.c_int32), ("pdl", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
 
 
 def _load() -> ctypes.CDLL:
@@ -74,6 +75,8 @@ def _load() -> ctypes.CDLL:
         "paged_decode_attention_ex": (I, [P, I, P, I, P, I, P, I, P, I, I, F, F, F, I, P, Z,
                                           ctypes.POINTER(LaunchOpts), P]),
         "merge_partials": (I, [P, I, P, P, I, I, I, I, P]),
+        "paged_decode_step": (I, [P, I, P, I, P, P, I, P, I, P, I, P, I, I, F, F, F, I, P, Z,
+                                  ctypes.POINTER(LaunchOpts), P]),
         "paged_decode_attention_static": (I, [P, I, P, I, P, I, P, I, P, I, I, F, F, F, I, P]),
         "pkv_check_status": (I, [P, P]),
         "pkv_strerror": (ctypes.c_char_p, [I]),
@@ -92,7 +95,7 @@ EXPORTS = ("kv_pool_bytes", "kv_pool_create", "kv_pool_destroy", "kv_pool_geomet
            "kv_pool_refcount", "kv_pool_num_free", "kv_pool_cow", "kv_append",
            "kv_append_tokens", "kv_absmax", "paged_decode_workspace_bytes",
            "paged_decode_attention", "paged_decode_attention_ex", "merge_partials",
-           "paged_decode_attention_static",
+           "paged_decode_attention_static", "paged_decode_step",
            "pkv_check_status", "pkv_strerror", "pkv_launch_count")
 
 
@@ -140,10 +143,11 @@ def launch_count() -> int:
     return int(_lib.pkv_launch_count())
 
 
-def launch_opts(kernel=0, ctas_per_sm=0, kv_heads_per_cta=0, stages=0, phase=0) -> LaunchOpts:
+def launch_opts(kernel=0, ctas_per_sm=0, kv_heads_per_cta=0, stages=0, phase=0,
+                pdl=0) -> LaunchOpts:
     o = LaunchOpts()
-    o.kernel, o.ctas_per_sm, o.kv_heads_per_cta, o.stages, o.phase = \
-        kernel, ctas_per_sm, kv_heads_per_cta, stages, phase
+    o.kernel, o.ctas_per_sm, o.kv_heads_per_cta, o.stages, o.phase, o.pdl = \
+        kernel, ctas_per_sm, kv_heads_per_cta, stages, phase, pdl
     return o
 
 
@@ -272,6 +276,23 @@ def paged_decode_attention_static(out, q, pool: KVPool, layer, tables, seq_lens,
         _ptr(out), TORCH_CODE[out.dtype], _ptr(q), TORCH_CODE[q.dtype], pool.handle, layer,
         _ptr(tables), tables.shape[1], _ptr(seq_lens), q.shape[0], max_seq_len, scale, k_scale,
         v_scale, num_splits, _stream(stream)), "paged_decode_attention_static")
+    return out
+
+
+def paged_decode_step(out, q, k_new, v_new, pool: KVPool, layer, tables, seq_lens, max_seq_len,
+                      scale, k_scale=1.0, v_scale=1.0, num_splits=0, workspace=None, opts=None,
+                      stream=None):
+    """Store each sequence's new token at position seq_len - 1, then decode attention
+    (fused into one attention launch on the tensor-core kernel)."""
+    if workspace is None:
+        nb = workspace_bytes(pool.geom, q.shape[0], max_seq_len, num_splits)
+        workspace = torch.empty(max(nb, 16), dtype=torch.uint8, device=q.device)
+    _check(_lib.paged_decode_step(
+        _ptr(out), TORCH_CODE[out.dtype], _ptr(q), TORCH_CODE[q.dtype], _ptr(k_new), _ptr(v_new),
+        TORCH_CODE[k_new.dtype], pool.handle, layer, _ptr(tables), tables.shape[1],
+        _ptr(seq_lens), q.shape[0], max_seq_len, scale, k_scale, v_scale, num_splits,
+        _ptr(workspace), workspace.numel(), None if opts is None else ctypes.byref(opts),
+        _stream(stream)), "paged_decode_step")
     return out
 
 

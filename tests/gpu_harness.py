@@ -54,6 +54,16 @@ class GpuCase:
             self.pool.append_tokens(case.layer, self.k_tokens, self.v_tokens, self.tables,
                                     self.tok_seq, self.tok_pos, self.k_scale, self.v_scale)
 
+    def fused_step(self, out_dtype="f32", num_splits=0, opts=None):
+        """One decode step through paged_decode_step (store + attention in one launch)."""
+        c = self.case
+        out = torch.full((c.batch, c.num_q_heads, c.head_dim), float("nan"),
+                         dtype=OUT_DT[out_dtype], device=self.q.device)
+        self.pkv.paged_decode_step(out, self.q, self.k_new, self.v_new, self.pool, c.layer,
+                                   self.tables, self.seq_lens, self.max_seq_len, c.scale,
+                                   self.k_scale, self.v_scale, num_splits=num_splits, opts=opts)
+        return out
+
     def step(self, out_dtype="f32", num_splits=0, opts=None, append=True):
         """One decode step: append the last token of every sequence, then attend."""
         c = self.case

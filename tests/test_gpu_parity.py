@@ -107,6 +107,42 @@ def test_decode_parity_low_precision_out(case):
     assert_parity(case, out, ref, pool, seqs, gc.v_scale, case.name, out_dtype=case.out_dtype)
 
 
+@pytest.mark.parametrize("splits", [0, 3])
+@pytest.mark.parametrize("kernel", [0, 1])
+@pytest.mark.parametrize("case", CASES, ids=lambda c: c.name)
+def test_fused_decode_step_matches_append_then_attend(case, kernel, splits):
+    """paged_decode_step stores the new tokens itself; its pool must equal the
+    oracle's and its output must match the oracle like the two-call path."""
+    from paged_kv_cache_215_gb300 import pkv
+    tens = wl.make_tensors(case)
+    gc = GpuCase(case, tens)                                    # new tokens not yet stored
+    _, pool, ref, seqs = _sides(case)
+    opts = pkv.launch_opts(kernel=kernel) if kernel else None
+    try:
+        out = gc.fused_step(num_splits=splits, opts=opts)
+    except pkv.PkvError as e:
+        if e.code == pkv.PKV_EUNSUPPORTED:
+            pytest.skip("kernel does not take this shape")
+        raise
+    torch.cuda.synchronize()
+    assert gc.status() == 0
+    assert np.array_equal(gc.pool.storage.cpu().numpy(), pool), "pool bytes differ"
+    assert_parity(case, out, ref, pool, seqs, gc.v_scale, f"{case.name} fused k{kernel} s{splits}")
+    two_call = gc.step(num_splits=splits, opts=opts)             # same pool, same inputs
+    assert torch.equal(out, two_call)
+
+
+def test_programmatic_dependent_launch_keeps_results():
+    from paged_kv_cache_215_gb300 import pkv
+    case = wl.llama8b_batch(batch=5, lo=100, hi=1500, seed=11)
+    gc, pool, ref, seqs = _sides(case)
+    plain = gc.fused_step()
+    outs = [gc.fused_step(opts=pkv.launch_opts(pdl=1)) for _ in range(3)]   # back to back
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(o, plain)
+
+
 def test_zero_length_sequence_gives_zero_and_single_token_gives_v():
     case = [c for c in CASES if c.name == "ragged_edges_bf16"][0]
     gc, pool, ref, seqs = _sides(case)
