@@ -392,6 +392,21 @@ def measure(name, steps, warmup, device, with_clocks=False, gpu_index=0, e2e=Tru
     return w, res
 
 
+def aggregate_ranks(ms_per_step, kv_bytes_per_step, device="cpu"):
+    """Whole-job throughput over all ranks: every rank ran its own batch (no data
+    exchange), the job took as long as the slowest rank, and the job moved the
+    sum of all ranks' KV bytes.  Returns (max ms per step, GB/s of the job)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms_per_step, kv_bytes_per_step / (ms_per_step * 1e-3) / 1e9
+    t = torch.tensor([ms_per_step, float(kv_bytes_per_step)], dtype=torch.float64, device=device)
+    mx = t.clone()
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    ms = float(mx[0].item())
+    return ms, float(t[1].item()) / (ms * 1e-3) / 1e9
+
+
 def run_ours(args):
     ws, rank, local = dist_env()
     if ws > 1:
@@ -406,13 +421,7 @@ def run_ours(args):
         dist.barrier()
     name = args.workload
     w, res = measure(name, args.steps, args.warmup, device, with_clocks=True, gpu_index=local)
-    # whole-job time: max over ranks of the headline loop
-    ms = res["ms_per_step"]
-    if ws > 1:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = ws * res["kv_bytes"] / (ms * 1e-3) / 1e9
+    ms, value = aggregate_ranks(res["ms_per_step"], res["kv_bytes"], device)
     extra = {}
     if rank == 0 and not args.no_cpu_baseline:
         extra["cpu_baseline"] = cpu_baseline(w)

@@ -695,7 +695,7 @@ size_t mma_smem_bytes(int kv_dtype, int BS, int HG, int stages) {
 
 bool mma_supported(int kv_dtype, int BS, int D, int G) {
   return (kv_dtype == PKV_BF16 || kv_dtype == PKV_F16 || kv_dtype == PKV_FP8_E4M3) &&
-         (BS == 16 || BS == 32) && D == kD && G >= 1 && G <= 8;
+         (BS == 16 || BS == 32 || BS == 64) && D == kD && G >= 1 && G <= 8;
 }
 
 template <int KVT, int BS>
@@ -730,6 +730,9 @@ cudaError_t launch_decode_mma(const CUtensorMap* map, const DecodeArgs& a, int g
     case PKV_F16 * 100 + 32: return launch_t<PKV_F16, 32>(map, a, gx, gy, stream);
     case PKV_FP8_E4M3 * 100 + 16: return launch_t<PKV_FP8_E4M3, 16>(map, a, gx, gy, stream);
     case PKV_FP8_E4M3 * 100 + 32: return launch_t<PKV_FP8_E4M3, 32>(map, a, gx, gy, stream);
+    case PKV_BF16 * 100 + 64: return launch_t<PKV_BF16, 64>(map, a, gx, gy, stream);
+    case PKV_F16 * 100 + 64: return launch_t<PKV_F16, 64>(map, a, gx, gy, stream);
+    case PKV_FP8_E4M3 * 100 + 64: return launch_t<PKV_FP8_E4M3, 64>(map, a, gx, gy, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -103,7 +103,7 @@ def _build_tables(lens, bs, num_blocks, perm, shared_tokens=0):
 
 def make_case(name: str, seq_lens, num_q_heads, num_kv_heads, head_dim, block_size,
               kv_dtype, q_dtype, out_dtype, seed, pool_slack=0.10, spike_frac=0.0,
-              shared_prefix_tokens=0) -> Case:
+              shared_prefix_tokens=0, num_layers=1, layer=0) -> Case:
     lens = np.asarray(seq_lens, dtype=np.int32)
     bs = block_size
     need = sum((int(n) + bs - 1) // bs for n in lens)
@@ -120,7 +120,7 @@ def make_case(name: str, seq_lens, num_q_heads, num_kv_heads, head_dim, block_si
                 head_dim=head_dim, block_size=bs, kv_dtype=kv_dtype, q_dtype=q_dtype,
                 out_dtype=out_dtype, seq_lens=lens, tables=tables, num_blocks=num_blocks,
                 seed=seed, spike_frac=spike_frac, shared_prefix_tokens=shared_prefix_tokens,
-                shared_blocks=shared)
+                shared_blocks=shared, num_layers=num_layers, layer=layer)
 
 
 # ---------------------------------------------------------------------------

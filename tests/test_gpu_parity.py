@@ -45,6 +45,16 @@ def small_cases():
                      "bf16", "bf16", seed=18),
         wl.make_case("ragged_edges_bs32_g8", [1, 32, 33, 64, 0, 95], 64, 8, 128, 32, "bf16",
                      "bf16", "bf16", seed=19),
+        wl.make_case("bs64_bf16", [1, 63, 64, 65, 700, 2049], 32, 8, 128, 64, "bf16", "bf16",
+                     "bf16", seed=40),
+        wl.make_case("bs64_fp8", [64, 129, 1500], 32, 8, 128, 64, "e4m3", "bf16", "bf16",
+                     seed=41),
+        wl.make_case("fp8_bs32_g8", [31, 33, 900], 64, 8, 128, 32, "e4m3", "bf16", "bf16",
+                     seed=42),
+        wl.make_case("layers3_layer2_bf16", [40, 333, 1000], 32, 8, 128, 16, "bf16", "bf16",
+                     "bf16", seed=43, num_layers=3, layer=2),
+        wl.make_case("layers2_layer0_fp8_bs32", [77, 600], 32, 8, 128, 32, "e4m3", "bf16",
+                     "bf16", seed=44, num_layers=2, layer=0),
     ]
 
 

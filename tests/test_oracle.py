@@ -142,6 +142,8 @@ def _small_cases():
         wl.make_case("gqa4_f16_bs32", [33, 64, 70], 8, 2, 16, 32, "f16", "f16", "f16", seed=6),
         wl.make_case("gqa8_bf16_prefix", [20, 70, 40], 16, 2, 16, 16, "bf16", "bf16", "bf16",
                      seed=7, shared_prefix_tokens=32),
+        wl.make_case("layers3_layer1_bs64", [5, 64, 130], 4, 2, 16, 64, "bf16", "bf16", "bf16",
+                     seed=8, num_layers=3, layer=1),
     ]
 
 
