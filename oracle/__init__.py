@@ -58,6 +58,9 @@ def lib() -> ctypes.CDLL:
             L.or_decode.restype = I
             L.or_decode.argtypes = [P, P, P, P, I, P, I, I, I, I, I, I, I, I, P, I, P, I,
                                     D, D, D, P, P, P, I, I]
+            L.or_decode_mq.restype = I
+            L.or_decode_mq.argtypes = [P, P, P, I, P, I, I, I, I, I, I, I, I, P, I, P, I, I,
+                                       D, D, D]
             L.or_append.restype = I
             L.or_append.argtypes = [P, I, I, I, I, I, I, I, P, P, I, P, I, P, I, F, F]
             L.or_append_tokens.restype = I
@@ -160,6 +163,28 @@ def decode(q, q_dtype, pool, kv_dtype, geom, layer, tables, seq_lens, scale,
     if rc != 0:
         raise ValueError(f"oracle decode rejected its inputs (code {rc})")
     return out, lse, wsum
+
+
+def decode_mq(q, q_dtype, pool, kv_dtype, geom, layer, tables, seq_lens, q_len, scale,
+              k_scale=1.0, v_scale=1.0):
+    """fp64 causal attention of the last q_len tokens of every sequence over its
+    paged K/V.  q [B, q_len, Hq, D] -> (out [B, q_len, Hq, D], lse [B, q_len, Hq])."""
+    q = np.ascontiguousarray(q)
+    pool = np.ascontiguousarray(pool)
+    tables = _i32(tables)
+    seq_lens = _i32(seq_lens)
+    B = seq_lens.shape[0]
+    Hq, D = geom["num_q_heads"], geom["head_dim"]
+    out = np.empty((B, q_len, Hq, D))
+    lse = np.empty((B, q_len, Hq))
+    rc = lib().or_decode_mq(_ptr(out), _ptr(lse), _ptr(q), DT[q_dtype], _ptr(pool), DT[kv_dtype],
+                            geom["num_blocks"], geom["num_layers"], geom["num_kv_heads"],
+                            geom["block_size"], D, Hq, layer, _ptr(tables), tables.shape[1],
+                            _ptr(seq_lens), B, int(q_len), float(scale), float(k_scale),
+                            float(v_scale))
+    if rc != 0:
+        raise ValueError(f"oracle decode_mq rejected its inputs (code {rc})")
+    return out, lse
 
 
 def append(pool, kv_dtype, geom, layer, k, v, in_dtype, tables, positions,

@@ -233,9 +233,9 @@ int or_append_tokens(void* pool, int kv_dtype, int NB, int L, int Hkv, int bs, i
  * mutant != 0 plants a deliberate mistake (used only by the tests that show
  * the pins catch such mistakes).
  */
-static double or_head(double* o, double* wsum_out, const void* q, int q_dtype, const void* pool,
-                      int kv_dtype, int L, int Hkv, int bs, int D, int Hq, int layer,
-                      const int32_t* table_row, int s, int hq, int tb, int te, double scale,
+static double or_head(double* o, double* wsum_out, const void* q, int q_dtype, size_t qrow,
+                      const void* pool, int kv_dtype, int L, int Hkv, int bs, int D, int Hq,
+                      int layer, const int32_t* table_row, int hq, int tb, int te, double scale,
                       double k_scale, double v_scale, double* sbuf, int mutant) {
   int G = Hq / Hkv;
   int h = (mutant == 1) ? (hq % Hkv) : (hq / G);
@@ -244,7 +244,7 @@ static double or_head(double* o, double* wsum_out, const void* q, int q_dtype, c
   for (int d = 0; d < D; ++d) o[d] = 0.0;
   if (wsum_out) *wsum_out = 0.0;
   if (te <= tb) return -INFINITY;
-  size_t qrow = ((size_t)s * Hq + hq) * (size_t)D;
+  qrow *= (size_t)D;   /* element offset of the query row */
   double m = -INFINITY;
   for (int j = tb; j < te; ++j) {
     int jj = (mutant == 2) ? (j + 1) % (te > tb ? te : 1) : j;
@@ -326,12 +326,68 @@ int or_decode(double* out, double* lse, double* wsum, const void* q, int q_dtype
         int tb = tok_begin ? tok_begin[s] : 0;
         int te = tok_end ? tok_end[s] : seq_lens[s];
         double ws = 0.0;
-        double l = or_head(o, &ws, q, q_dtype, pool, kv_dtype, L, Hkv, bs, D, Hq, layer,
-                           tables + (size_t)s * max_blocks, s, hq, tb, te, scale, k_scale,
-                           v_scale, sbuf, mutant);
+        double l = or_head(o, &ws, q, q_dtype, (size_t)s * Hq + hq, pool, kv_dtype, L, Hkv, bs,
+                           D, Hq, layer, tables + (size_t)s * max_blocks, hq, tb, te, scale,
+                           k_scale, v_scale, sbuf, mutant);
         memcpy(out + (size_t)row * D, o, sizeof(double) * (size_t)D);
         if (lse) lse[row] = l;
         if (wsum) wsum[row] = ws;
+      }
+    }
+    free(sbuf);
+    free(o);
+  }
+  return bad ? -3 : 0;
+}
+
+/*
+ * Multi-token decode ([UNLOCK 5.2] chunked prefill interleaved with decode,
+ * read for a chunk of q_len new tokens): sequence s holds n = seq_lens[s]
+ * tokens whose last q_len are the chunk's queries.  Query token i (position
+ * n - q_len + i) attends causally over tokens [0, n - q_len + i] -- the plain
+ * definition of causal attention, computed per row exactly like or_decode.
+ *   q   [B, q_len, Hq, D] ;  out [B, q_len, Hq, D] fp64 ;  lse [B, q_len, Hq] or NULL
+ * A query whose position is negative (n < q_len - i) attends to nothing: out 0,
+ * lse -inf.  Returns 0, -1 (geometry), -2 (block id out of range).
+ */
+int or_decode_mq(double* out, double* lse, const void* q, int q_dtype, const void* pool,
+                 int kv_dtype, int NB, int L, int Hkv, int bs, int D, int Hq, int layer,
+                 const int32_t* tables, int max_blocks, const int32_t* seq_lens, int B, int q_len,
+                 double scale, double k_scale, double v_scale) {
+  if (q_len < 1 || Hkv <= 0 || Hq % Hkv != 0 || layer < 0 || layer >= L) return -1;
+  int max_len = 0;
+  for (int s = 0; s < B; ++s) {
+    int n = seq_lens[s];
+    if (n > max_len) max_len = n;
+    int nblk = (n + bs - 1) / bs;
+    if (nblk > max_blocks) return -1;
+    for (int i = 0; i < nblk; ++i) {
+      int blk = tables[(size_t)s * max_blocks + i];
+      if (blk < 0 || blk >= NB) return -2;
+    }
+  }
+  long long total = (long long)B * q_len * Hq;
+  int bad = 0;
+#pragma omp parallel
+  {
+    double* sbuf = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+    double* o = (double*)malloc(sizeof(double) * (size_t)D);
+    if (!sbuf || !o) {
+#pragma omp atomic write
+      bad = 1;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (long long r = 0; r < total; ++r) {
+        int s = (int)(r / ((long long)q_len * Hq));
+        int i = (int)((r / Hq) % q_len);
+        int hq = (int)(r % Hq);
+        int te = seq_lens[s] - q_len + i + 1;        /* keys 0 .. position of query i */
+        if (te < 0) te = 0;
+        double l = or_head(o, NULL, q, q_dtype, ((size_t)s * q_len + i) * Hq + hq, pool,
+                           kv_dtype, L, Hkv, bs, D, Hq, layer, tables + (size_t)s * max_blocks,
+                           hq, 0, te, scale, k_scale, v_scale, sbuf, 0);
+        memcpy(out + (size_t)r * D, o, sizeof(double) * (size_t)D);
+        if (lse) lse[r] = l;
       }
     }
     free(sbuf);

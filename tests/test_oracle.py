@@ -344,3 +344,39 @@ def test_planted_mistakes_fail_a_pin(mutant):
     ref = _naive_case(case, tens)
     np.testing.assert_allclose(good, ref, atol=1e-12)
     assert np.max(np.abs(bad - ref)) > 1e-6, MUTANTS[mutant]
+
+
+# --------------------------------------------------------------------------- multi-token decode
+def _mq_q(case, q_len, seed=0):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(case.batch, q_len, case.num_q_heads, case.head_dim, generator=g).to(
+        wl.TORCH_DT[case.q_dtype])
+
+
+@pytest.mark.parametrize("q_len", [1, 2, 5])
+def test_multi_token_decode_equals_causal_naive_attention(q_len):
+    case = wl.make_case("mq", [q_len, 40, 77], 8, 2, 32, 16, "bf16", "bf16", "bf16", seed=120)
+    tens = wl.make_tensors(case)
+    pool = oracle_pool(case, tens, include_new=True)
+    q = _mq_q(case, q_len)
+    out, lse = oracle.decode_mq(np_raw(q), "bf16", pool, "bf16", case.geometry, 0, case.tables,
+                                case.seq_lens, q_len, case.scale)
+    qd = q.double().numpy()
+    G = case.num_q_heads // case.num_kv_heads
+    for s, (K, V) in enumerate(logical_kv(case, tens)):
+        n = int(case.seq_lens[s])
+        for i in range(q_len):
+            end = n - q_len + i + 1          # causal: keys up to the query's own position
+            for h in range(case.num_q_heads):
+                ref, w = _naive(qd[s, i, h], K[:end, h // G], V[:end, h // G], case.scale)
+                np.testing.assert_allclose(out[s, i, h], ref, rtol=0, atol=1e-12)
+
+
+def test_multi_token_decode_with_one_token_is_single_query_decode():
+    case = wl.make_case("mq1", [33, 100], 8, 2, 32, 16, "f32", "f32", "f32", seed=121)
+    tens = wl.make_tensors(case)
+    pool = oracle_pool(case, tens, include_new=True)
+    a, la = oracle.decode_mq(np_raw(tens.q).reshape(2, 1, 8, 32), "f32", pool, "f32",
+                             case.geometry, 0, case.tables, case.seq_lens, 1, case.scale)
+    b, lb, _ = _run_oracle(case, tens, pool)
+    assert np.array_equal(a[:, 0], b) and np.array_equal(la[:, 0], lb)
