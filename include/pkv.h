@@ -238,6 +238,28 @@ PKV_API int paged_decode_step(void* d_out, pkv_dtype out_dtype, const void* d_q,
                               int num_splits, void* d_workspace, size_t ws_bytes,
                               const pkv_launch_opts* opts, cudaStream_t stream);
 
+/* Multi-token decode: every sequence s has n = d_seq_lens[s] tokens in the pool,
+ * the last q_len of which are new (already stored, e.g. by kv_append_tokens).
+ * Query token i (0 <= i < q_len) of sequence s sits at position n - q_len + i and
+ * attends causally over tokens 0 .. n - q_len + i -- the chunked-prefill /
+ * speculative-verification reading of [UNLOCK] 5.2; q_len = 1 is
+ * paged_decode_attention.  A query whose position is negative gets out = 0.
+ * d_q and d_out: [batch, q_len, num_q_heads, head_dim].  The tensor-core kernel
+ * takes q_len * (num_q_heads / num_kv_heads) <= 16 (<= 8 at block_size 64);
+ * larger chunks return PKV_EUNSUPPORTED.  Other arguments and errors as in
+ * paged_decode_attention_ex; the workspace is paged_decode_workspace_bytes_mq. */
+PKV_API int paged_decode_attention_mq(void* d_out, pkv_dtype out_dtype, const void* d_q,
+                                      pkv_dtype q_dtype, int q_len, const pkv_pool* pool,
+                                      int layer, const int32_t* d_block_tables,
+                                      int max_blocks_per_seq, const int32_t* d_seq_lens,
+                                      int batch, int max_seq_len, float scale, float k_scale,
+                                      float v_scale, int num_splits, void* d_workspace,
+                                      size_t ws_bytes, const pkv_launch_opts* opts,
+                                      cudaStream_t stream);
+/* Workspace bytes of paged_decode_attention_mq (an upper bound over launch plans). */
+PKV_API size_t paged_decode_workspace_bytes_mq(const pkv_geometry* geom, int batch, int q_len,
+                                               int max_seq_len, int num_splits);
+
 /* Log-sum-exp merge of partial results ([SEQPAR] incremental softmax,
  * [ENG26] 3.1): for each row r = (s, h) of batch x num_q_heads,
  *   M = max_p lse[r,p],  w_p = exp(lse[r,p] - M),

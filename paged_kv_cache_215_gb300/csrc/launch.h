@@ -29,6 +29,8 @@ struct DecodeArgs {
   int stages;                // shared-memory pipeline depth
   int mode;                  // 0 balanced token stream, 1 fixed S partitions per sequence
   int S;                     // partitions per sequence in mode 1
+  int q_len;                 // query tokens per sequence (1: decode; >1: causal chunk)
+  int R;                     // query rows per KV head: q_len * G
   float qk_scale_log2;       // softmax scale * log2(e) (* k_scale for E4M3)
   float v_scale;             // v_scale for E4M3, else 1
   // Fused append (decode step): when k_new is set, the new token of sequence s
@@ -46,7 +48,7 @@ struct DecodeArgs {
 // Shared memory the tensor-core kernel needs for one CTA.
 size_t mma_stage_bytes(int kv_dtype, int BS, int HG);
 size_t mma_smem_bytes(int kv_dtype, int BS, int HG, int stages);
-bool mma_supported(int kv_dtype, int BS, int D, int G);
+bool mma_supported(int kv_dtype, int BS, int D, int G, int q_len);
 
 cudaError_t launch_decode_mma(const CUtensorMap* map, const DecodeArgs& a, int grid_x, int grid_y,
                               cudaStream_t stream);

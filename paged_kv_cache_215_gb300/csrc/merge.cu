@@ -135,8 +135,8 @@ __device__ void merge_row(const float* __restrict__ lse, size_t lse_stride,
 }
 
 // Balanced-stream partials: unit u = (s, hg) has `count` partials in slots
-// first .. first+count-1, each with HG*G heads; count 1 means the attention
-// kernel already wrote the output.
+// first .. first+count-1, each with HG*R rows (R = q_len * G); count 1 means the
+// attention kernel already wrote the output.
 __global__ void __launch_bounds__(kThreads) merge_units_kernel(const DecodeArgs a) {
   grid_dependency_wait();
   // the next launch may begin now: this grid's inputs are complete
@@ -144,12 +144,15 @@ __global__ void __launch_bounds__(kThreads) merge_units_kernel(const DecodeArgs 
   const int u = blockIdx.x, hl = blockIdx.y;
   const int2 info = a.unit_info[u];
   if (info.y == 1) return;
-  const int HGG = a.HG * a.G;
+  // row hl of a unit: KV head w of the group, column r = i * G + g (query token i, head g)
+  const int HGR = a.HG * a.R;
   const int s = u / a.NHG, hg = u % a.NHG;
-  const size_t out_off = ((size_t)s * a.Hq + (size_t)hg * HGG + hl) * a.D;
-  const size_t row0 = (size_t)info.x * HGG + hl;
-  merge_row(a.part_lse + row0, HGG, a.part_o + row0 * a.D, (size_t)HGG * a.D, info.y, a.D, a.out,
-            out_off, a.out_dtype);
+  const int w = hl / a.R, r = hl % a.R;
+  const int i = r / a.G, g = r % a.G;
+  const size_t q_row = ((size_t)s * a.q_len + i) * a.Hq + (size_t)(hg * a.HG + w) * a.G + g;
+  const size_t row0 = (size_t)info.x * HGR + hl;
+  merge_row(a.part_lse + row0, HGR, a.part_o + row0 * a.D, (size_t)HGR * a.D, info.y, a.D, a.out,
+            q_row * a.D, a.out_dtype);
 }
 
 // [rows, S, D] partials (the layout of the public merge_partials).
@@ -188,7 +191,7 @@ cudaError_t launch_merge_units(const DecodeArgs& a, bool pdl, cudaStream_t strea
   DecodeArgs copy = a;
   void* args[] = {&copy};
   return launch_pdl(reinterpret_cast<const void*>(merge_units_kernel),
-                    dim3(units, a.HG * a.G), args, pdl, stream);
+                    dim3(units, a.HG * a.R), args, pdl, stream);
 }
 
 cudaError_t launch_merge_rows(void* out, int out_dtype, const float* part_o, const float* part_lse,

@@ -137,10 +137,10 @@ static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 struct BalancedWs {
   size_t o_off, lse_off, info_off, bytes;
 };
-static BalancedWs balanced_ws(const pkv_geometry& g, int batch, const MmaPlan& p) {
+static BalancedWs balanced_ws(const pkv_geometry& g, int batch, int q_len, const MmaPlan& p) {
   const size_t units = (size_t)batch * p.NHG;
   const size_t slots = (size_t)p.grid + units;
-  const size_t hgg = (size_t)p.HG * (g.num_q_heads / g.num_kv_heads);
+  const size_t hgg = (size_t)p.HG * (g.num_q_heads / g.num_kv_heads) * q_len;
   BalancedWs w;
   w.o_off = 0;
   w.lse_off = align256(slots * hgg * g.head_dim * sizeof(float));
@@ -149,9 +149,9 @@ static BalancedWs balanced_ws(const pkv_geometry& g, int batch, const MmaPlan& p
   return w;
 }
 
-// Fixed-split workspace: [B, Hq, S, D] and [B, Hq, S].
-static size_t fixed_ws(const pkv_geometry& g, int batch, int S, size_t* lse_off) {
-  const size_t rows = (size_t)batch * g.num_q_heads * S;
+// Fixed-split workspace: [B, q_len, Hq, S, D] and [B, q_len, Hq, S].
+static size_t fixed_ws(const pkv_geometry& g, int batch, int q_len, int S, size_t* lse_off) {
+  const size_t rows = (size_t)batch * q_len * g.num_q_heads * S;
   const size_t o = align256(rows * g.head_dim * sizeof(float));
   if (lse_off) *lse_off = o;
   return S > 1 ? o + align256(rows * sizeof(float)) : 0;
@@ -428,13 +428,14 @@ int kv_absmax(const void* d_x, pkv_dtype dtype, int64_t n, float* d_amax, cudaSt
   return launch_absmax(d_x, dtype, n, d_amax, stream) == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
-size_t paged_decode_workspace_bytes(const pkv_geometry* g, int batch, int max_seq_len,
-                                    int num_splits) {
-  if (!geometry_ok(g) || batch < 0 || max_seq_len < 0 || num_splits < 0) return 0;
+size_t paged_decode_workspace_bytes_mq(const pkv_geometry* g, int batch, int q_len,
+                                       int max_seq_len, int num_splits) {
+  if (!geometry_ok(g) || batch < 0 || q_len < 1 || max_seq_len < 0 || num_splits < 0) return 0;
   DeviceInfo dev;
   if (!device_info(&dev)) return 0;
-  if (num_splits > 0) return fixed_ws(*g, batch, num_splits, nullptr) + 256;
-  size_t need = fixed_ws(*g, batch, simt_auto_splits(*g, batch, max_seq_len, dev.sms), nullptr);
+  if (num_splits > 0) return fixed_ws(*g, batch, q_len, num_splits, nullptr) + 256;
+  size_t need = fixed_ws(*g, batch, q_len, simt_auto_splits(*g, batch, max_seq_len, dev.sms),
+                         nullptr);
   for (int hg = 1; hg <= 8; ++hg) {
     if (!hg_ok(*g, hg)) continue;
     for (int c = 1; c <= 4; ++c) {
@@ -442,17 +443,22 @@ size_t paged_decode_workspace_bytes(const pkv_geometry* g, int batch, int max_se
       p.HG = hg;
       p.NHG = g->num_kv_heads / hg;
       p.grid = dev.sms * c;
-      need = std::max(need, balanced_ws(*g, batch, p).bytes);
+      need = std::max(need, balanced_ws(*g, batch, q_len, p).bytes);
     }
   }
   return need + 256;
+}
+
+size_t paged_decode_workspace_bytes(const pkv_geometry* g, int batch, int max_seq_len,
+                                    int num_splits) {
+  return paged_decode_workspace_bytes_mq(g, batch, 1, max_seq_len, num_splits);
 }
 
 // Shared body of paged_decode_attention_ex and paged_decode_step.  With k_new
 // set, every sequence's new token is first stored at position seq_lens[s] - 1
 // (fused into the tensor-core kernel, or a separate append launch otherwise).
 static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_dtype q_dtype,
-                         const void* d_k_new, const void* d_v_new, int new_dtype,
+                         int q_len, const void* d_k_new, const void* d_v_new, int new_dtype,
                          const pkv_pool* pool, int layer, const int32_t* d_block_tables,
                          int max_blocks_per_seq, const int32_t* d_seq_lens, int batch,
                          int max_seq_len, float scale, float k_scale, float v_scale,
@@ -460,10 +466,11 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
                          const pkv_launch_opts* opts, cudaStream_t stream) {
   pkv_pool* p = const_cast<pkv_pool*>(pool);
   if (!p || batch < 0 || max_seq_len < 0 || num_splits < 0 || layer < 0 ||
-      layer >= p->g.num_layers)
+      layer >= p->g.num_layers || q_len < 1)
     return PKV_EINVAL;
   if (batch == 0) return PKV_OK;
   const pkv_geometry& g = p->g;
+  if (q_len > 1 && d_k_new) return PKV_EINVAL;
   if (!d_out || !d_q || !d_block_tables || !d_seq_lens || max_blocks_per_seq < 1)
     return PKV_EINVAL;
   if (!act_dtype(out_dtype) || !act_dtype(q_dtype) || !aligned16(d_q) || !aligned16(d_out))
@@ -490,8 +497,8 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
   const int G = g.num_q_heads / g.num_kv_heads;
   const bool q_ok_mma = fp8 ? true
                             : (g.kv_dtype == PKV_BF16 ? q_dtype == PKV_BF16 : q_dtype == PKV_F16);
-  const bool mma_ok = mma_supported(g.kv_dtype, g.block_size, g.head_dim, G) && q_ok_mma;
-  const bool simt_ok = g.head_dim % 32 == 0 && g.head_dim <= 256 && G <= 16;
+  const bool mma_ok = mma_supported(g.kv_dtype, g.block_size, g.head_dim, G, q_len) && q_ok_mma;
+  const bool simt_ok = g.head_dim % 32 == 0 && g.head_dim <= 256 && G <= 16 && q_len == 1;
   bool use_mma;
   if (kernel == 2) {
     if (!mma_ok) return PKV_EUNSUPPORTED;
@@ -529,6 +536,8 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
   a.k_enc_scale = k_scale;
   a.v_enc_scale = v_scale;
   a.new_dtype = new_dtype;
+  a.q_len = q_len;
+  a.R = G * q_len;
   if (d_workspace && !aligned16(d_workspace)) return PKV_EINVAL;
   char* ws = static_cast<char*>(d_workspace);
 
@@ -574,7 +583,7 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
     const CUtensorMap* map = p->tmap(plan.HG);
     if (!map) return PKV_ECUDA;
     if (num_splits == 0) {
-      const BalancedWs w = balanced_ws(g, batch, plan);
+      const BalancedWs w = balanced_ws(g, batch, q_len, plan);
       if (!ws || ws_bytes < w.bytes) return PKV_ENOMEM;
       a.mode = 0;
       a.S = 0;
@@ -587,7 +596,7 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
       return PKV_OK;
     }
     size_t lse_off = 0;
-    const size_t need = fixed_ws(g, batch, num_splits, &lse_off);
+    const size_t need = fixed_ws(g, batch, q_len, num_splits, &lse_off);
     if (num_splits > 1 && (!ws || ws_bytes < need)) return PKV_ENOMEM;
     a.mode = 1;
     a.S = num_splits;
@@ -598,7 +607,7 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
     if (phase != 2 && launch_decode_mma(map, a, num_splits, (int)units, stream) != cudaSuccess)
       return PKV_ECUDA;
     if (num_splits > 1 && phase != 1 &&
-        launch_merge_rows(d_out, out_dtype, a.part_o, a.part_lse, batch * g.num_q_heads,
+        launch_merge_rows(d_out, out_dtype, a.part_o, a.part_lse, batch * q_len * g.num_q_heads,
                           num_splits, g.head_dim, phase == 0, stream) != cudaSuccess)
       return PKV_ECUDA;
     return PKV_OK;
@@ -608,7 +617,7 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
   const int S = num_splits > 0 ? num_splits : simt_auto_splits(g, batch, max_seq_len, dev.sms);
   if (batch > 65535 || g.num_kv_heads > 65535) return PKV_EUNSUPPORTED;
   size_t lse_off = 0;
-  const size_t need = fixed_ws(g, batch, S, &lse_off);
+  const size_t need = fixed_ws(g, batch, 1, S, &lse_off);
   if (S > 1 && (!ws || ws_bytes < need)) return PKV_ENOMEM;
   a.mode = 1;
   a.S = S;
@@ -630,7 +639,18 @@ int paged_decode_attention_ex(void* d_out, pkv_dtype out_dtype, const void* d_q,
                               int max_seq_len, float scale, float k_scale, float v_scale,
                               int num_splits, void* d_workspace, size_t ws_bytes,
                               const pkv_launch_opts* opts, cudaStream_t stream) {
-  return decode_common(d_out, out_dtype, d_q, q_dtype, nullptr, nullptr, 0, pool, layer,
+  return decode_common(d_out, out_dtype, d_q, q_dtype, 1, nullptr, nullptr, 0, pool, layer,
+                       d_block_tables, max_blocks_per_seq, d_seq_lens, batch, max_seq_len, scale,
+                       k_scale, v_scale, num_splits, d_workspace, ws_bytes, opts, stream);
+}
+
+int paged_decode_attention_mq(void* d_out, pkv_dtype out_dtype, const void* d_q,
+                              pkv_dtype q_dtype, int q_len, const pkv_pool* pool, int layer,
+                              const int32_t* d_block_tables, int max_blocks_per_seq,
+                              const int32_t* d_seq_lens, int batch, int max_seq_len, float scale,
+                              float k_scale, float v_scale, int num_splits, void* d_workspace,
+                              size_t ws_bytes, const pkv_launch_opts* opts, cudaStream_t stream) {
+  return decode_common(d_out, out_dtype, d_q, q_dtype, q_len, nullptr, nullptr, 0, pool, layer,
                        d_block_tables, max_blocks_per_seq, d_seq_lens, batch, max_seq_len, scale,
                        k_scale, v_scale, num_splits, d_workspace, ws_bytes, opts, stream);
 }
@@ -643,7 +663,7 @@ int paged_decode_step(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_dty
                       void* d_workspace, size_t ws_bytes, const pkv_launch_opts* opts,
                       cudaStream_t stream) {
   if (!d_k_new) return PKV_EINVAL;
-  return decode_common(d_out, out_dtype, d_q, q_dtype, d_k_new, d_v_new, new_dtype, pool, layer,
+  return decode_common(d_out, out_dtype, d_q, q_dtype, 1, d_k_new, d_v_new, new_dtype, pool, layer,
                        d_block_tables, max_blocks_per_seq, d_seq_lens, batch, max_seq_len, scale,
                        k_scale, v_scale, num_splits, d_workspace, ws_bytes, opts, stream);
 }

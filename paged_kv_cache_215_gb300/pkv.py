@@ -71,6 +71,9 @@ def _load() -> ctypes.CDLL:
         "kv_append_tokens": (I, [P, I, P, P, I, P, I, I, P, P, I64, F, F, P]),
         "kv_absmax": (I, [P, I, I64, P, P]),
         "paged_decode_workspace_bytes": (Z, [G, I, I, I]),
+        "paged_decode_workspace_bytes_mq": (Z, [G, I, I, I, I]),
+        "paged_decode_attention_mq": (I, [P, I, P, I, I, P, I, P, I, P, I, I, F, F, F, I, P, Z,
+                                          ctypes.POINTER(LaunchOpts), P]),
         "paged_decode_attention": (I, [P, I, P, I, P, I, P, I, P, I, I, F, F, F, I, P, Z, P]),
         "paged_decode_attention_ex": (I, [P, I, P, I, P, I, P, I, P, I, I, F, F, F, I, P, Z,
                                           ctypes.POINTER(LaunchOpts), P]),
@@ -96,6 +99,7 @@ EXPORTS = ("kv_pool_bytes", "kv_pool_create", "kv_pool_destroy", "kv_pool_geomet
            "kv_append_tokens", "kv_absmax", "paged_decode_workspace_bytes",
            "paged_decode_attention", "paged_decode_attention_ex", "merge_partials",
            "paged_decode_attention_static", "paged_decode_step",
+           "paged_decode_attention_mq", "paged_decode_workspace_bytes_mq",
            "pkv_check_status", "pkv_strerror", "pkv_launch_count")
 
 
@@ -293,6 +297,25 @@ def paged_decode_step(out, q, k_new, v_new, pool: KVPool, layer, tables, seq_len
         _ptr(seq_lens), q.shape[0], max_seq_len, scale, k_scale, v_scale, num_splits,
         _ptr(workspace), workspace.numel(), None if opts is None else ctypes.byref(opts),
         _stream(stream)), "paged_decode_step")
+    return out
+
+
+def paged_decode_attention_mq(out, q, pool: KVPool, layer, tables, seq_lens, max_seq_len, scale,
+                              k_scale=1.0, v_scale=1.0, num_splits=0, workspace=None, opts=None,
+                              stream=None):
+    """Causal attention of the last q_len tokens of every sequence (q, out:
+    [B, q_len, Hq, D]) over the paged pool, the new tokens already stored."""
+    B, q_len = q.shape[0], q.shape[1]
+    if workspace is None:
+        nb = int(_lib.paged_decode_workspace_bytes_mq(ctypes.byref(pool.geom), B, q_len,
+                                                      max_seq_len, num_splits))
+        workspace = torch.empty(max(nb, 16), dtype=torch.uint8, device=q.device)
+    _check(_lib.paged_decode_attention_mq(
+        _ptr(out), TORCH_CODE[out.dtype], _ptr(q), TORCH_CODE[q.dtype], q_len, pool.handle, layer,
+        _ptr(tables), tables.shape[1], _ptr(seq_lens), B, max_seq_len, scale, k_scale, v_scale,
+        num_splits, _ptr(workspace), workspace.numel(),
+        None if opts is None else ctypes.byref(opts), _stream(stream)),
+        "paged_decode_attention_mq")
     return out
 
 
