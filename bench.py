@@ -17,6 +17,7 @@ Rank 0 prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -40,9 +41,10 @@ METRIC = "paged decode attn KV GB/s (fraction of HBM peak); decode tokens/s at 1
 UNIT = "GB/s"
 PRIMARY = "long_128k"
 SECONDARY = ["llama8b_b32_8k", "long_1m", "fp8_b8_32k", "llama70b_prefix_bs16",
-             "llama70b_prefix_bs32"]
+             "llama70b_prefix_bs32", "long_128k_bs64", "llama8b_b32_8k_layers4"]
 MODEL_LAYERS = {"long_128k": 32, "long_1m": 32, "llama8b_b32_8k": 32, "fp8_b8_32k": 32,
-                "llama70b_prefix_bs16": 80, "llama70b_prefix_bs32": 80}
+                "llama70b_prefix_bs16": 80, "llama70b_prefix_bs32": 80, "long_128k_bs64": 32,
+                "llama8b_b32_8k_layers4": 32}
 KERNEL_SOURCES = ["paged_kv_cache_215_gb300/csrc/decode_mma.cu",
                   "paged_kv_cache_215_gb300/csrc/device.cuh"]
 
@@ -407,6 +409,43 @@ def aggregate_ranks(ms_per_step, kv_bytes_per_step, device="cpu"):
     return ms, float(t[1].item()) / (ms * 1e-3) / 1e9
 
 
+def measure_multi_token(base, q_len, steps, device):
+    """Multi-token decode (q_len new tokens per sequence, causal within the chunk)
+    on a full-size workload: store the chunk's tokens, then one attention launch
+    (+ merge), timed per step with CUDA events."""
+    from paged_kv_cache_215_gb300 import pkv
+    w = Workload(base, device)
+    c = w.case
+    g = torch.Generator(device=device).manual_seed(77)
+    q = torch.randn(c.batch, q_len, c.num_q_heads, c.head_dim, generator=g,
+                    device=device).to(torch.bfloat16)
+    out = torch.empty(c.batch, q_len, c.num_q_heads, c.head_dim, dtype=torch.bfloat16,
+                      device=device)
+    nb = int(pkv.lib().paged_decode_workspace_bytes_mq(ctypes.byref(w.geom), c.batch, q_len,
+                                                       w.max_len, 0))
+    ws = torch.empty(nb, dtype=torch.uint8, device=device)
+
+    def step():
+        pkv.paged_decode_attention_mq(out, q, w.pool, c.layer, w.tables, w.seq_lens, w.max_len,
+                                      c.scale, w.ks, w.vs, 0, ws)
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    w.close()
+    del w
+    torch.cuda.empty_cache()
+    return {"q_len": q_len, "ms_per_step": ms, "kv_gbs": kv_bytes(c) / (ms * 1e-3) / 1e9,
+            "roofline_frac": kv_bytes(c) / (ms * 1e-3) / 1e9 / peaks()[0],
+            "query_tokens_per_s_per_layer": c.batch * q_len / (ms * 1e-3), "batch": c.batch}
+
+
 def run_ours(args):
     ws, rank, local = dist_env()
     if ws > 1:
@@ -445,6 +484,9 @@ def run_ours(args):
             others[other]["achieved_gbs"] = ores["roofline"]["achieved"]
             if "unique_kv_gbs" in ores:
                 others[other]["unique_kv_gbs"] = ores["unique_kv_gbs"]
+    if rank == 0 and not args.only_primary:
+        for mq_name, (base, q_len) in wl.MULTI_TOKEN.items():
+            others[mq_name] = measure_multi_token(base, q_len, max(50, args.steps // 20), device)
     if ws > 1:
         dist.barrier()
     if rank != 0:

@@ -170,6 +170,21 @@ def llama70b_prefix(batch=64, lo=512, hi=131072, block_size=16, prefix=4096, see
                      shared_prefix_tokens=prefix)
 
 
+def llama8b_layers(num_layers=4, layer=2, batch=32, lo=4096, hi=12288, seed=1005) -> Case:
+    """The 8B-shaped batch in a pool holding several layers; one layer is read."""
+    g = _gen(seed)
+    lens = torch.randint(lo, hi + 1, (batch,), generator=g).numpy().astype(np.int32)
+    return make_case(f"llama8b_decode_b{batch}_len{lo}-{hi}_L{num_layers}_layer{layer}", lens, 32,
+                     8, 128, 16, "bf16", "bf16", "bf16", seed=seed, num_layers=num_layers,
+                     layer=layer)
+
+
+def long_context_bs64(tokens=131072, seed=1006) -> Case:
+    """The 128K request in 64-token blocks."""
+    return make_case(f"long_context_b1_{tokens}_bs64", [tokens], 32, 8, 128, 64, "bf16", "bf16",
+                     "bf16", seed=seed, spike_frac=0.01)
+
+
 FULL = {
     "tiny": tiny_gqa2_d64_f32,
     "llama8b_b32_8k": lambda: llama8b_batch(),
@@ -178,7 +193,12 @@ FULL = {
     "fp8_b8_32k": lambda: fp8_batch(),
     "llama70b_prefix_bs16": lambda: llama70b_prefix(block_size=16),
     "llama70b_prefix_bs32": lambda: llama70b_prefix(block_size=32),
+    "long_128k_bs64": lambda: long_context_bs64(),
+    "llama8b_b32_8k_layers4": lambda: llama8b_layers(),
 }
+
+# query tokens per sequence of the multi-token (speculative verification) measurements
+MULTI_TOKEN = {"llama8b_b32_8k_q4": ("llama8b_b32_8k", 4)}
 
 
 # ---------------------------------------------------------------------------
