@@ -195,7 +195,9 @@ PKV_API int paged_decode_attention(void* d_out, pkv_dtype out_dtype, const void*
 /* Launch choices a caller may force (tests, ablations, benchmarks).  Zero-filled
  * means "automatic" for every field. */
 typedef struct {
-  int32_t kernel;          /* 0 auto, 1 the SIMT kernel, 2 the tensor-core (mma) kernel */
+  int32_t kernel;          /* 0 auto, 1 the SIMT kernel, 2 the mma.sync tensor-core kernel,
+                              3 the tcgen05 chunked-prefill kernel (multi-token calls,
+                              bf16/f16 pools, q dtype = pool dtype, num_splits = 0) */
   int32_t ctas_per_sm;     /* 0 auto; the persistent grid is SMs x this */
   int32_t kv_heads_per_cta;/* 0 auto */
   int32_t stages;          /* 0 auto; shared-memory pipeline depth */
@@ -245,8 +247,11 @@ PKV_API int paged_decode_step(void* d_out, pkv_dtype out_dtype, const void* d_q,
  * speculative-verification reading of [UNLOCK] 5.2; q_len = 1 is
  * paged_decode_attention.  A query whose position is negative gets out = 0.
  * d_q and d_out: [batch, q_len, num_q_heads, head_dim].  The tensor-core kernel
- * takes q_len * (num_q_heads / num_kv_heads) <= 16 (<= 8 at block_size 64);
- * larger chunks return PKV_EUNSUPPORTED.  Other arguments and errors as in
+ * (mma.sync) takes q_len * (num_q_heads / num_kv_heads) <= 16 rows per KV head
+ * (<= 8 at block_size 64); larger chunks on bf16 / f16 pools (q in the pool's
+ * dtype) run on the tcgen05 kernel: UMMA tiles of 128 query rows x 64 keys with
+ * S and O in tensor memory (num_splits must be 0 there).  Other combinations
+ * return PKV_EUNSUPPORTED.  Other arguments and errors as in
  * paged_decode_attention_ex; the workspace is paged_decode_workspace_bytes_mq. */
 PKV_API int paged_decode_attention_mq(void* d_out, pkv_dtype out_dtype, const void* d_q,
                                       pkv_dtype q_dtype, int q_len, const pkv_pool* pool,

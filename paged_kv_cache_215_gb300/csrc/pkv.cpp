@@ -489,7 +489,7 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
   const int phase = opts ? opts->phase : 0;
   const int kernel = opts ? opts->kernel : 0;
   const int pdl = opts ? opts->pdl : 0;
-  if (phase < 0 || phase > 2 || kernel < 0 || kernel > 2 || pdl < 0 || pdl > 1)
+  if (phase < 0 || phase > 2 || kernel < 0 || kernel > 3 || pdl < 0 || pdl > 1)
     return PKV_EINVAL;
   DeviceInfo dev;
   if (!device_info(&dev)) return PKV_ECUDA;
@@ -499,6 +499,41 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
                             : (g.kv_dtype == PKV_BF16 ? q_dtype == PKV_BF16 : q_dtype == PKV_F16);
   const bool mma_ok = mma_supported(g.kv_dtype, g.block_size, g.head_dim, G, q_len) && q_ok_mma;
   const bool simt_ok = g.head_dim % 32 == 0 && g.head_dim <= 256 && G <= 16 && q_len == 1;
+  // chunks with more query rows per KV head than the mma.sync kernel holds go to
+  // the tcgen05 chunked-prefill kernel (also forced with kernel = 3)
+  const bool tc_ok = !fused_append && prefill_tc_supported(g.kv_dtype, q_dtype, g.block_size,
+                                                           g.head_dim, G);
+  if (kernel == 3 || (kernel == 0 && q_len > 1 && !mma_ok && tc_ok)) {
+    if (!tc_ok) return PKV_EUNSUPPORTED;
+    if (num_splits != 0 || phase == 2) return phase == 2 ? PKV_OK : PKV_EUNSUPPORTED;
+    if (batch > 65535 || g.num_kv_heads > 65535) return PKV_EUNSUPPORTED;
+    const CUtensorMap* map = p->tmap(1);
+    if (!map) return PKV_ECUDA;
+    DecodeArgs t{};
+    t.q = d_q;
+    t.out = d_out;
+    t.tables = d_block_tables;
+    t.seq_lens = d_seq_lens;
+    t.status = p->d_status;
+    t.B = batch;
+    t.Hq = g.num_q_heads;
+    t.Hkv = g.num_kv_heads;
+    t.G = G;
+    t.D = g.head_dim;
+    t.BS = g.block_size;
+    t.L = g.num_layers;
+    t.layer = layer;
+    t.max_blocks = max_blocks_per_seq;
+    t.num_blocks = g.num_blocks;
+    t.q_dtype = q_dtype;
+    t.out_dtype = out_dtype;
+    t.kv_dtype = g.kv_dtype;
+    t.q_len = q_len;
+    t.R = G * q_len;
+    t.qk_scale_log2 = (float)((double)scale * 1.4426950408889634);
+    t.v_scale = 1.f;
+    return launch_prefill_tc(map, t, stream) == cudaSuccess ? PKV_OK : PKV_ECUDA;
+  }
   bool use_mma;
   if (kernel == 2) {
     if (!mma_ok) return PKV_EUNSUPPORTED;

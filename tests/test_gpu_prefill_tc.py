@@ -1,0 +1,71 @@
+"""Chunked prefill on the tcgen05 kernel (needs a GPU): the last q_len tokens of
+every sequence attend causally over the paged pool, many query rows per KV
+head (UMMA tiles of 128 rows).  CUDA path vs the fp64 oracle's causal decode:
+max |err| <= 2e-3 x max|V| per sequence."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_215_gb300 import workloads as wl
+from tests.gpu_harness import TOL, GpuCase, oracle_side, vmax_per_seq
+from tests.helpers import np_raw
+
+pytestmark = pytest.mark.gpu
+
+
+def _q(case, q_len, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(case.batch, q_len, case.num_q_heads, case.head_dim, generator=g).to(
+        wl.TORCH_DT[case.q_dtype])
+
+
+CASES = [
+    (wl.make_case("tc_g4_bs16", [300, 1000, 40], 32, 8, 128, 16, "bf16", "bf16", "bf16",
+                  seed=80), [17, 64, 100]),
+    (wl.make_case("tc_g8_bs32", [500, 2000], 64, 8, 128, 32, "bf16", "bf16", "bf16", seed=81),
+     [48]),
+    (wl.make_case("tc_f16_bs64", [700, 129], 32, 8, 128, 64, "f16", "f16", "f16", seed=82),
+     [130]),
+    (wl.make_case("tc_mha_bs16", [260, 77], 4, 4, 128, 16, "bf16", "bf16", "bf16", seed=83),
+     [128, 200]),
+]
+
+
+def _check(case, q_lens, kernel):
+    from paged_kv_cache_215_gb300 import pkv
+    tens = wl.make_tensors(case)
+    gc = GpuCase(case, tens)
+    gc.pool.append(case.layer, gc.k_new, gc.v_new, gc.tables, gc.new_pos)
+    pool, _, seqs = oracle_side(case, tens, None)
+    vm = vmax_per_seq(case, pool, seqs, 1.0)
+    worst = 0.0
+    for q_len in q_lens:
+        q = _q(case, q_len, seed=q_len)
+        ref, _ = oracle.decode_mq(np_raw(q), case.q_dtype, pool, case.kv_dtype, case.geometry,
+                                  case.layer, case.tables, case.seq_lens, q_len, case.scale)
+        out = torch.full((case.batch, q_len, case.num_q_heads, case.head_dim), float("nan"),
+                         device="cuda")
+        pkv.paged_decode_attention_mq(out, q.cuda(), gc.pool, case.layer, gc.tables,
+                                      gc.seq_lens, gc.max_seq_len, case.scale,
+                                      opts=pkv.launch_opts(kernel=kernel) if kernel else None)
+        torch.cuda.synchronize()
+        assert gc.status() == 0
+        got = out.double().cpu().numpy()
+        assert np.all(np.isfinite(got))
+        for s in seqs:
+            err = np.abs(got[s] - ref[s]).max()
+            bound = TOL[case.kv_dtype] * vm[s]
+            worst = max(worst, err / bound)
+            assert err <= bound, f"{case.name} q_len {q_len} seq {s}: {err} > {bound}"
+    return worst
+
+
+@pytest.mark.parametrize("case,q_lens", CASES, ids=lambda c: getattr(c, "name", ""))
+def test_chunked_prefill_tcgen05_parity(case, q_lens):
+    _check(case, q_lens, kernel=0)
+
+
+def test_tcgen05_kernel_forced_on_short_chunks():
+    case = wl.make_case("tc_forced", [90, 33, 5], 32, 8, 128, 16, "bf16", "bf16", "bf16", seed=84)
+    _check(case, [1, 2, 7], kernel=3)
