@@ -446,6 +446,58 @@ def measure_multi_token(base, q_len, steps, device):
             "query_tokens_per_s_per_layer": c.batch * q_len / (ms * 1e-3), "batch": c.batch}
 
 
+def measure_chunked_prefill(device, batch=4, context=16384, chunk=2048, steps=20):
+    """Chunked prefill on the tcgen05 kernel: `batch` sequences of `context` tokens
+    (32 query / 8 KV heads, D 128, bf16, bs 16) whose last `chunk` tokens are the
+    new queries, causal within the chunk.  Work = 4 * D flops per (query head, visible key)."""
+    from paged_kv_cache_215_gb300 import pkv
+    case = wl.make_case(f"chunked_prefill_b{batch}_ctx{context}_chunk{chunk}", [context] * batch,
+                        32, 8, 128, 16, "bf16", "bf16", "bf16", seed=1007)
+    t = wl.make_tensors(case, device=device)
+    geom = pkv.geometry(1, 32, 8, 128, 16, case.num_blocks, "bf16")
+    pool = pkv.KVPool(geom, device=device)
+    pool.storage.zero_()
+    ids = case.tables[case.tables >= 0]
+    pool.reserve(np.unique(ids).tolist())
+    tables = torch.from_numpy(case.tables).to(device)
+    lens = torch.from_numpy(case.seq_lens).to(device)
+    pool.append_tokens(0, t.k_tokens, t.v_tokens, tables, t.tok_seq, t.tok_pos)
+    pool.append(0, t.k_new, t.v_new, tables, t.new_pos)
+    g = torch.Generator(device=device).manual_seed(78)
+    q = torch.randn(batch, chunk, 32, 128, generator=g, device=device).to(torch.bfloat16)
+    out = torch.empty(batch, chunk, 32, 128, dtype=torch.bfloat16, device=device)
+    ws = torch.empty(16, dtype=torch.uint8, device=device)
+
+    def step():
+        pkv.paged_decode_attention_mq(out, q, pool, 0, tables, lens, context, case.scale,
+                                      workspace=ws)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    keys = sum(context - chunk + i + 1 for i in range(chunk))      # visible keys per query row
+    flops = 4.0 * 128 * 32 * keys * batch
+    pool.close()
+    peak = bf16_peak()
+    return {"workload": case.name, "ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+            "roofline": {"bound": "tensor", "peak": peak, "unit": "TFLOP/s",
+                         "frac": flops / (ms * 1e-3) / 1e12 / peak},
+            "query_tokens_per_s": batch * chunk / (ms * 1e-3)}
+
+
+def bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p))["bf16_tflops"])
+    return 1900.0
+
+
 def run_ours(args):
     ws, rank, local = dist_env()
     if ws > 1:
@@ -487,6 +539,8 @@ def run_ours(args):
     if rank == 0 and not args.only_primary:
         for mq_name, (base, q_len) in wl.MULTI_TOKEN.items():
             others[mq_name] = measure_multi_token(base, q_len, max(50, args.steps // 20), device)
+        cp = measure_chunked_prefill(device)
+        others[cp.pop("workload")] = cp
     if ws > 1:
         dist.barrier()
     if rank != 0:

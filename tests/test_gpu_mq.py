@@ -77,13 +77,31 @@ def test_multi_token_decode_with_one_token_equals_decode():
     assert torch.equal(out[:, 0], single)
 
 
-def test_multi_token_decode_rejects_too_many_rows():
+def test_large_chunks_route_to_tcgen05_or_are_refused():
+    """More than 16 query rows per KV head: bf16 pools run on the tcgen05 kernel
+    (checked against the oracle); E4M3 pools have no kernel for it."""
     from paged_kv_cache_215_gb300 import pkv
     case = wl.llama8b_batch(batch=2, lo=100, hi=200, seed=67)
-    gc = GpuCase(case)
-    q = torch.zeros(2, 5, 32, 128, dtype=torch.bfloat16, device="cuda")   # 5 x 4 = 20 rows
+    tens = wl.make_tensors(case)
+    gc = GpuCase(case, tens)
+    gc.pool.append(case.layer, gc.k_new, gc.v_new, gc.tables, gc.new_pos)
+    pool, _, seqs = oracle_side(case, tens, None)
+    q = _q(case, 5, seed=5)                                      # 5 x 4 = 20 rows
+    ref, _ = oracle.decode_mq(np_raw(q), "bf16", pool, "bf16", case.geometry, 0, case.tables,
+                              case.seq_lens, 5, case.scale)
     out = torch.empty(2, 5, 32, 128, device="cuda")
+    pkv.paged_decode_attention_mq(out, q.cuda(), gc.pool, 0, gc.tables, gc.seq_lens,
+                                  gc.max_seq_len, case.scale)
+    torch.cuda.synchronize()
+    vm = vmax_per_seq(case, pool, seqs, 1.0)
+    got = out.double().cpu().numpy()
+    for s_ in seqs:
+        assert np.abs(got[s_] - ref[s_]).max() <= TOL["bf16"] * vm[s_]
+    c8 = wl.make_case("mq_fp8_big", [300], 32, 8, 128, 16, "e4m3", "bf16", "bf16", seed=68)
+    g8 = GpuCase(c8)
+    q8 = torch.zeros(1, 5, 32, 128, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(pkv.PkvError) as e:
-        pkv.paged_decode_attention_mq(out, q, gc.pool, 0, gc.tables, gc.seq_lens,
-                                      gc.max_seq_len, case.scale)
+        pkv.paged_decode_attention_mq(torch.empty(1, 5, 32, 128, device="cuda"), q8, g8.pool, 0,
+                                      g8.tables, g8.seq_lens, g8.max_seq_len, c8.scale,
+                                      g8.k_scale, g8.v_scale)
     assert e.value.code == pkv.PKV_EUNSUPPORTED
