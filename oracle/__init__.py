@@ -57,15 +57,17 @@ def lib() -> ctypes.CDLL:
             LL = ctypes.c_longlong
             L.or_decode.restype = I
             L.or_decode.argtypes = [P, P, P, P, I, P, I, I, I, I, I, I, I, I, P, I, P, I,
-                                    D, D, D, P, P, P, I, I]
+                                    D, D, D, P, P, P, I, I, P]
             L.or_decode_mq.restype = I
             L.or_decode_mq.argtypes = [P, P, P, I, P, I, I, I, I, I, I, I, I, P, I, P, I, I,
-                                       D, D, D]
+                                       D, D, D, P]
+            L.or_block_scales.restype = I
+            L.or_block_scales.argtypes = [P, I, I, I, I, I, I, P, P, I, P, I, I, P, P, LL]
             L.or_append.restype = I
-            L.or_append.argtypes = [P, I, I, I, I, I, I, I, P, P, I, P, I, P, I, F, F]
+            L.or_append.argtypes = [P, I, I, I, I, I, I, I, P, P, I, P, I, P, I, F, F, P]
             L.or_append_tokens.restype = I
             L.or_append_tokens.argtypes = [P, I, I, I, I, I, I, I, P, P, I, P, I, I, P, P, LL,
-                                           F, F]
+                                           F, F, P]
             L.or_merge.restype = None
             L.or_merge.argtypes = [P, P, P, P, LL, I, I]
             L.or_absmax.restype = D
@@ -99,6 +101,13 @@ def _ptr(a):
 
 def _i32(a):
     return None if a is None else np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _f32(a):
+    if a is None:
+        return None
+    assert a.dtype == np.float32 and a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
 
 
 def num_threads() -> int:
@@ -139,7 +148,7 @@ def absmax(raw, dtype: str) -> float:
 
 def decode(q, q_dtype, pool, kv_dtype, geom, layer, tables, seq_lens, scale,
            k_scale=1.0, v_scale=1.0, tok_begin=None, tok_end=None, rows=None,
-           mutant=0):
+           mutant=0, block_scales=None):
     """fp64 decode attention.  geom = dict(num_blocks, num_layers, num_kv_heads,
     block_size, head_dim, num_q_heads).  Returns (out [B,Hq,D], lse [B,Hq],
     wsum [B,Hq]) as fp64 arrays; rows not requested are NaN."""
@@ -159,14 +168,14 @@ def decode(q, q_dtype, pool, kv_dtype, geom, layer, tables, seq_lens, scale,
                          geom["num_kv_heads"], geom["block_size"], D, Hq, layer,
                          _ptr(tables), max_blocks, _ptr(seq_lens), B, float(scale),
                          float(k_scale), float(v_scale), _ptr(tb), _ptr(te), _ptr(rr),
-                         0 if rr is None else rr.size, int(mutant))
+                         0 if rr is None else rr.size, int(mutant), _f32(block_scales))
     if rc != 0:
         raise ValueError(f"oracle decode rejected its inputs (code {rc})")
     return out, lse, wsum
 
 
 def decode_mq(q, q_dtype, pool, kv_dtype, geom, layer, tables, seq_lens, q_len, scale,
-              k_scale=1.0, v_scale=1.0):
+              k_scale=1.0, v_scale=1.0, block_scales=None):
     """fp64 causal attention of the last q_len tokens of every sequence over its
     paged K/V.  q [B, q_len, Hq, D] -> (out [B, q_len, Hq, D], lse [B, q_len, Hq])."""
     q = np.ascontiguousarray(q)
@@ -181,14 +190,14 @@ def decode_mq(q, q_dtype, pool, kv_dtype, geom, layer, tables, seq_lens, q_len, 
                             geom["num_blocks"], geom["num_layers"], geom["num_kv_heads"],
                             geom["block_size"], D, Hq, layer, _ptr(tables), tables.shape[1],
                             _ptr(seq_lens), B, int(q_len), float(scale), float(k_scale),
-                            float(v_scale))
+                            float(v_scale), _f32(block_scales))
     if rc != 0:
         raise ValueError(f"oracle decode_mq rejected its inputs (code {rc})")
     return out, lse
 
 
 def append(pool, kv_dtype, geom, layer, k, v, in_dtype, tables, positions,
-           k_scale=1.0, v_scale=1.0):
+           k_scale=1.0, v_scale=1.0, block_scales=None):
     """[ENG26 2.2] append_token into `pool` (modified in place)."""
     tables = _i32(tables)
     positions = _i32(positions)
@@ -197,13 +206,14 @@ def append(pool, kv_dtype, geom, layer, k, v, in_dtype, tables, positions,
     rc = lib().or_append(_ptr(pool), DT[kv_dtype], geom["num_blocks"], geom["num_layers"],
                          geom["num_kv_heads"], geom["block_size"], geom["head_dim"], layer,
                          _ptr(k), _ptr(v), DT[in_dtype], _ptr(tables), tables.shape[1],
-                         _ptr(positions), positions.shape[0], float(k_scale), float(v_scale))
+                         _ptr(positions), positions.shape[0], float(k_scale), float(v_scale),
+                         _f32(block_scales))
     if rc != 0:
         raise ValueError(f"oracle append rejected its inputs (code {rc})")
 
 
 def append_tokens(pool, kv_dtype, geom, layer, k, v, in_dtype, tables, seq_ids, positions,
-                  k_scale=1.0, v_scale=1.0):
+                  k_scale=1.0, v_scale=1.0, block_scales=None):
     """Bulk append: token i -> sequence seq_ids[i], position positions[i]."""
     tables = _i32(tables)
     seq_ids = _i32(seq_ids)
@@ -215,9 +225,25 @@ def append_tokens(pool, kv_dtype, geom, layer, k, v, in_dtype, tables, seq_ids, 
                                 geom["head_dim"], layer, _ptr(k), _ptr(v), DT[in_dtype],
                                 _ptr(tables), tables.shape[1], tables.shape[0], _ptr(seq_ids),
                                 _ptr(positions), seq_ids.shape[0], float(k_scale),
-                                float(v_scale))
+                                float(v_scale), _f32(block_scales))
     if rc != 0:
         raise ValueError(f"oracle append_tokens rejected its inputs (code {rc})")
+
+
+def block_scales(scales, geom, layer, k, v, in_dtype, tables, seq_ids, positions):
+    """[UNLOCK 3.2] per-block scales amax / 448 of the tiles these tokens land in,
+    written into `scales` ([NB, 2, L, Hkv] float32, modified in place)."""
+    tables = _i32(tables)
+    seq_ids = _i32(seq_ids)
+    positions = _i32(positions)
+    k = np.ascontiguousarray(k)
+    v = np.ascontiguousarray(v)
+    rc = lib().or_block_scales(_f32(scales), geom["num_blocks"], geom["num_layers"],
+                               geom["num_kv_heads"], geom["block_size"], geom["head_dim"], layer,
+                               _ptr(k), _ptr(v), DT[in_dtype], _ptr(tables), tables.shape[1],
+                               tables.shape[0], _ptr(seq_ids), _ptr(positions), seq_ids.shape[0])
+    if rc != 0:
+        raise ValueError(f"oracle block_scales rejected its inputs (code {rc})")
 
 
 def merge(part_o, part_lse):

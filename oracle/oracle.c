@@ -156,18 +156,28 @@ static size_t or_pool_index(int blk, int kv, int layer, int h, int t, int d,
   return (((((size_t)blk * 2 + kv) * L + layer) * Hkv + h) * bs + t) * (size_t)D + d;
 }
 
+/* Scale of the E4M3 tile (blk, kv, layer, h): from the block-scale array
+ * [NB, 2, L, Hkv] when one is given ([UNLOCK 3.2] block-wise scaling), else the
+ * per-tensor scale. */
+static float or_tile_scale(const float* block_scales, float tensor_scale, int blk, int kv,
+                           int layer, int h, int L, int Hkv) {
+  if (!block_scales) return tensor_scale;
+  return block_scales[(((size_t)blk * 2 + kv) * L + layer) * Hkv + h];
+}
+
 /* Store one token's k or v row [Hkv, D] (dtype in_dtype) into slot (blk, t). */
 static void or_store_token(void* pool, int kv_dtype, int L, int Hkv, int bs, int D,
                            int layer, int kv, int blk, int t, const void* src, size_t src_row,
-                           int in_dtype, float fp8_scale) {
+                           int in_dtype, float fp8_scale, const float* block_scales) {
   int eb = or_elem_bytes(kv_dtype);
   for (int h = 0; h < Hkv; ++h) {
+    float sc = or_tile_scale(block_scales, fp8_scale, blk, kv, layer, h, L, Hkv);
     for (int d = 0; d < D; ++d) {
       size_t di = or_pool_index(blk, kv, layer, h, t, d, L, Hkv, bs, D);
       size_t si = (src_row * Hkv + h) * (size_t)D + d;
       if (kv_dtype == OR_E4M3) {
         float x = (float)or_load(src, si, in_dtype);   /* f32/f16/bf16 -> f32 is exact */
-        ((uint8_t*)pool)[di] = or_e4m3_encode(x, fp8_scale);
+        ((uint8_t*)pool)[di] = or_e4m3_encode(x, sc);
       } else {
         memcpy((char*)pool + di * eb, (const char*)src + si * eb, (size_t)eb);
       }
@@ -185,7 +195,8 @@ static void or_store_token(void* pool, int kv_dtype, int L, int Hkv, int bs, int
  */
 int or_append(void* pool, int kv_dtype, int NB, int L, int Hkv, int bs, int D, int layer,
               const void* k, const void* v, int in_dtype, const int32_t* tables, int max_blocks,
-              const int32_t* positions, int B, float k_scale, float v_scale) {
+              const int32_t* positions, int B, float k_scale, float v_scale,
+              const float* block_scales) {
   if (kv_dtype != OR_E4M3 && in_dtype != kv_dtype) return -1;
   for (int s = 0; s < B; ++s) {
     int pos = positions[s];
@@ -193,8 +204,8 @@ int or_append(void* pool, int kv_dtype, int NB, int L, int Hkv, int bs, int D, i
     if (pos / bs >= max_blocks) return -2;
     int blk = tables[(size_t)s * max_blocks + pos / bs];
     if (blk < 0 || blk >= NB) return -2;
-    or_store_token(pool, kv_dtype, L, Hkv, bs, D, layer, 0, blk, pos % bs, k, (size_t)s, in_dtype, k_scale);
-    or_store_token(pool, kv_dtype, L, Hkv, bs, D, layer, 1, blk, pos % bs, v, (size_t)s, in_dtype, v_scale);
+    or_store_token(pool, kv_dtype, L, Hkv, bs, D, layer, 0, blk, pos % bs, k, (size_t)s, in_dtype, k_scale, block_scales);
+    or_store_token(pool, kv_dtype, L, Hkv, bs, D, layer, 1, blk, pos % bs, v, (size_t)s, in_dtype, v_scale, block_scales);
   }
   return 0;
 }
@@ -208,7 +219,7 @@ int or_append(void* pool, int kv_dtype, int NB, int L, int Hkv, int bs, int D, i
 int or_append_tokens(void* pool, int kv_dtype, int NB, int L, int Hkv, int bs, int D, int layer,
                      const void* k, const void* v, int in_dtype, const int32_t* tables,
                      int max_blocks, int B, const int32_t* seq_ids, const int32_t* positions,
-                     long long n, float k_scale, float v_scale) {
+                     long long n, float k_scale, float v_scale, const float* block_scales) {
   if (kv_dtype != OR_E4M3 && in_dtype != kv_dtype) return -1;
   for (long long i = 0; i < n; ++i) {
     int s = seq_ids[i], pos = positions[i];
@@ -216,9 +227,47 @@ int or_append_tokens(void* pool, int kv_dtype, int NB, int L, int Hkv, int bs, i
     if (s < 0 || s >= B || pos / bs >= max_blocks) return -2;
     int blk = tables[(size_t)s * max_blocks + pos / bs];
     if (blk < 0 || blk >= NB) return -2;
-    or_store_token(pool, kv_dtype, L, Hkv, bs, D, layer, 0, blk, pos % bs, k, (size_t)i, in_dtype, k_scale);
-    or_store_token(pool, kv_dtype, L, Hkv, bs, D, layer, 1, blk, pos % bs, v, (size_t)i, in_dtype, v_scale);
+    or_store_token(pool, kv_dtype, L, Hkv, bs, D, layer, 0, blk, pos % bs, k, (size_t)i, in_dtype, k_scale, block_scales);
+    or_store_token(pool, kv_dtype, L, Hkv, bs, D, layer, 1, blk, pos % bs, v, (size_t)i, in_dtype, v_scale, block_scales);
   }
+  return 0;
+}
+
+/*
+ * [UNLOCK 3.2] block-wise scaling, read as one fp32 scale per pool block (and per
+ * K / V, layer and KV head): for every tile (blk, kv, layer, h) that the n tokens
+ * land in, scale = fp32(amax over those tokens' elements) / 448 in IEEE single
+ * precision (amax 0 -> 1).  Tiles no token lands in are left unchanged.
+ * scales: [NB, 2, L, Hkv] fp32.  Returns 0 or -2 (a token out of range).
+ */
+int or_block_scales(float* scales, int NB, int L, int Hkv, int bs, int D, int layer,
+                    const void* k, const void* v, int in_dtype, const int32_t* tables,
+                    int max_blocks, int B, const int32_t* seq_ids, const int32_t* positions,
+                    long long n) {
+  size_t tiles = (size_t)NB * 2 * L * Hkv;
+  double* amax = (double*)calloc(tiles, sizeof(double));
+  char* touched = (char*)calloc(tiles, 1);
+  if (!amax || !touched) { free(amax); free(touched); return -3; }
+  for (long long i = 0; i < n; ++i) {
+    int s = seq_ids[i], pos = positions[i];
+    if (pos < 0) continue;
+    if (s < 0 || s >= B || pos / bs >= max_blocks) { free(amax); free(touched); return -2; }
+    int blk = tables[(size_t)s * max_blocks + pos / bs];
+    if (blk < 0 || blk >= NB) { free(amax); free(touched); return -2; }
+    for (int kv = 0; kv < 2; ++kv)
+      for (int h = 0; h < Hkv; ++h) {
+        size_t tile = (((size_t)blk * 2 + kv) * L + layer) * Hkv + h;
+        touched[tile] = 1;
+        for (int d = 0; d < D; ++d) {
+          double x = fabs(or_load(kv ? v : k, ((size_t)i * Hkv + h) * D + d, in_dtype));
+          if (x > amax[tile]) amax[tile] = x;      /* NaN is ignored */
+        }
+      }
+  }
+  for (size_t t = 0; t < tiles; ++t)
+    if (touched[t]) scales[t] = amax[t] > 0 ? (float)amax[t] / 448.0f : 1.0f;
+  free(amax);
+  free(touched);
   return 0;
 }
 
@@ -236,11 +285,11 @@ int or_append_tokens(void* pool, int kv_dtype, int NB, int L, int Hkv, int bs, i
 static double or_head(double* o, double* wsum_out, const void* q, int q_dtype, size_t qrow,
                       const void* pool, int kv_dtype, int L, int Hkv, int bs, int D, int Hq,
                       int layer, const int32_t* table_row, int hq, int tb, int te, double scale,
-                      double k_scale, double v_scale, double* sbuf, int mutant) {
+                      double k_scale, double v_scale, const float* block_scales, double* sbuf,
+                      int mutant) {
   int G = Hq / Hkv;
   int h = (mutant == 1) ? (hq % Hkv) : (hq / G);
-  double ks = (kv_dtype == OR_E4M3) ? k_scale : 1.0;
-  double vs = (kv_dtype == OR_E4M3) ? v_scale : 1.0;
+  const int fp8 = kv_dtype == OR_E4M3;
   for (int d = 0; d < D; ++d) o[d] = 0.0;
   if (wsum_out) *wsum_out = 0.0;
   if (te <= tb) return -INFINITY;
@@ -250,6 +299,7 @@ static double or_head(double* o, double* wsum_out, const void* q, int q_dtype, s
     int jj = (mutant == 2) ? (j + 1) % (te > tb ? te : 1) : j;
     int blk = table_row[jj / bs];
     int t = jj % bs;
+    double ks = fp8 ? or_tile_scale(block_scales, (float)k_scale, blk, 0, layer, h, L, Hkv) : 1.0;
     double acc = 0.0;
     for (int d = 0; d < D; ++d) {
       int dk = (mutant == 3) ? (D - 1 - d) : d;
@@ -272,6 +322,7 @@ static double or_head(double* o, double* wsum_out, const void* q, int q_dtype, s
     int blk = table_row[j / bs];
     int t = j % bs;
     int kv = (mutant == 6) ? 0 : 1;
+    double vs = fp8 ? or_tile_scale(block_scales, (float)v_scale, blk, 1, layer, h, L, Hkv) : 1.0;
     for (int d = 0; d < D; ++d)
       o[d] += w * (or_load(pool, or_pool_index(blk, kv, layer, h, t, d, L, Hkv, bs, D), kv_dtype) * vs);
   }
@@ -296,7 +347,8 @@ int or_decode(double* out, double* lse, double* wsum, const void* q, int q_dtype
               const void* pool, int kv_dtype, int NB, int L, int Hkv, int bs, int D, int Hq,
               int layer, const int32_t* tables, int max_blocks, const int32_t* seq_lens, int B,
               double scale, double k_scale, double v_scale, const int32_t* tok_begin,
-              const int32_t* tok_end, const int32_t* rows, int n_rows, int mutant) {
+              const int32_t* tok_end, const int32_t* rows, int n_rows, int mutant,
+              const float* block_scales) {
   if (Hkv <= 0 || Hq % Hkv != 0 || bs <= 0 || D <= 0 || layer < 0 || layer >= L) return -1;
   long long total = rows ? n_rows : (long long)B * Hq;
   int max_len = 0;
@@ -328,7 +380,7 @@ int or_decode(double* out, double* lse, double* wsum, const void* q, int q_dtype
         double ws = 0.0;
         double l = or_head(o, &ws, q, q_dtype, (size_t)s * Hq + hq, pool, kv_dtype, L, Hkv, bs,
                            D, Hq, layer, tables + (size_t)s * max_blocks, hq, tb, te, scale,
-                           k_scale, v_scale, sbuf, mutant);
+                           k_scale, v_scale, block_scales, sbuf, mutant);
         memcpy(out + (size_t)row * D, o, sizeof(double) * (size_t)D);
         if (lse) lse[row] = l;
         if (wsum) wsum[row] = ws;
@@ -353,7 +405,7 @@ int or_decode(double* out, double* lse, double* wsum, const void* q, int q_dtype
 int or_decode_mq(double* out, double* lse, const void* q, int q_dtype, const void* pool,
                  int kv_dtype, int NB, int L, int Hkv, int bs, int D, int Hq, int layer,
                  const int32_t* tables, int max_blocks, const int32_t* seq_lens, int B, int q_len,
-                 double scale, double k_scale, double v_scale) {
+                 double scale, double k_scale, double v_scale, const float* block_scales) {
   if (q_len < 1 || Hkv <= 0 || Hq % Hkv != 0 || layer < 0 || layer >= L) return -1;
   int max_len = 0;
   for (int s = 0; s < B; ++s) {
@@ -385,7 +437,7 @@ int or_decode_mq(double* out, double* lse, const void* q, int q_dtype, const voi
         if (te < 0) te = 0;
         double l = or_head(o, NULL, q, q_dtype, ((size_t)s * q_len + i) * Hq + hq, pool,
                            kv_dtype, L, Hkv, bs, D, Hq, layer, tables + (size_t)s * max_blocks,
-                           hq, 0, te, scale, k_scale, v_scale, sbuf, 0);
+                           hq, 0, te, scale, k_scale, v_scale, block_scales, sbuf, 0);
         memcpy(out + (size_t)r * D, o, sizeof(double) * (size_t)D);
         if (lse) lse[r] = l;
       }

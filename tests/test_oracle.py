@@ -380,3 +380,89 @@ def test_multi_token_decode_with_one_token_is_single_query_decode():
                              case.geometry, 0, case.tables, case.seq_lens, 1, case.scale)
     b, lb, _ = _run_oracle(case, tens, pool)
     assert np.array_equal(a[:, 0], b) and np.array_equal(la[:, 0], lb)
+
+
+# --------------------------------------------------------------------------- block-wise FP8 scales
+def _bs_setup(case, tens):
+    geom = case.geometry
+    nb = case.num_blocks
+    scales = np.zeros((nb, 2, case.num_layers, case.num_kv_heads), np.float32)
+    seq = np.concatenate([np_raw(tens.tok_seq), np.arange(case.batch, dtype=np.int32)])
+    pos = np.concatenate([np_raw(tens.tok_pos), np_raw(tens.new_pos)])
+    k = np.concatenate([np_raw(tens.k_tokens), np_raw(tens.k_new)])
+    v = np.concatenate([np_raw(tens.v_tokens), np_raw(tens.v_new)])
+    oracle.block_scales(scales, geom, case.layer, k, v, "bf16", case.tables, seq, pos)
+    pool = np.zeros(oracle.kv_bytes(case.num_layers, case.num_kv_heads, case.head_dim,
+                                    nb * case.block_size, 1), np.uint8)
+    oracle.append_tokens(pool, "e4m3", geom, case.layer, k, v, "bf16", case.tables, seq, pos,
+                         block_scales=scales)
+    return scales, pool
+
+
+def test_uniform_block_scales_equal_the_per_tensor_path():
+    case = wl.make_case("bs_uni", [100, 33], 8, 2, 32, 16, "e4m3", "bf16", "bf16", seed=130)
+    tens = wl.make_tensors(case)
+    ks = 0.0123
+    uni = np.full((case.num_blocks, 2, 1, 2), ks, np.float32)
+    a = oracle_pool(case, tens, ks, ks, include_new=True)
+    b = np.zeros_like(a)
+    seq = np.concatenate([np_raw(tens.tok_seq), np.arange(2, dtype=np.int32)])
+    pos = np.concatenate([np_raw(tens.tok_pos), np_raw(tens.new_pos)])
+    oracle.append_tokens(b, "e4m3", case.geometry, 0,
+                         np.concatenate([np_raw(tens.k_tokens), np_raw(tens.k_new)]),
+                         np.concatenate([np_raw(tens.v_tokens), np_raw(tens.v_new)]), "bf16",
+                         case.tables, seq, pos, block_scales=uni)
+    assert np.array_equal(a, b)
+    o1, l1, _ = _run_oracle(case, tens, a, ks, ks)
+    o2, l2, _ = oracle.decode(np_raw(tens.q), "bf16", b, "e4m3", case.geometry, 0, case.tables,
+                              case.seq_lens, case.scale, 99.0, 99.0, block_scales=uni)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_block_scales_put_each_tiles_largest_value_at_448():
+    case = wl.make_case("bs_max", [70, 300], 8, 2, 32, 16, "e4m3", "bf16", "bf16", seed=131)
+    tens = wl.make_tensors(case)
+    scales, pool = _bs_setup(case, tens)
+    codes = pool.reshape(case.num_blocks, 2, 1, 2, 16, 32)
+    used = sorted({int(b) for b in case.tables[case.tables >= 0]})
+    for blk in used:
+        for kv in range(2):
+            for h in range(2):
+                assert scales[blk, kv, 0, h] > 0
+                tile = codes[blk, kv, 0, h]
+                assert np.any((tile == 0x7E) | (tile == 0xFE)), (blk, kv, h)
+
+
+def test_block_scaled_decode_equals_naive_on_dequantised_values():
+    case = wl.make_case("bs_naive", [150, 61], 8, 2, 32, 16, "e4m3", "bf16", "bf16", seed=132)
+    tens = wl.make_tensors(case)
+    scales, pool = _bs_setup(case, tens)
+    out, _, _ = oracle.decode(np_raw(tens.q), "bf16", pool, "e4m3", case.geometry, 0,
+                              case.tables, case.seq_lens, case.scale, block_scales=scales)
+    dec = torch.from_numpy(pool).view(torch.float8_e4m3fn).double().numpy().reshape(
+        case.num_blocks, 2, 1, 2, 16, 32) * scales[:, :, :, :, None, None]
+    kv = []
+    for s in range(case.batch):
+        n = int(case.seq_lens[s])
+        blocks = case.tables[s, :(n + 15) // 16]
+        K = dec[blocks, 0, 0].transpose(0, 2, 1, 3).reshape(-1, 2, 32)[:n]
+        V = dec[blocks, 1, 0].transpose(0, 2, 1, 3).reshape(-1, 2, 32)[:n]
+        kv.append((K, V))
+    ref = _naive_case(case, tens, kv)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+
+
+def test_block_scales_are_more_accurate_than_one_scale_on_spiky_keys():
+    case = wl.make_case("bs_spiky", [2000], 8, 2, 32, 16, "e4m3", "bf16", "bf16", seed=133,
+                        spike_frac=0.01)
+    tens = wl.make_tensors(case)
+    exact_case = wl.make_case("bs_spiky", [2000], 8, 2, 32, 16, "bf16", "bf16", "bf16", seed=133,
+                              spike_frac=0.01)
+    exact, _, _ = _run_oracle(exact_case, tens, oracle_pool(exact_case, tens, include_new=True))
+    ks, vs = fp8_scales(tens)
+    per_tensor, _, _ = _run_oracle(case, tens, oracle_pool(case, tens, ks, vs, include_new=True),
+                                   ks, vs)
+    scales, pool = _bs_setup(case, tens)
+    blockwise, _, _ = oracle.decode(np_raw(tens.q), "bf16", pool, "e4m3", case.geometry, 0,
+                                    case.tables, case.seq_lens, case.scale, block_scales=scales)
+    assert np.abs(blockwise - exact).max() < np.abs(per_tensor - exact).max()
