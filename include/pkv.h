@@ -149,6 +149,27 @@ PKV_API int kv_append_tokens(pkv_pool* pool, int layer, const void* d_k, const v
                              const int32_t* d_positions, int64_t num_tokens, float k_scale,
                              float v_scale, cudaStream_t stream);
 
+/* Block-wise FP8 scaling ([UNLOCK] 3.2: one scale per 64-128 tokens), read as one
+ * fp32 scale per pool block, K or V, layer and KV head.  d_scales is a
+ * caller-owned device array [num_blocks, 2, num_layers, num_kv_heads] of fp32
+ * (16-byte aligned).  While it is attached to an E4M3 pool, kv_append,
+ * kv_append_tokens, paged_decode_step and every decode call encode and
+ * dequantise each tile with its own scale (x / scale stored, value x scale
+ * read) and ignore their k_scale / v_scale arguments.  NULL detaches it.
+ * PKV_EINVAL for a pool that is not E4M3. */
+PKV_API int kv_pool_set_block_scales(pkv_pool* pool, float* d_scales);
+/* Set the attached block scales of every tile the given tokens land in (token
+ * i: sequence d_seq_ids[i], or i when d_seq_ids is NULL, at d_positions[i]) to
+ * amax / 448 over those tokens' elements of that tile (IEEE fp32 division;
+ * amax = 0 gives 1); other tiles keep their scales.  Run it on the tokens that
+ * fill a block before storing them (a prefill); a block's scale must not change
+ * while it holds encoded tokens, so later appends into it reuse its scale and
+ * values beyond 448 x scale saturate. */
+PKV_API int kv_block_scales(pkv_pool* pool, int layer, const void* d_k, const void* d_v,
+                            pkv_dtype in_dtype, const int32_t* d_block_tables,
+                            int max_blocks_per_seq, int batch, const int32_t* d_seq_ids,
+                            const int32_t* d_positions, int64_t num_tokens, cudaStream_t stream);
+
 /* Largest |x| over n elements of d_x (f32/f16/bf16; NaN ignored), written to
  * *d_amax (device float) on `stream`.  The per-tensor FP8 scale is amax / 448
  * (amax = 0 -> scale 1). */

@@ -53,7 +53,65 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
         (((((size_t)blk * 2 + kv) * a.L + a.layer) * a.Hkv + h) * a.BS + pos % a.BS) * a.D +
         (size_t)d8 * 8;
     const void* in = kv ? a.v : a.k;
-    store8_to_pool(a.pool, dst, KV, in, src, IN, kv ? a.v_scale : a.k_scale);
+    float sc = kv ? a.v_scale : a.k_scale;
+    if (KV == PKV_FP8_E4M3 && a.block_scales)
+      sc = a.block_scales[(((size_t)blk * 2 + kv) * a.L + a.layer) * a.Hkv + h];
+    store8_to_pool(a.pool, dst, KV, in, src, IN, sc);
+  }
+}
+
+// Tile of token `tok` for (kv, h), or -1 when the token is skipped / out of range.
+__device__ __forceinline__ long long tile_of(const AppendArgs& a, long long tok, int kv, int h) {
+  const int s = a.seq_ids ? __ldg(a.seq_ids + tok) : (int)tok;
+  const int pos = __ldg(a.positions + tok);
+  if (pos < 0 || s < 0 || s >= a.B || pos / a.BS >= a.max_blocks) return -1;
+  const int blk = __ldg(a.tables + (size_t)s * a.max_blocks + pos / a.BS);
+  if (blk < 0 || blk >= a.num_blocks) return -1;
+  return (((long long)blk * 2 + kv) * a.L + a.layer) * a.Hkv + h;
+}
+
+// Block-wise scales, pass 1: mark every tile the tokens land in with -0.0.
+__global__ void __launch_bounds__(256) scales_mark_kernel(const AppendArgs a, float* scales) {
+  const long long total = a.num_tokens * 2 * a.Hkv;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int h = (int)(i % a.Hkv), kv = (int)((i / a.Hkv) % 2);
+    const long long t = tile_of(a, i / (2 * a.Hkv), kv, h);
+    if (t >= 0) scales[t] = -0.0f;
+  }
+}
+
+// Pass 2: fold |x| of every element into its tile as -amax (sign bit set): as
+// unsigned integers, 0x80000000 | bits(|x|) orders like |x|, and the -0.0 marker
+// is the smallest such value.
+template <int IN>
+__global__ void __launch_bounds__(256) scales_amax_kernel(const AppendArgs a, float* scales) {
+  const long long total = a.num_tokens * 2 * a.Hkv * a.D;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int d = (int)(i % a.D);
+    long long r = i / a.D;
+    const int h = (int)(r % a.Hkv);
+    r /= a.Hkv;
+    const int kv = (int)(r % 2);
+    const long long tok = r / 2;
+    const long long t = tile_of(a, tok, kv, h);
+    if (t < 0) continue;
+    const float x = fabsf(load_as_float(kv ? a.v : a.k, ((size_t)tok * a.Hkv + h) * a.D + d, IN));
+    if (isnan(x)) continue;
+    atomicMax(reinterpret_cast<unsigned int*>(scales) + t, 0x80000000u | __float_as_uint(x));
+  }
+}
+
+// Pass 3: every tile holding -amax becomes amax / 448 (IEEE fp32 division; amax 0 -> 1).
+__global__ void __launch_bounds__(256) scales_finish_kernel(float* scales, long long tiles) {
+  for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < tiles;
+       t += (long long)gridDim.x * blockDim.x) {
+    const unsigned int u = __float_as_uint(scales[t]);
+    if (u & 0x80000000u) {
+      const float amax = __uint_as_float(u & 0x7fffffffu);
+      scales[t] = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    }
   }
 }
 
@@ -103,6 +161,28 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   }
   if (e == cudaSuccess) count_launch();
+  return e;
+}
+
+cudaError_t launch_block_scales(const AppendArgs& a, float* scales, cudaStream_t stream) {
+  const long long tiles = (long long)a.num_blocks * 2 * a.L * a.Hkv;
+  if (a.num_tokens > 0) {
+    const long long t1 = a.num_tokens * 2 * a.Hkv, t2 = t1 * a.D;
+    scales_mark_kernel<<<(int)std::min<long long>((t1 + 255) / 256, 1LL << 16), 256, 0, stream>>>(
+        a, scales);
+    const int g2 = (int)std::min<long long>((t2 + 255) / 256, 1LL << 16);
+    switch (a.in_dtype) {
+      case PKV_F32: scales_amax_kernel<PKV_F32><<<g2, 256, 0, stream>>>(a, scales); break;
+      case PKV_F16: scales_amax_kernel<PKV_F16><<<g2, 256, 0, stream>>>(a, scales); break;
+      case PKV_BF16: scales_amax_kernel<PKV_BF16><<<g2, 256, 0, stream>>>(a, scales); break;
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  scales_finish_kernel<<<(int)std::min<long long>((tiles + 255) / 256, 1LL << 16), 256, 0,
+                         stream>>>(scales, tiles);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess)
+    for (int i = 0; i < (a.num_tokens > 0 ? 3 : 1); ++i) count_launch();
   return e;
 }
 

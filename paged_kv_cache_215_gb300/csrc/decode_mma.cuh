@@ -111,6 +111,7 @@ __device__ __forceinline__ long long owner_of(long long b, long long T, long lon
 struct SmemHeader {
   uint64_t full[16];
   uint64_t empty[16];
+  float bscale[16][2][kMaxHG];   // E4M3 block-wise scales of each stage's tiles (K, V)
   long long total, gb0, gb1;
   int s, hg, j;
   volatile int abort_flag;
@@ -194,8 +195,9 @@ struct Consumer {
   }
 
   // The single-token path (one query token, G <= 8 heads as the 8 columns).
+  // ks_b / vs_b: the block's own E4M3 scales (block-wise scaling), else 1.
   __device__ __forceinline__ void block_decode(uint32_t kbase, uint32_t vbase, uint32_t region_bytes,
-                                        int row0, int valid, int lane) {
+                                        int row0, int valid, int lane, float ks_b, float vs_b) {
     const int c = lane & 3;
     const uint32_t sw = lane & 7;   // every ldmatrix row index is congruent to lane mod 8
     float s[kTiles][4];
@@ -237,7 +239,7 @@ struct Consumer {
     }
 
     // ---- online softmax (log2 domain); thread holds tokens lane/4 (+8), heads 2c, 2c+1
-    const float qs = qk_scale_log2_;
+    const float qs = T::kFp8 ? qk_scale_log2_ * ks_b : qk_scale_log2_;
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int mt = 0; mt < kTiles; ++mt) {
@@ -284,8 +286,10 @@ struct Consumer {
     uint32_t bh[kTiles][2], bl[kTiles][2];
 #pragma unroll
     for (int mt = 0; mt < kTiles; ++mt) {
-      const uint32_t x0 = pack2<T::kBf16Mma>(p[mt][0], p[mt][1]);
-      const uint32_t x1 = pack2<T::kBf16Mma>(p[mt][2], p[mt][3]);
+      // E4M3: the block's V scale rides on P (the row sums l keep unscaled p)
+      const float pv = T::kFp8 ? vs_b : 1.f;
+      const uint32_t x0 = pack2<T::kBf16Mma>(p[mt][0] * pv, p[mt][1] * pv);
+      const uint32_t x1 = pack2<T::kBf16Mma>(p[mt][2] * pv, p[mt][3] * pv);
       bh[mt][0] = movmatrix_t(x0);
       bh[mt][1] = movmatrix_t(x1);
       if constexpr (kSplitP) {
@@ -430,9 +434,10 @@ struct Consumer {
   // `jbase` the block's first token position; `valid` its tokens inside the
   // sequence; `full`: no key of the block is hidden from any query row.
   __device__ __forceinline__ void block(uint32_t kbase, uint32_t vbase, uint32_t region_bytes,
-                                        int row0, int jbase, int valid, bool full, int lane) {
+                                        int row0, int jbase, int valid, bool full, int lane,
+                                        float ks_b, float vs_b) {
     if constexpr (NT == 1 && !kCausal) {
-      block_decode(kbase, vbase, region_bytes, row0, valid, lane);
+      block_decode(kbase, vbase, region_bytes, row0, valid, lane, ks_b, vs_b);
       return;
     }
     const int c = lane & 3;
@@ -488,7 +493,7 @@ struct Consumer {
     }
 
     // ---- online softmax (log2 domain); thread holds tokens lane/4 (+8), columns 2c, 2c+1
-    const float qs = qk_scale_log2_;
+    const float qs = T::kFp8 ? qk_scale_log2_ * ks_b : qk_scale_log2_;
     float mx[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) mx[nt][0] = mx[nt][1] = -INFINITY;
@@ -561,8 +566,9 @@ struct Consumer {
     for (int mt = 0; mt < kTiles; ++mt)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const uint32_t x0 = pack2<T::kBf16Mma>(p[mt][nt][0], p[mt][nt][1]);
-        const uint32_t x1 = pack2<T::kBf16Mma>(p[mt][nt][2], p[mt][nt][3]);
+        const float pv = T::kFp8 ? vs_b : 1.f;   // E4M3: the block's V scale rides on P
+        const uint32_t x0 = pack2<T::kBf16Mma>(p[mt][nt][0] * pv, p[mt][nt][1] * pv);
+        const uint32_t x1 = pack2<T::kBf16Mma>(p[mt][nt][2] * pv, p[mt][nt][3] * pv);
         bh[mt][nt][0] = movmatrix_t(x0);
         bh[mt][nt][1] = movmatrix_t(x1);
         if constexpr (kSplitP) {
@@ -856,18 +862,34 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
           const size_t dst =
               (((((size_t)blk * 2 + kv) * a.L + a.layer) * a.Hkv + h) * BS + t) * kD +
               (size_t)d8 * 8;
+          float sc = kv ? a.v_enc_scale : a.k_enc_scale;
+          if (T::kFp8 && a.block_scales)
+            sc = a.block_scales[(((size_t)blk * 2 + kv) * a.L + a.layer) * a.Hkv + h];
           store8_to_pool(const_cast<void*>(a.pool), dst, KVT, kv ? a.v_new : a.k_new, src,
-                         a.new_dtype, kv ? a.v_enc_scale : a.k_enc_scale);
+                         a.new_dtype, sc);
         }
         fence_proxy_async_global();
         __syncwarp();
       }
       if (lane == 0) {
-        bool ok = mbar_wait_bounded(&hdr->empty[stage], (round & 1) ^ 1);
+        const bool ok = mbar_wait_bounded(&hdr->empty[stage], (round & 1) ^ 1);
         if (!ok || hdr->abort_flag) {
           if (!ok) record_error(a.status, PKV_ETIMEOUT);
           hdr->abort_flag = 1;
-        } else {
+        }
+      }
+      if (__shfl_sync(0xffffffffu, (int)hdr->abort_flag, 0)) break;
+      if (T::kFp8 && a.block_scales) {
+        // the stage's per-tile scales, visible to the consumers through the full barrier
+        if (lane < 2 * a.HG) {
+          const int kv = lane / a.HG, hl = lane % a.HG;
+          hdr->bscale[stage][kv][hl] =
+              a.block_scales[(((size_t)blk * 2 + kv) * a.L + a.layer) * a.Hkv + cur.hg * a.HG + hl];
+        }
+        __syncwarp();
+      }
+      if (lane == 0) {
+        {
           mbar_arrive_expect_tx(&hdr->full[stage], stage_bytes);
           uint8_t* st = smem + (size_t)stage * stage_bytes;
           const int hrow = cur.hg * a.HG * BS;   // first row of the head group in a (blk, kv, layer) slab
@@ -881,7 +903,6 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
           }
         }
       }
-      if (__shfl_sync(0xffffffffu, (int)hdr->abort_flag, 0)) break;
       ++issued;
       if (++stage == a.stages) {
         stage = 0;
@@ -948,8 +969,13 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
     const int valid = min(BS, cur.n - cur.j * BS);
     const int jbase = cur.j * BS;
     const bool full = !kCausal || jbase + BS - 1 <= cur.n - a.q_len;
+    float ks_b = 1.f, vs_b = 1.f;
+    if (T::kFp8 && a.block_scales) {
+      ks_b = hdr->bscale[stage][0][w];
+      vs_b = hdr->bscale[stage][1][w];
+    }
     cons.block(sbase, sbase + T::kRegions * region_bytes, region_bytes, w * BS, jbase, valid,
-               full, lane);
+               full, lane, ks_b, vs_b);
     __syncwarp();
     if (lane == 0) mbar_arrive(&hdr->empty[stage]);
     if (++stage == a.stages) {

@@ -76,11 +76,18 @@ __global__ void __launch_bounds__(32 * kWarps) decode_simt_kernel(const DecodeAr
     const size_t kb = ((((size_t)blk * 2 + 0) * a.L + a.layer) * a.Hkv + hkv) * a.BS + t % a.BS;
     const size_t vb = ((((size_t)blk * 2 + 1) * a.L + a.layer) * a.Hkv + hkv) * a.BS + t % a.BS;
     float kr[kMaxDL], vr[kMaxDL];
+    // E4M3 block-wise scales: this token's K / V tile scales (the per-tensor
+    // scales are folded into qs and into the output instead)
+    float kbs = 1.f, vbs = 1.f;
+    if (KVT == PKV_FP8_E4M3 && a.block_scales) {
+      kbs = a.block_scales[(((size_t)blk * 2 + 0) * a.L + a.layer) * a.Hkv + hkv];
+      vbs = a.block_scales[(((size_t)blk * 2 + 1) * a.L + a.layer) * a.Hkv + hkv];
+    }
 #pragma unroll
     for (int k = 0; k < kMaxDL; ++k) {
       if (k < DL) {
-        kr[k] = load_kv<KVT>(a.pool, kb * D + lane + 32 * k);
-        vr[k] = load_kv<KVT>(a.pool, vb * D + lane + 32 * k);
+        kr[k] = load_kv<KVT>(a.pool, kb * D + lane + 32 * k) * kbs;
+        vr[k] = load_kv<KVT>(a.pool, vb * D + lane + 32 * k) * vbs;
       }
     }
 #pragma unroll

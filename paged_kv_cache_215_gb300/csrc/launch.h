@@ -40,6 +40,8 @@ struct DecodeArgs {
   const void* v_new;
   int new_dtype;
   float k_enc_scale, v_enc_scale;
+  // E4M3 per-tile scales [NB, 2, L, Hkv] (block-wise scaling) or nullptr.
+  const float* block_scales;
   // 1: launched with programmatic dependent launch; every write to out, the
   // workspace or the pool waits for the preceding kernel (griddepcontrol.wait).
   int pdl;
@@ -76,8 +78,11 @@ struct AppendArgs {
   int B, Hkv, D, BS, L, layer, max_blocks, num_blocks;
   int in_dtype, kv_dtype;
   float k_scale, v_scale;
+  const float* block_scales;  // E4M3 per-tile scales [NB, 2, L, Hkv], or nullptr (per-tensor)
 };
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
+// Per-tile E4M3 scales amax / 448 of the tiles the tokens land in (three launches).
+cudaError_t launch_block_scales(const AppendArgs& a, float* scales, cudaStream_t stream);
 cudaError_t launch_absmax(const void* x, int dtype, int64_t n, float* amax, cudaStream_t stream);
 
 // Launch counter shared by every launcher.

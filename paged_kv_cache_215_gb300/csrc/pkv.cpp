@@ -187,6 +187,7 @@ struct pkv_pool {
   void* d_pool = nullptr;
   size_t bytes = 0;
   int32_t* d_status = nullptr;
+  float* d_block_scales = nullptr; // E4M3 per-tile scales [NB, 2, L, Hkv] (caller-owned) or null
   std::vector<int32_t> ref;        // reference count per block, 0 = free
   std::vector<int32_t> free_ids;   // stack of free ids
   std::vector<int32_t> free_pos;   // position of an id in free_ids, -1 if taken
@@ -377,7 +378,8 @@ static int append_common(pkv_pool* p, int layer, const void* k, const void* v, p
   const bool fp8 = p->g.kv_dtype == PKV_FP8_E4M3;
   if (fp8) {
     if (!act_dtype(in_dtype)) return PKV_EINVAL;
-    if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+    if (!p->d_block_scales &&
+        (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale)))
       return PKV_EINVAL;
   } else if ((int)in_dtype != p->g.kv_dtype) {
     return PKV_EINVAL;
@@ -404,6 +406,7 @@ static int append_common(pkv_pool* p, int layer, const void* k, const void* v, p
   a.kv_dtype = p->g.kv_dtype;
   a.k_scale = k_scale;
   a.v_scale = v_scale;
+  a.block_scales = fp8 ? p->d_block_scales : nullptr;
   return launch_append(a, stream) == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
@@ -421,6 +424,43 @@ int kv_append_tokens(pkv_pool* p, int layer, const void* d_k, const void* d_v, p
   if (num_tokens > 0 && !d_seq_ids) return PKV_EINVAL;
   return append_common(p, layer, d_k, d_v, in_dtype, d_block_tables, max_blocks_per_seq, batch,
                        d_seq_ids, d_positions, num_tokens, k_scale, v_scale, stream);
+}
+
+int kv_pool_set_block_scales(pkv_pool* p, float* d_scales) {
+  if (!p) return PKV_EINVAL;
+  if (d_scales && (p->g.kv_dtype != PKV_FP8_E4M3 || !aligned16(d_scales))) return PKV_EINVAL;
+  p->d_block_scales = d_scales;
+  return PKV_OK;
+}
+
+int kv_block_scales(pkv_pool* p, int layer, const void* d_k, const void* d_v, pkv_dtype in_dtype,
+                    const int32_t* d_block_tables, int max_blocks_per_seq, int batch,
+                    const int32_t* d_seq_ids, const int32_t* d_positions, int64_t num_tokens,
+                    cudaStream_t stream) {
+  if (!p || !p->d_block_scales || layer < 0 || layer >= p->g.num_layers || num_tokens < 0 ||
+      batch < 0 || !act_dtype(in_dtype))
+    return PKV_EINVAL;
+  if (num_tokens > 0 &&
+      (!d_k || !d_v || !d_block_tables || !d_positions || max_blocks_per_seq < 1 || batch < 1))
+    return PKV_EINVAL;
+  AppendArgs a{};
+  a.k = d_k;
+  a.v = d_v;
+  a.tables = d_block_tables;
+  a.seq_ids = d_seq_ids;
+  a.positions = d_positions;
+  a.num_tokens = num_tokens;
+  a.B = batch;
+  a.Hkv = p->g.num_kv_heads;
+  a.D = p->g.head_dim;
+  a.BS = p->g.block_size;
+  a.L = p->g.num_layers;
+  a.layer = layer;
+  a.max_blocks = max_blocks_per_seq;
+  a.num_blocks = p->g.num_blocks;
+  a.in_dtype = in_dtype;
+  a.kv_dtype = p->g.kv_dtype;
+  return launch_block_scales(a, p->d_block_scales, stream) == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
 int kv_absmax(const void* d_x, pkv_dtype dtype, int64_t n, float* d_amax, cudaStream_t stream) {
@@ -478,9 +518,11 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
   if ((long long)max_seq_len > (long long)max_blocks_per_seq * g.block_size) return PKV_EINVAL;
   if (!std::isfinite(scale)) return PKV_EINVAL;
   const bool fp8 = g.kv_dtype == PKV_FP8_E4M3;
-  if (fp8 && (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) ||
-              !std::isfinite(v_scale)))
+  const float* bscales = fp8 ? p->d_block_scales : nullptr;
+  if (fp8 && !bscales &&
+      (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale)))
     return PKV_EINVAL;
+  if (bscales) k_scale = v_scale = 1.f;   // the per-tile scales take their place
   const bool fused_append = d_k_new != nullptr;
   if (fused_append) {
     if (!d_v_new || !aligned16(d_k_new) || !aligned16(d_v_new)) return PKV_EINVAL;
@@ -570,6 +612,7 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
   a.v_scale = fp8 ? v_scale : 1.f;
   a.k_enc_scale = k_scale;
   a.v_enc_scale = v_scale;
+  a.block_scales = bscales;
   a.new_dtype = new_dtype;
   a.q_len = q_len;
   a.R = G * q_len;
@@ -601,6 +644,7 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
     ap.kv_dtype = g.kv_dtype;
     ap.k_scale = k_scale;
     ap.v_scale = v_scale;
+    ap.block_scales = bscales;
     return launch_append(ap, stream) == cudaSuccess ? PKV_OK : PKV_ECUDA;
   };
 

@@ -70,6 +70,8 @@ def _load() -> ctypes.CDLL:
         "kv_append": (I, [P, I, P, P, I, P, I, P, I, F, F, P]),
         "kv_append_tokens": (I, [P, I, P, P, I, P, I, I, P, P, I64, F, F, P]),
         "kv_absmax": (I, [P, I, I64, P, P]),
+        "kv_pool_set_block_scales": (I, [P, P]),
+        "kv_block_scales": (I, [P, I, P, P, I, P, I, I, P, P, I64, P]),
         "paged_decode_workspace_bytes": (Z, [G, I, I, I]),
         "paged_decode_workspace_bytes_mq": (Z, [G, I, I, I, I]),
         "paged_decode_attention_mq": (I, [P, I, P, I, I, P, I, P, I, P, I, I, F, F, F, I, P, Z,
@@ -97,6 +99,7 @@ EXPORTS = ("kv_pool_bytes", "kv_pool_create", "kv_pool_destroy", "kv_pool_geomet
            "kv_pool_alloc", "kv_pool_reserve", "kv_pool_free", "kv_pool_share",
            "kv_pool_refcount", "kv_pool_num_free", "kv_pool_cow", "kv_append",
            "kv_append_tokens", "kv_absmax", "paged_decode_workspace_bytes",
+           "kv_pool_set_block_scales", "kv_block_scales",
            "paged_decode_attention", "paged_decode_attention_ex", "merge_partials",
            "paged_decode_attention_static", "paged_decode_step",
            "paged_decode_attention_mq", "paged_decode_workspace_bytes_mq",
@@ -234,6 +237,17 @@ class KVPool:
                                      _ptr(tables), tables.shape[1], tables.shape[0],
                                      _ptr(seq_ids), _ptr(positions), seq_ids.shape[0], k_scale,
                                      v_scale, _stream(stream)), "kv_append_tokens")
+
+    def set_block_scales(self, scales: Optional[torch.Tensor]):
+        """Attach a [NB, 2, L, Hkv] float32 device tensor of per-tile E4M3 scales."""
+        self.block_scales = scales
+        _check(_lib.kv_pool_set_block_scales(self.handle, _ptr(scales)), "kv_pool_set_block_scales")
+
+    def compute_block_scales(self, layer, k, v, tables, seq_ids, positions, stream=None):
+        _check(_lib.kv_block_scales(self.handle, layer, _ptr(k), _ptr(v), TORCH_CODE[k.dtype],
+                                    _ptr(tables), tables.shape[1], tables.shape[0],
+                                    _ptr(seq_ids), _ptr(positions), positions.shape[0],
+                                    _stream(stream)), "kv_block_scales")
 
     def check_status(self, stream=None) -> int:
         return int(_lib.pkv_check_status(self.handle, _stream(stream)))
