@@ -46,6 +46,9 @@ MODEL_LAYERS = {"long_128k": 32, "long_1m": 32, "llama8b_b32_8k": 32, "fp8_b8_32
                 "llama70b_prefix_bs16": 80, "llama70b_prefix_bs32": 80, "long_128k_bs64": 32,
                 "llama8b_b32_8k_layers4": 32}
 KERNEL_SOURCES = ["paged_kv_cache_215_gb300/csrc/decode_mma.cu",
+                  "paged_kv_cache_215_gb300/csrc/decode_mma.cuh",
+                  "paged_kv_cache_215_gb300/csrc/decode_mma_bf16.cu",
+                  "paged_kv_cache_215_gb300/csrc/decode_mma_fp8.cu",
                   "paged_kv_cache_215_gb300/csrc/device.cuh"]
 
 
@@ -660,11 +663,17 @@ def main():
     ap.add_argument("--workload", default=PRIMARY, choices=sorted(wl.FULL))
     ap.add_argument("--only-primary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the chunked-prefill (tcgen05) case and print its JSON")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.prefill_only:
+        from paged_kv_cache_215_gb300 import build
+        build.build()
+        print(json.dumps(measure_chunked_prefill("cuda", steps=args.steps)), flush=True)
     else:
         run_ours(args)
 

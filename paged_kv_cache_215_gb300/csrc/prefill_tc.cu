@@ -42,6 +42,11 @@ constexpr uint32_t kSmemV = kSmemK + 2 * 2 * kKVHalf;
 constexpr uint32_t kSmemP = kSmemV + 2 * 2 * kKVHalf;     // 128 rows x 64 keys
 constexpr uint32_t kSmemBytes = kSmemP + kM * 128;
 constexpr uint32_t kTmemCols = 256;          // S0 [0,64) S1 [64,128) O [128,256)
+// Slack for aligning the tiles to 1024 bytes (the 128-byte swizzle atom).  Two
+// CTAs per SM must fit in its 228 KB (each also holds 1 KB for the system):
+// 114,688 B of tiles + the barriers + this slack stays under 115,712 B.  A
+// base that needs more is refused in the kernel (an error, no access).
+constexpr uint32_t kAlignSlack = 896;
 
 struct Bars {
   uint64_t kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, o_done;
@@ -54,11 +59,16 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
 }
 
 template <bool kBf16>
-__global__ void __launch_bounds__(160, 1)
+__global__ void __launch_bounds__(160, 2)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
-  uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const uint32_t shift = ((raw + 1023u) & ~1023u) - raw;
+  if (shift > kAlignSlack) {                    // uniform over the CTA
+    if (threadIdx.x == 0) record_error(a.status, PKV_ECUDA);
+    return;
+  }
+  uint8_t* sm = smem_raw + shift;
   Bars* bars = reinterpret_cast<Bars*>(sm + kSmemBytes);
   const uint32_t base = smem_u32(sm);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -348,7 +358,7 @@ __global__ void __launch_bounds__(160, 1)
 
 }  // namespace
 
-size_t prefill_tc_smem_bytes() { return kSmemBytes + sizeof(Bars) + 1024; }
+size_t prefill_tc_smem_bytes() { return kSmemBytes + sizeof(Bars) + kAlignSlack; }
 
 bool prefill_tc_supported(int kv_dtype, int q_dtype, int BS, int D, int G) {
   return (kv_dtype == PKV_BF16 || kv_dtype == PKV_F16) && q_dtype == kv_dtype && D == kD &&

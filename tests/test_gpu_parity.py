@@ -109,6 +109,33 @@ def test_decode_parity(case, kernel, splits):
     assert_parity(case, out, ref, pool, seqs, gc.v_scale, f"{case.name} k{kernel} s{splits}")
 
 
+# (KV heads per CTA, CTAs per SM) away from the default plan: the widest CTA
+# (8 consumer warps), one head per CTA, and shapes that change the stage count
+# and the balanced partition's run lengths.
+LAUNCH_SHAPES = [(8, 1), (1, 6), (2, 4), (4, 1), (2, 2)]
+
+
+@pytest.mark.parametrize("shape", LAUNCH_SHAPES, ids=lambda s: f"hg{s[0]}c{s[1]}")
+@pytest.mark.parametrize("case", [c for c in CASES if c.kv_dtype != "f32"], ids=lambda c: c.name)
+def test_decode_parity_launch_shapes(case, shape):
+    from paged_kv_cache_215_gb300 import pkv
+    gc, pool, ref, seqs = _sides(case)
+    hg, ctas = shape
+    if case.num_kv_heads % hg:
+        pytest.skip("head group does not divide the KV heads")
+    opts = pkv.launch_opts(kernel=2, kv_heads_per_cta=hg, ctas_per_sm=ctas)
+    try:
+        out = gc.step(opts=opts)
+    except pkv.PkvError as e:
+        if e.code == pkv.PKV_EUNSUPPORTED:
+            pytest.skip("kernel does not take this shape")
+        raise
+    torch.cuda.synchronize()
+    assert gc.status() == 0
+    assert_parity(case, out, ref, pool, seqs, gc.v_scale, f"{case.name} hg{hg} c{ctas}")
+    assert torch.equal(out, gc.step(opts=opts))                 # deterministic
+
+
 @pytest.mark.parametrize("case", [c for c in CASES if c.kv_dtype != "f32"], ids=lambda c: c.name)
 def test_decode_parity_low_precision_out(case):
     gc, pool, ref, seqs = _sides(case)
