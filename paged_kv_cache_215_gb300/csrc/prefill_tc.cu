@@ -248,28 +248,31 @@ __global__ void __launch_bounds__(160, 2)
       }
       tc_fence_after();
       float sv[kN];
-      {
-        float t[32];
-        tmem_ld32(tmem + lane_base + b * kN, t);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 32; ++c) sv[c] = t[c];
-        tmem_ld32(tmem + lane_base + b * kN + 32, t);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 32; ++c) sv[32 + c] = t[c];
-      }
+      tmem_ld64_sync(tmem + lane_base + b * kN, sv);
       tc_fence_before();
       mbar_arrive(&bars->s_free[b]);
-      // scale, causal mask, row max
+      // scale, causal mask, row max (8 partial maxima: short dependency chains)
       const int kpos0 = j * kN;
-      float mx = -INFINITY;
+      float mp[8];
 #pragma unroll
-      for (int c = 0; c < kN; ++c) {
-        const bool vis = live && kpos0 + c <= pos;
-        sv[c] = vis ? sv[c] * qs : -INFINITY;
-        mx = fmaxf(mx, sv[c]);
+      for (int e = 0; e < 8; ++e) mp[e] = -INFINITY;
+      if (__all_sync(0xffffffffu, live && kpos0 + kN - 1 <= pos)) {
+        // the warp's rows see every key of the tile: no mask
+#pragma unroll
+        for (int c = 0; c < kN; ++c) {
+          sv[c] *= qs;
+          mp[c & 7] = fmaxf(mp[c & 7], sv[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kN; ++c) {
+          const bool vis = live && kpos0 + c <= pos;
+          sv[c] = vis ? sv[c] * qs : -INFINITY;
+          mp[c & 7] = fmaxf(mp[c & 7], sv[c]);
+        }
       }
+      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       bool rescale = false;
       float alpha = 1.f;
       if (mx > mref + 8.f) {            // also the first visible key (mref = -inf)
@@ -278,14 +281,17 @@ __global__ void __launch_bounds__(160, 2)
         rescale = j > 0;
       }
       const float ref = mref == -INFINITY ? 0.f : mref;
-      float ps = 0.f;
+      float pp[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) pp[e] = 0.f;
       uint32_t pk[kN / 2];
 #pragma unroll
       for (int c = 0; c < kN; c += 2) {
         const float p0 = exp2f(sv[c] - ref), p1 = exp2f(sv[c + 1] - ref);
-        ps += p0 + p1;
+        pp[(c >> 1) & 7] += p0 + p1;
         pk[c / 2] = pack2<kBf16>(p0, p1);
       }
+      const float ps = ((pp[0] + pp[1]) + (pp[2] + pp[3])) + ((pp[4] + pp[5]) + (pp[6] + pp[7]));
       lsum = lsum * alpha + ps;
       // P_{j-1} must be consumed (and O stable) before P_j and any rescale
       if (j > 0) {
