@@ -28,12 +28,13 @@
 //   (tcgen05.ld/st) only when the true max exceeds it by more than 8 (log2
 //   units); P is then at most 2^8, exact in fp32 accumulation, and O and the
 //   row sum share the same reference.
-// One thread of warp 8 issues the TMA loads and the S MMAs, one thread of warp
-// 9 the P V MMAs: a single thread issues a UMMA about every 70 cycles, well
-// short of what an N = 64 tile takes on the tensor core, and two issuers
-// nearly double the rate.  mbarriers (all waits bounded) pass the tiles
-// between the roles; a stage is refilled once both issuers' MMAs reading it
-// have completed.
+// One thread of warp 8 issues the S MMAs, one thread of warp 9 the P V MMAs:
+// a single thread issues a UMMA about every 70 cycles, well short of what an
+// N = 64 tile takes on the tensor core, and two issuers nearly double the
+// rate.  Warp 10 issues the K/V loads (16 boxes per tile at block size 16,
+// from 16 lanes), off the MMA issuers' path.  mbarriers (all waits bounded)
+// pass the tiles between the roles; a stage is refilled once both issuers'
+// MMAs reading it have completed.
 #include "device.cuh"
 #include "launch.h"
 
@@ -46,9 +47,10 @@ constexpr int kQT = 2;                       // query tiles per CTA
 constexpr int kN = 64;                       // keys per K/V tile
 constexpr int kStages = 4;                   // K/V tiles in flight
 constexpr int kSoftmaxWarps = 4 * kQT;
-constexpr int kWarpS = kSoftmaxWarps;        // TMA loads + S MMAs
+constexpr int kWarpS = kSoftmaxWarps;        // S MMAs
 constexpr int kWarpPV = kSoftmaxWarps + 1;   // P V MMAs
-constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
+constexpr int kWarpTMA = kSoftmaxWarps + 2;  // K/V loads
+constexpr int kThreads = 32 * (kSoftmaxWarps + 3);
 constexpr uint32_t kHalf = 16384;            // 128 rows x 128 B: one 64-column half of Q
 constexpr uint32_t kKVHalf = kN * 128;       // 64 rows x 128 B
 constexpr uint32_t kStageBytes = 4 * kKVHalf;        // K halves 0, 1 then V halves 0, 1
@@ -145,10 +147,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem;
 
-  if (warp == kWarpS || warp == kWarpPV) {
+  if (warp >= kSoftmaxWarps) {
     // ------------------------------------------------------------ issuers
     // Each issuer warp walks its loop and waits as a whole (so it stays
-    // converged); its lane 0 issues the TMA loads, the MMAs and the commits.
+    // converged); its lane 0 issues the MMAs and the commits.
     if (T > 0) {
       const bool leader = lane == 0;
       const int bpt = kN / a.BS;                               // blocks per key tile
@@ -240,8 +242,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         return __all_sync(0xffffffffu, got) && !bars->abort_flag;
       };
       bool ok = true;
-      if (warp == kWarpS) {
+      if (warp == kWarpTMA) {
         for (int j = 0; j < T && j < kStages; ++j) load_tile(j);
+        // key tile k goes into the stage of tile k - kStages once both issuers'
+        // MMAs reading that tile have completed
+        for (int k = kStages; k < T && ok; ++k) {
+          ok = wait(&bars->kv_empty[(k - kStages) % kStages], ((k - kStages) / kStages) & 1);
+          if (!ok) break;
+          load_tile(k);
+        }
+      } else if (warp == kWarpS) {
         for (int j = 0; j < T && ok; ++j) {
           ok = wait(&bars->kv_full[j % kStages], (j / kStages) & 1);
           // S_tj reuses the TMEM buffer of S_t,j-2: its softmax must have read it
@@ -254,14 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j < tiles[t]) issue_s(j, t);
           if (leader) tc_commit(&bars->kv_empty[j % kStages]);  // S_j has read K_j
           __syncwarp();
-          // refill the stage of key tile j - 2 once P V has read it too
-          if (j >= 2 && j - 2 + kStages < T) {
-            ok = wait(&bars->kv_empty[(j - 2) % kStages], ((j - 2) / kStages) & 1);
-            if (!ok) break;
-            load_tile(j - 2 + kStages);
-          }
         }
-      } else {
+      } else if (warp == kWarpPV) {
         for (int j = 0; j < T && ok; ++j) {
           for (int t = 0; t < kQT && ok; ++t) {
             if (j >= tiles[t]) continue;
@@ -282,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every TMA load issued must land before the CTA may exit.  A stage's key
       // tile k is requested only after tile k - kStages landed and was read, so
       // waiting for the phase of the last tile requested into it covers all.
-      if (leader && warp == kWarpS) {
+      if (leader && warp == kWarpTMA) {
         for (int st = 0; st < kStages; ++st)
           if (last_load[st] >= 0)
             mbar_wait_bounded(&bars->kv_full[st], (last_load[st] / kStages) & 1);
