@@ -32,8 +32,9 @@ CASES = [
 ]
 
 
-def _check(case, q_lens, kernel):
+def _check(case, q_lens, kernel, scale=None):
     from paged_kv_cache_215_gb300 import pkv
+    scale = case.scale if scale is None else scale
     tens = wl.make_tensors(case)
     gc = GpuCase(case, tens)
     gc.pool.append(case.layer, gc.k_new, gc.v_new, gc.tables, gc.new_pos)
@@ -43,11 +44,11 @@ def _check(case, q_lens, kernel):
     for q_len in q_lens:
         q = _q(case, q_len, seed=q_len)
         ref, _ = oracle.decode_mq(np_raw(q), case.q_dtype, pool, case.kv_dtype, case.geometry,
-                                  case.layer, case.tables, case.seq_lens, q_len, case.scale)
+                                  case.layer, case.tables, case.seq_lens, q_len, scale)
         out = torch.full((case.batch, q_len, case.num_q_heads, case.head_dim), float("nan"),
                          device="cuda")
         pkv.paged_decode_attention_mq(out, q.cuda(), gc.pool, case.layer, gc.tables,
-                                      gc.seq_lens, gc.max_seq_len, case.scale,
+                                      gc.seq_lens, gc.max_seq_len, scale,
                                       opts=pkv.launch_opts(kernel=kernel) if kernel else None)
         torch.cuda.synchronize()
         assert gc.status() == 0
@@ -69,3 +70,11 @@ def test_chunked_prefill_tcgen05_parity(case, q_lens):
 def test_tcgen05_kernel_forced_on_short_chunks():
     case = wl.make_case("tc_forced", [90, 33, 5], 32, 8, 128, 16, "bf16", "bf16", "bf16", seed=84)
     _check(case, [1, 2, 7], kernel=3)
+
+
+@pytest.mark.parametrize("scale", [-0.125, 0.3])
+def test_tcgen05_softmax_scale_sign_and_size(scale):
+    """A negative scale (carried on Q by the kernel) and a large one (frequent
+    rescales of O) against the oracle at the same scale."""
+    case = wl.make_case("tc_scale", [400, 129], 32, 8, 128, 16, "bf16", "bf16", "bf16", seed=85)
+    _check(case, [64, 100], kernel=0, scale=scale)
