@@ -494,6 +494,57 @@ def measure_chunked_prefill(device, batch=4, context=16384, chunk=2048, steps=20
             "query_tokens_per_s": batch * chunk / (ms * 1e-3)}
 
 
+CASCADE = ["shared_prefix_64k_b32", "llama70b_prefix_bs16"]
+
+
+def measure_cascade(name, device, steps=20):
+    """Decode attention (no append) of a batch whose sequences share a prefix of
+    blocks: the plain path (every sequence reads the prefix) against the
+    shared-prefix path (the prefix read once for all sequences on the tcgen05
+    kernel, the private suffixes through the decode kernel).  Logical GB/s
+    counts every sequence's whole KV, like the plain decode's metric."""
+    from paged_kv_cache_215_gb300 import pkv
+    w = Workload(name, device)
+    c = w.case
+    table, P, lens = wl.prefix_args(c)
+    table = torch.from_numpy(table).to(device)
+    lens = torch.from_numpy(lens).to(device)
+    out = torch.empty_like(w.out)
+    ws = torch.empty(pkv.cascade_workspace_bytes(w.geom, c.batch, c.max_blocks, w.max_len, P),
+                     dtype=torch.uint8, device=device)
+
+    def cascade():
+        pkv.paged_decode_attention_cascade(out, w.tens.q, w.pool, c.layer, table, P, lens,
+                                           w.tables, w.seq_lens, w.max_len, c.scale, workspace=ws)
+
+    def plain():
+        pkv.paged_decode_attention(w.out, w.tens.q, w.pool, c.layer, w.tables, w.seq_lens,
+                                   w.max_len, c.scale, workspace=w.ws)
+    res = {}
+    for nm, f in (("plain", plain), ("cascade", cascade)) * 2:
+        for _ in range(3):
+            f()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(steps):
+            f()
+        e.record()
+        torch.cuda.synchronize()
+        res[nm] = min(res.get(nm, 1e9), s.elapsed_time(e) / steps * 1e3)
+    status = w.pool.check_status()
+    kvb = kv_bytes(c)
+    w.close()
+    del w
+    torch.cuda.empty_cache()
+    return {"batch": c.batch, "shared_prefix_tokens": P, "status": status,
+            "plain_us": res["plain"], "cascade_us": res["cascade"],
+            "speedup": res["plain"] / res["cascade"],
+            "kv_gbs_plain": kvb / (res["plain"] * 1e-6) / 1e9,
+            "kv_gbs_cascade": kvb / (res["cascade"] * 1e-6) / 1e9,
+            "unique_kv_bytes": unique_kv_bytes(c)}
+
+
 def bf16_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -544,6 +595,8 @@ def run_ours(args):
             others[mq_name] = measure_multi_token(base, q_len, max(50, args.steps // 20), device)
         cp = measure_chunked_prefill(device)
         others[cp.pop("workload")] = cp
+        for cname in CASCADE:
+            others[f"{cname}_shared_prefix_decode"] = measure_cascade(cname, device)
     if ws > 1:
         dist.barrier()
     if rank != 0:

@@ -286,6 +286,47 @@ PKV_API int paged_decode_attention_mq(void* d_out, pkv_dtype out_dtype, const vo
 PKV_API size_t paged_decode_workspace_bytes_mq(const pkv_geometry* geom, int batch, int q_len,
                                                int max_seq_len, int num_splits);
 
+/* Decode attention over sequences that share a prefix of blocks ([UNLOCK] 3.1:
+ * a shared prompt prefix is one set of physical blocks referenced by many
+ * tables, copy-on-write).  The result equals paged_decode_attention_ex over each
+ * sequence's own table; the shared blocks are read once per KV head for all
+ * sequences instead of once per sequence:
+ *   1. sequence s's first d_prefix_lens[s] tokens (a multiple of block_size,
+ *      0 .. prefix_len_max) must be blocks d_prefix_table[0 .. d_prefix_lens[s] /
+ *      block_size) -- the same ids as its own table (checked on the device;
+ *      a mismatch, a length that is not a multiple of block_size or exceeds the
+ *      sequence or prefix_len_max is reported by pkv_check_status as PKV_EINVAL);
+ *   2. the prefix keys are attended by all batch x num_q_heads query rows at
+ *      once on the tcgen05 kernel (128-row query tiles, key range split across
+ *      CTAs), each row limited to its own prefix length, giving fp32 partials;
+ *   3. each sequence's remaining tokens go through the decode kernel over a
+ *      suffix table built in the workspace, and one merge combines all partials
+ *      by log-sum-exp ([SEQPAR] incremental softmax).
+ * d_prefix_table: int32 [prefix_blocks], prefix_len_max <= prefix_blocks *
+ * block_size (0: plain decode through the same path).  bf16 / f16 pools, q in
+ * the pool's dtype, head_dim 128, num_q_heads / num_kv_heads dividing 128 and at
+ * most 8 (16 at block size <= 32); otherwise PKV_EUNSUPPORTED.  No E4M3 scales
+ * (the pool must not be E4M3).  The workspace (caller-owned, 16-byte aligned) is
+ * paged_decode_workspace_bytes_cascade; other arguments, ownership and errors as
+ * in paged_decode_attention_ex.
+ * When it pays: the prefix pass replaces one read of the shared blocks per
+ * sequence; a prefix that stays in L2 (a few thousand tokens per layer) was
+ * read once from HBM anyway, and then the extra pass and merge cost a few
+ * percent.  Measured on one GB300: 32 sequences sharing 64K tokens, 6x faster
+ * than paged_decode_attention; 64 sequences sharing 4K tokens, 4% slower. */
+PKV_API int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void* d_q,
+                                           pkv_dtype q_dtype, const pkv_pool* pool, int layer,
+                                           const int32_t* d_prefix_table, int prefix_blocks,
+                                           int prefix_len_max, const int32_t* d_prefix_lens,
+                                           const int32_t* d_block_tables, int max_blocks_per_seq,
+                                           const int32_t* d_seq_lens, int batch, int max_seq_len,
+                                           float scale, void* d_workspace, size_t ws_bytes,
+                                           cudaStream_t stream);
+/* Workspace bytes of paged_decode_attention_cascade (an upper bound over launch plans). */
+PKV_API size_t paged_decode_workspace_bytes_cascade(const pkv_geometry* geom, int batch,
+                                                    int max_blocks_per_seq, int max_seq_len,
+                                                    int prefix_len_max);
+
 /* Log-sum-exp merge of partial results ([SEQPAR] incremental softmax,
  * [ENG26] 3.1): for each row r = (s, h) of batch x num_q_heads,
  *   M = max_p lse[r,p],  w_p = exp(lse[r,p] - M),

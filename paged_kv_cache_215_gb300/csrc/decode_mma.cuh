@@ -995,7 +995,8 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
       bool whole;
       long long slot = 0;
       if (a.mode == 0) {
-        whole = first && unit_end;
+        // (a shared-prefix decode merges every row with its prefix partials)
+        whole = first && unit_end && a.ext_lse == nullptr;
         slot = (long long)blockIdx.x + u;
         if (first && w == 0 && lane == 0) {
           const long long unit_first_gb = cur.gb - cur.j;

@@ -45,6 +45,18 @@ struct DecodeArgs {
   // 1: launched with programmatic dependent launch; every write to out, the
   // workspace or the pool waits for the preceding kernel (griddepcontrol.wait).
   int pdl;
+  // Shared-prefix decode (cascade).  Decode kernel + merge: ext_count partials per
+  // output row computed elsewhere (over the shared prefix), [ext_count][B*Hq][D] and
+  // [ext_count][B*Hq]; every unit then leaves partials and the merge adds these.
+  const float* ext_o;
+  const float* ext_lse;
+  int ext_count;
+  // Prefill kernel over a shared prefix: query token i is sequence i, it sees keys
+  // [0, key_limit[i]) (no causal mask); the key range is cut into S splits
+  // (blockIdx.z), each writing fp32 normalised O to out and its lse to out_lse at
+  // row (split * q_len + i) * Hq + head.
+  const int32_t* key_limit;
+  float* out_lse;
 };
 
 // Shared memory the tensor-core kernel needs for one CTA.
@@ -61,6 +73,18 @@ bool prefill_tc_supported(int kv_dtype, int q_dtype, int BS, int D, int G);
 cudaError_t launch_prefill_tc(const CUtensorMap* map, const DecodeArgs& a, cudaStream_t stream);
 // Merge of the balanced-mode partials, one CTA per (unit, head in the unit).
 cudaError_t launch_merge_units(const DecodeArgs& a, bool pdl, cudaStream_t stream);
+// Cascade merge: the decode's balanced-mode partials of each row plus a.ext_count
+// external partials.
+cudaError_t launch_merge_units_ext(const DecodeArgs& a, cudaStream_t stream);
+// Suffix tables of a shared-prefix decode: suffix_tables[s][j] = tables[s][j + pb_s]
+// with pb_s = prefix_lens[s] / BS, suffix_lens[s] = seq_lens[s] - prefix_lens[s];
+// n_prefix[0] = prefix_len_max.  A prefix that is not the shared table, not a
+// multiple of BS, or longer than the sequence is recorded as PKV_EINVAL.
+cudaError_t launch_suffix_tables(const int32_t* tables, int max_blocks, const int32_t* seq_lens,
+                                 const int32_t* prefix_table, int prefix_blocks,
+                                 const int32_t* prefix_lens, int prefix_len_max, int B, int BS,
+                                 int32_t* suffix_tables, int32_t* suffix_lens, int32_t* n_prefix,
+                                 int32_t* status, cudaStream_t stream);
 // Merge of [rows, S, D] partials (the public merge_partials layout).
 cudaError_t launch_merge_rows(void* out, int out_dtype, const float* part_o, const float* part_lse,
                               int rows, int S, int D, bool pdl, cudaStream_t stream);

@@ -204,3 +204,96 @@ cudaError_t launch_merge_rows(void* out, int out_dtype, const float* part_o, con
 }
 
 }  // namespace pkv
+
+// ---------------------------------------------------------------- shared-prefix decode
+namespace pkv {
+namespace {
+
+// One row per CTA (D threads): the decode's `count` partials of the row (slots
+// first .. first+count-1, stride HG*R rows) and the ext_count partials computed
+// over the shared prefix, combined by log-sum-exp as in merge_row.
+__global__ void __launch_bounds__(256) merge_units_ext_kernel(const DecodeArgs a) {
+  const int u = blockIdx.x, hl = blockIdx.y;
+  const int2 info = a.unit_info[u];
+  const int HGR = a.HG * a.R;
+  const int s = u / a.NHG, hg = u % a.NHG;
+  const int w = hl / a.R, r = hl % a.R;
+  const int i = r / a.G, g = r % a.G;
+  const size_t q_row = ((size_t)s * a.q_len + i) * a.Hq + (size_t)(hg * a.HG + w) * a.G + g;
+  const size_t rows = (size_t)a.B * a.q_len * a.Hq;           // rows of one ext partial set
+  const size_t row0 = (size_t)info.x * HGR + hl;
+  float M = -INFINITY;
+  for (int p = 0; p < info.y; ++p) M = fmaxf(M, a.part_lse[row0 + (size_t)p * HGR]);
+  for (int p = 0; p < a.ext_count; ++p) M = fmaxf(M, a.ext_lse[(size_t)p * rows + q_row]);
+  for (int d = threadIdx.x; d < a.D; d += blockDim.x) {
+    float W = 0.f, v = 0.f;
+    if (M != -INFINITY) {
+      for (int p = 0; p < info.y; ++p) {
+        const size_t pr = row0 + (size_t)p * HGR;
+        const float wt = exp2f((a.part_lse[pr] - M) * kLog2e);
+        W += wt;
+        v = fmaf(wt, a.part_o[pr * a.D + d], v);
+      }
+      for (int p = 0; p < a.ext_count; ++p) {
+        const size_t pr = (size_t)p * rows + q_row;
+        const float wt = exp2f((a.ext_lse[pr] - M) * kLog2e);
+        W += wt;
+        v = fmaf(wt, a.ext_o[pr * a.D + d], v);
+      }
+    }
+    store_from_float(a.out, q_row * a.D + d, a.out_dtype, W > 0.f ? v / W : 0.f);
+  }
+}
+
+// Suffix tables: one thread per (sequence, entry).
+__global__ void suffix_tables_kernel(const int32_t* tables, int max_blocks, const int32_t* seq_lens,
+                                     const int32_t* prefix_table, int prefix_blocks,
+                                     const int32_t* prefix_lens, int prefix_len_max, int B, int BS,
+                                     int32_t* suffix_tables, int32_t* suffix_lens,
+                                     int32_t* n_prefix, int32_t* status) {
+  const int s = blockIdx.y;
+  if (s >= B) return;
+  const int n = seq_lens[s], pl = prefix_lens[s];
+  const bool bad = pl < 0 || pl % BS != 0 || pl > prefix_len_max || pl > n ||
+                   pl / BS > prefix_blocks || n > max_blocks * BS;
+  if (bad && threadIdx.x == 0 && blockIdx.x == 0) record_error(status, PKV_EINVAL);
+  const int pb = bad ? 0 : pl / BS;
+  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < max_blocks; j += gridDim.x * blockDim.x) {
+    if (j < pb && tables[(size_t)s * max_blocks + j] != prefix_table[j])
+      record_error(status, PKV_EINVAL);                     // not the shared prefix
+    suffix_tables[(size_t)s * max_blocks + j] =
+        j + pb < max_blocks ? tables[(size_t)s * max_blocks + j + pb] : -1;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    suffix_lens[s] = bad ? 0 : n - pl;
+    if (s == 0) n_prefix[0] = prefix_len_max;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_merge_units_ext(const DecodeArgs& a, cudaStream_t stream) {
+  const int units = a.B * a.NHG;
+  if (units == 0) return cudaSuccess;
+  merge_units_ext_kernel<<<dim3(units, a.HG * a.R), a.D <= 256 ? 128 : 256, 0, stream>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  return e;
+}
+
+cudaError_t launch_suffix_tables(const int32_t* tables, int max_blocks, const int32_t* seq_lens,
+                                 const int32_t* prefix_table, int prefix_blocks,
+                                 const int32_t* prefix_lens, int prefix_len_max, int B, int BS,
+                                 int32_t* suffix_tables, int32_t* suffix_lens, int32_t* n_prefix,
+                                 int32_t* status, cudaStream_t stream) {
+  if (B == 0) return cudaSuccess;
+  const int gx = (max_blocks + 255) / 256;
+  suffix_tables_kernel<<<dim3(gx > 64 ? 64 : gx, B), 256, 0, stream>>>(
+      tables, max_blocks, seq_lens, prefix_table, prefix_blocks, prefix_lens, prefix_len_max, B, BS,
+      suffix_tables, suffix_lens, n_prefix, status);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  return e;
+}
+
+}  // namespace pkv

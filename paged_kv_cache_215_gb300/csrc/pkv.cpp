@@ -494,16 +494,26 @@ size_t paged_decode_workspace_bytes(const pkv_geometry* g, int batch, int max_se
   return paged_decode_workspace_bytes_mq(g, batch, 1, max_seq_len, num_splits);
 }
 
+// Partials computed over a shared prefix, merged into every output row.
+struct ExtPartials {
+  const float* o;      // [count][B * Hq][D]
+  const float* lse;    // [count][B * Hq]
+  int count;
+};
+
 // Shared body of paged_decode_attention_ex and paged_decode_step.  With k_new
 // set, every sequence's new token is first stored at position seq_lens[s] - 1
 // (fused into the tensor-core kernel, or a separate append launch otherwise).
+// With ext set (shared-prefix decode) the tensor-core kernel in balanced mode
+// is required and the merge adds the external partials.
 static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_dtype q_dtype,
                          int q_len, const void* d_k_new, const void* d_v_new, int new_dtype,
                          const pkv_pool* pool, int layer, const int32_t* d_block_tables,
                          int max_blocks_per_seq, const int32_t* d_seq_lens, int batch,
                          int max_seq_len, float scale, float k_scale, float v_scale,
                          int num_splits, void* d_workspace, size_t ws_bytes,
-                         const pkv_launch_opts* opts, cudaStream_t stream) {
+                         const pkv_launch_opts* opts, cudaStream_t stream,
+                         const ExtPartials* ext = nullptr) {
   pkv_pool* p = const_cast<pkv_pool*>(pool);
   if (!p || batch < 0 || max_seq_len < 0 || num_splits < 0 || layer < 0 ||
       layer >= p->g.num_layers || q_len < 1)
@@ -577,7 +587,10 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
     return launch_prefill_tc(map, t, stream) == cudaSuccess ? PKV_OK : PKV_ECUDA;
   }
   bool use_mma;
-  if (kernel == 2) {
+  if (ext) {
+    if (!mma_ok || num_splits != 0 || q_len != 1 || kernel == 1) return PKV_EUNSUPPORTED;
+    use_mma = true;
+  } else if (kernel == 2) {
     if (!mma_ok) return PKV_EUNSUPPORTED;
     use_mma = true;
   } else if (kernel == 1) {
@@ -669,9 +682,19 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
       a.part_o = reinterpret_cast<float*>(ws + w.o_off);
       a.part_lse = reinterpret_cast<float*>(ws + w.lse_off);
       a.unit_info = reinterpret_cast<int2*>(ws + w.info_off);
+      if (ext) {
+        a.ext_o = ext->o;
+        a.ext_lse = ext->lse;
+        a.ext_count = ext->count;
+        a.pdl = 0;
+      }
       if (phase != 2 && launch_decode_mma(map, a, plan.grid, 1, stream) != cudaSuccess)
         return PKV_ECUDA;
-      if (phase != 1 && launch_merge_units(a, phase == 0, stream) != cudaSuccess) return PKV_ECUDA;
+      if (phase != 1) {
+        const cudaError_t e = ext ? launch_merge_units_ext(a, stream)
+                                  : launch_merge_units(a, phase == 0, stream);
+        if (e != cudaSuccess) return PKV_ECUDA;
+      }
       return PKV_OK;
     }
     size_t lse_off = 0;
@@ -710,6 +733,132 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
                         g.head_dim, phase == 0, stream) != cudaSuccess)
     return PKV_ECUDA;
   return PKV_OK;
+}
+
+// ---------------------------------------------------------------- shared-prefix decode
+// Workspace sections: prefix length (one int), suffix lengths [B], suffix tables
+// [B, max_blocks], prefix partials O [S][B*Hq][D] and lse [S][B*Hq], then the
+// decode's own workspace.
+struct CascadeWs {
+  size_t n_off, lens_off, tab_off, o_off, lse_off, dec_off, bytes;
+  int S;
+};
+static CascadeWs cascade_ws(const pkv_geometry& g, int batch, int max_blocks, int prefix_len_max,
+                            int sms, size_t decode_bytes) {
+  CascadeWs w;
+  const int G = g.num_q_heads / g.num_kv_heads;
+  const int qtiles = (batch * G + 127) / 128;           // 128-row query tiles of the prefix pass
+  const int ctas = ((qtiles + 1) / 2) * g.num_kv_heads;  // CTAs per key split
+  const int ktiles = (prefix_len_max + 63) / 64;
+  int S = ctas > 0 ? (sms + ctas - 1) / ctas : 1;        // about one wave of CTAs
+  S = std::max(1, std::min(S, std::min(std::max(ktiles, 1), 64)));
+  w.S = S;
+  const size_t rows = (size_t)batch * g.num_q_heads;
+  w.n_off = 0;
+  w.lens_off = 256;
+  w.tab_off = w.lens_off + align256((size_t)batch * 4);
+  w.o_off = w.tab_off + align256((size_t)batch * max_blocks * 4);
+  w.lse_off = w.o_off + align256((size_t)S * rows * g.head_dim * 4);
+  w.dec_off = w.lse_off + align256((size_t)S * rows * 4);
+  w.bytes = w.dec_off + decode_bytes;
+  return w;
+}
+
+size_t paged_decode_workspace_bytes_cascade(const pkv_geometry* g, int batch,
+                                            int max_blocks_per_seq, int max_seq_len,
+                                            int prefix_len_max) {
+  if (!geometry_ok(g) || batch < 0 || max_blocks_per_seq < 1 || max_seq_len < 0 ||
+      prefix_len_max < 0)
+    return 0;
+  DeviceInfo dev;
+  if (!device_info(&dev)) return 0;
+  const size_t dec = paged_decode_workspace_bytes(g, batch, max_seq_len, 0);
+  return cascade_ws(*g, batch, max_blocks_per_seq, prefix_len_max, dev.sms, dec).bytes;
+}
+
+int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void* d_q,
+                                   pkv_dtype q_dtype, const pkv_pool* pool, int layer,
+                                   const int32_t* d_prefix_table, int prefix_blocks,
+                                   int prefix_len_max, const int32_t* d_prefix_lens,
+                                   const int32_t* d_block_tables, int max_blocks_per_seq,
+                                   const int32_t* d_seq_lens, int batch, int max_seq_len,
+                                   float scale, void* d_workspace, size_t ws_bytes,
+                                   cudaStream_t stream) {
+  pkv_pool* p = const_cast<pkv_pool*>(pool);
+  if (!p || batch < 0 || layer < 0 || layer >= p->g.num_layers || max_seq_len < 0 ||
+      prefix_len_max < 0 || max_blocks_per_seq < 1)
+    return PKV_EINVAL;
+  if (batch == 0) return PKV_OK;
+  const pkv_geometry& g = p->g;
+  const int G = g.num_q_heads / g.num_kv_heads;
+  if (!d_out || !d_q || !d_block_tables || !d_seq_lens || !d_prefix_lens || !d_workspace ||
+      !aligned16(d_workspace) || !aligned16(d_q) || !aligned16(d_out) || !act_dtype(out_dtype))
+    return PKV_EINVAL;
+  if (prefix_len_max % g.block_size != 0 ||
+      (prefix_len_max > 0 && (!d_prefix_table || prefix_blocks * g.block_size < prefix_len_max)))
+    return PKV_EINVAL;
+  if ((long long)max_seq_len > (long long)max_blocks_per_seq * g.block_size) return PKV_EINVAL;
+  if (!std::isfinite(scale)) return PKV_EINVAL;
+  if (!prefill_tc_supported(g.kv_dtype, q_dtype, g.block_size, g.head_dim, G) ||
+      !mma_supported(g.kv_dtype, g.block_size, g.head_dim, G, 1) || batch > 65535)
+    return PKV_EUNSUPPORTED;
+  DeviceInfo dev;
+  if (!device_info(&dev)) return PKV_ECUDA;
+  const size_t dec = paged_decode_workspace_bytes(&g, batch, max_seq_len, 0);
+  const CascadeWs w = cascade_ws(g, batch, max_blocks_per_seq, prefix_len_max, dev.sms, dec);
+  if (ws_bytes < w.bytes) return PKV_ENOMEM;
+  char* ws = static_cast<char*>(d_workspace);
+  int32_t* n_prefix = reinterpret_cast<int32_t*>(ws + w.n_off);
+  int32_t* suf_lens = reinterpret_cast<int32_t*>(ws + w.lens_off);
+  int32_t* suf_tab = reinterpret_cast<int32_t*>(ws + w.tab_off);
+  float* ext_o = reinterpret_cast<float*>(ws + w.o_off);
+  float* ext_lse = reinterpret_cast<float*>(ws + w.lse_off);
+
+  // 1. suffix tables and lengths (and the check that each prefix is the shared one)
+  if (launch_suffix_tables(d_block_tables, max_blocks_per_seq, d_seq_lens,
+                           prefix_len_max > 0 ? d_prefix_table : d_block_tables,
+                           prefix_len_max > 0 ? prefix_blocks : 0, d_prefix_lens, prefix_len_max,
+                           batch, g.block_size, suf_tab, suf_lens, n_prefix, p->d_status,
+                           stream) != cudaSuccess)
+    return PKV_ECUDA;
+  // 2. the shared prefix once for every sequence: tcgen05 tiles of 128 query rows
+  //    (sequences x heads of a KV head), key range cut into w.S splits
+  if (prefix_len_max > 0) {
+    const CUtensorMap* map = p->tmap(1);
+    if (!map) return PKV_ECUDA;
+    DecodeArgs t{};
+    t.q = d_q;
+    t.out = ext_o;
+    t.out_lse = ext_lse;
+    t.key_limit = d_prefix_lens;
+    t.tables = d_prefix_table;
+    t.seq_lens = n_prefix;
+    t.status = p->d_status;
+    t.B = 1;
+    t.Hq = g.num_q_heads;
+    t.Hkv = g.num_kv_heads;
+    t.G = G;
+    t.D = g.head_dim;
+    t.BS = g.block_size;
+    t.L = g.num_layers;
+    t.layer = layer;
+    t.max_blocks = prefix_blocks;
+    t.num_blocks = g.num_blocks;
+    t.q_dtype = q_dtype;
+    t.out_dtype = PKV_F32;
+    t.kv_dtype = g.kv_dtype;
+    t.q_len = batch;
+    t.R = G * batch;
+    t.S = w.S;
+    t.qk_scale_log2 = (float)((double)scale * 1.4426950408889634);
+    t.v_scale = 1.f;
+    if (launch_prefill_tc(map, t, stream) != cudaSuccess) return PKV_ECUDA;
+  }
+  // 3. the private suffixes, merged with the prefix partials
+  const ExtPartials ext{ext_o, ext_lse, prefix_len_max > 0 ? w.S : 0};
+  return decode_common(d_out, out_dtype, d_q, q_dtype, 1, nullptr, nullptr, 0, pool, layer, suf_tab,
+                       max_blocks_per_seq, suf_lens, batch, max_seq_len, scale, 1.f, 1.f, 0,
+                       ws + w.dec_off, ws_bytes - w.dec_off, nullptr, stream, &ext);
 }
 
 int paged_decode_attention_ex(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_dtype q_dtype,

@@ -95,7 +95,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars* bars = reinterpret_cast<Bars*>(sm + kSmemBytes);
   const uint32_t base = smem_u32(sm);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int hkv = blockIdx.y, s = blockIdx.z;
+  // shared-prefix mode: query token i is sequence i, one key table (the prefix),
+  // blockIdx.z cuts the key range into a.S splits
+  const bool casc = a.key_limit != nullptr;
+  const int hkv = blockIdx.y, s = casc ? 0 : blockIdx.z, split = casc ? blockIdx.z : 0;
   const int G = a.G, QT = kM / G;                 // query tokens per query tile
 
   int n = __ldg(a.seq_lens + s);
@@ -104,14 +107,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) record_error(a.status, PKV_EBOUNDS);
     n = n < 0 ? 0 : cap;
   }
-  int tiles[kQT];
+  // key tiles jt0 .. jt0 + T - 1 of the sequence; local tile j is global tile jt0 + j
+  int tiles[kQT], jt0 = 0;
+  if (casc) {
+    const int nt = (n + kN - 1) / kN;
+    jt0 = (int)((long long)split * nt / a.S);
+    const int jt1 = (int)((long long)(split + 1) * nt / a.S);
 #pragma unroll
-  for (int t = 0; t < kQT; ++t) tiles[t] = key_tiles(a, n, blockIdx.x * kQT + t);
+    for (int t = 0; t < kQT; ++t) tiles[t] = (blockIdx.x * kQT + t) * QT < a.q_len ? jt1 - jt0 : 0;
+  } else {
+#pragma unroll
+    for (int t = 0; t < kQT; ++t) tiles[t] = key_tiles(a, n, blockIdx.x * kQT + t);
+  }
   int T = 0;                                      // key tiles the CTA loads
 #pragma unroll
   for (int t = 0; t < kQT; ++t) T = max(T, tiles[t]);
-  // the sequence's last key tile, if it is ragged and this CTA reads it
-  const int j_tail = (n % kN != 0 && (n - 1) / kN < T) ? (n - 1) / kN : -1;
+  // the sequence's last key tile, if it is ragged and this CTA reads it (local index)
+  const int jg_tail = (n % kN != 0) ? (n - 1) / kN : -1;
+  const int j_tail = (jg_tail >= jt0 && jg_tail < jt0 + T) ? jg_tail - jt0 : -1;
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -197,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto load_tile = [&](int j) {
           const int st = j % kStages;
           last_load[st] = j;
-          const int first = j * bpt;                            // < nblk for every tile loaded
+          const int first = (jt0 + j) * bpt;                    // < nblk for every tile loaded
           if (id_base < 0 || first + bpt > id_base + 32) {
             id_base = first;
             ids = id_base + lane < nblk ? __ldg(trow + id_base + lane) : 0;
@@ -235,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && j_tail >= 0) {
           ok = wait(&bars->kv_full[j_tail % kStages], (j_tail / kStages) & 1);
           if (ok) {
-            const int valid = n - j_tail * kN;
+            const int valid = n - (jt0 + j_tail) * kN;
             uint8_t* vbuf = sm + kSmemKV + (j_tail % kStages) * kStageBytes + 2 * kKVHalf;
             for (int e = lane; e < (kN - valid) * 16; e += 32) {
               const int row = valid + e / 16, c16 = e % 16;
@@ -318,7 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = warp / 4, r = tid - 128 * t, i = r / G, g = r % G;
     const int tok = (blockIdx.x * kQT + t) * QT + i;
     const bool live = tok < a.q_len;
-    const int pos = n - a.q_len + tok;                          // this query's last visible key
+    // this query's last visible key: causal within the chunk, or its prefix length
+    const int pos = casc ? (live ? __ldg(a.key_limit + tok) : 0) - 1 : n - a.q_len + tok;
     const int my_tiles = tiles[t];
     const float qs = fabsf(a.qk_scale_log2);                  // Q carries the sign
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -341,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld64_sync(tcol + b * kN, sv);
       // causal mask and row max (8 partial maxima: short dependency chains),
       // over the raw scores: the scale is positive, so it commutes
-      const int kpos0 = j * kN;
+      const int kpos0 = (jt0 + j) * kN;
       float mp[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) mp[e] = -INFINITY;
@@ -420,7 +434,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // epilogue: O row / l -> out (every lane reads TMEM; live rows store).  The
     // softmax waits for P V only before a rescale, so the last P V may be up to
     // two phases of o_done away: a one-shot barrier marks the end instead.
-    const size_t orow = (((size_t)s * a.q_len + tok) * a.Hq + (size_t)hkv * G + g) * kD;
+    // (shared-prefix mode: fp32 partial O and its natural log-sum-exp per split)
+    const size_t hrow = ((size_t)(casc ? split : s) * a.q_len + tok) * a.Hq + (size_t)hkv * G + g;
+    const size_t orow = hrow * kD;
+    const int odt = casc ? PKV_F32 : a.out_dtype;
     if (ok && my_tiles > 0 && wait(&bars->o_final[t], 0)) {
       tc_fence_after();
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
@@ -431,13 +448,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         if (live) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            store_from_float(a.out, orow + c + e, a.out_dtype, o[e] * inv);
+          for (int e = 0; e < 32; ++e) store_from_float(a.out, orow + c + e, odt, o[e] * inv);
         }
       }
+      if (casc && live)
+        a.out_lse[hrow] = lsum > 0.f ? ((mref == -INFINITY ? 0.f : mref) + __log2f(lsum)) * kLn2
+                                     : -INFINITY;
     } else if (my_tiles == 0) {
-      if (live)
-        for (int e = 0; e < kD; ++e) store_from_float(a.out, orow + e, a.out_dtype, 0.f);
+      if (live) {
+        for (int e = 0; e < kD; ++e) store_from_float(a.out, orow + e, odt, 0.f);
+        if (casc) a.out_lse[hrow] = -INFINITY;
+      }
     } else {
       record_error(a.status, PKV_ETIMEOUT);
       bars->abort_flag = 1;
@@ -464,7 +485,8 @@ cudaError_t launch_prefill_tc(const CUtensorMap* map, const DecodeArgs& a, cudaS
   if (qtiles == 0 || a.B == 0) return cudaSuccess;
   const size_t smem = prefill_tc_smem_bytes();
   cudaError_t e;
-  dim3 grid((qtiles + kQT - 1) / kQT, a.Hkv, a.B);
+  if (a.key_limit && (a.S < 1 || a.S > 65535 || a.B != 1 || !a.out_lse)) return cudaErrorInvalidValue;
+  dim3 grid((qtiles + kQT - 1) / kQT, a.Hkv, a.key_limit ? a.S : a.B);
   if (a.kv_dtype == PKV_BF16) {
     e = cudaFuncSetAttribute(prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);

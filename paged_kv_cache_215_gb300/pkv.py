@@ -83,6 +83,9 @@ def _load() -> ctypes.CDLL:
         "paged_decode_step": (I, [P, I, P, I, P, P, I, P, I, P, I, P, I, I, F, F, F, I, P, Z,
                                   ctypes.POINTER(LaunchOpts), P]),
         "paged_decode_attention_static": (I, [P, I, P, I, P, I, P, I, P, I, I, F, F, F, I, P]),
+        "paged_decode_attention_cascade": (I, [P, I, P, I, P, I, P, I, I, P, P, I, P, I, I, F, P,
+                                               Z, P]),
+        "paged_decode_workspace_bytes_cascade": (Z, [G, I, I, I, I]),
         "pkv_check_status": (I, [P, P]),
         "pkv_strerror": (ctypes.c_char_p, [I]),
         "pkv_launch_count": (ctypes.c_uint64, []),
@@ -103,6 +106,7 @@ EXPORTS = ("kv_pool_bytes", "kv_pool_create", "kv_pool_destroy", "kv_pool_geomet
            "paged_decode_attention", "paged_decode_attention_ex", "merge_partials",
            "paged_decode_attention_static", "paged_decode_step",
            "paged_decode_attention_mq", "paged_decode_workspace_bytes_mq",
+           "paged_decode_attention_cascade", "paged_decode_workspace_bytes_cascade",
            "pkv_check_status", "pkv_strerror", "pkv_launch_count")
 
 
@@ -330,6 +334,31 @@ def paged_decode_attention_mq(out, q, pool: KVPool, layer, tables, seq_lens, max
         num_splits, _ptr(workspace), workspace.numel(),
         None if opts is None else ctypes.byref(opts), _stream(stream)),
         "paged_decode_attention_mq")
+    return out
+
+
+def cascade_workspace_bytes(geom: Geometry, batch: int, max_blocks: int, max_seq_len: int,
+                            prefix_len_max: int) -> int:
+    return int(_lib.paged_decode_workspace_bytes_cascade(ctypes.byref(geom), batch, max_blocks,
+                                                         max_seq_len, prefix_len_max))
+
+
+def paged_decode_attention_cascade(out, q, pool: KVPool, layer, prefix_table, prefix_len_max,
+                                   prefix_lens, tables, seq_lens, max_seq_len, scale,
+                                   workspace=None, stream=None):
+    """Decode attention of sequences sharing a prefix of blocks: the prefix
+    (prefix_table [P] int32, prefix_lens [B] int32 tokens per sequence) is read
+    once for all of them; the result equals paged_decode_attention."""
+    B = q.shape[0]
+    if workspace is None:
+        nb = cascade_workspace_bytes(pool.geom, B, tables.shape[1], max_seq_len, prefix_len_max)
+        workspace = torch.empty(max(nb, 16), dtype=torch.uint8, device=q.device)
+    _check(_lib.paged_decode_attention_cascade(
+        _ptr(out), TORCH_CODE[out.dtype], _ptr(q), TORCH_CODE[q.dtype], pool.handle, layer,
+        _ptr(prefix_table), int(prefix_table.numel()) if prefix_table is not None else 0,
+        prefix_len_max, _ptr(prefix_lens), _ptr(tables), tables.shape[1], _ptr(seq_lens), B,
+        max_seq_len, scale, _ptr(workspace), workspace.numel(), _stream(stream)),
+        "paged_decode_attention_cascade")
     return out
 
 

@@ -185,6 +185,28 @@ def long_context_bs64(tokens=131072, seed=1006) -> Case:
                      "bf16", seed=seed, spike_frac=0.01)
 
 
+def shared_prefix_long(batch=32, prefix=65536, lo=64, hi=2048, seed=1010) -> Case:
+    """Many requests over one long document: `batch` sequences whose first `prefix`
+    tokens are one shared list of blocks, each followed by a private part of
+    uniform [lo, hi] tokens; 32 query / 8 KV heads, head_dim 128, bf16, bs 16."""
+    g = _gen(seed)
+    lens = (prefix + torch.randint(lo, hi + 1, (batch,), generator=g)).numpy().astype(np.int32)
+    return make_case(f"shared_prefix_{prefix // 1024}k_b{batch}", lens, 32, 8, 128, 16, "bf16",
+                     "bf16", "bf16", seed=seed, shared_prefix_tokens=prefix)
+
+
+def prefix_args(case: Case, used: Optional[int] = None):
+    """(prefix table, prefix length, per-sequence prefix lengths) of a shared-prefix
+    decode over the first `used` tokens (default all) of the case's shared blocks:
+    sequence s uses min(n_s, used) rounded down to whole blocks."""
+    bs = case.block_size
+    used = case.shared_prefix_tokens if used is None else min(used, case.shared_prefix_tokens)
+    used = used // bs * bs
+    table = np.ascontiguousarray(case.shared_blocks[:used // bs]).astype(np.int32)
+    lens = np.array([min(int(n), used) // bs * bs for n in case.seq_lens], dtype=np.int32)
+    return table, used, lens
+
+
 FULL = {
     "tiny": tiny_gqa2_d64_f32,
     "llama8b_b32_8k": lambda: llama8b_batch(),
@@ -195,6 +217,7 @@ FULL = {
     "llama70b_prefix_bs32": lambda: llama70b_prefix(block_size=32),
     "long_128k_bs64": lambda: long_context_bs64(),
     "llama8b_b32_8k_layers4": lambda: llama8b_layers(),
+    "shared_prefix_64k_b32": lambda: shared_prefix_long(),
 }
 
 # query tokens per sequence of the multi-token (speculative verification) measurements

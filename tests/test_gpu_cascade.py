@@ -1,0 +1,101 @@
+"""Shared-prefix decode (needs a GPU): paged_decode_attention_cascade reads the
+blocks shared by many sequences once (tcgen05 prefix pass) and their private
+suffixes through the decode kernel, then merges.  It must equal the fp64
+oracle's attention over each sequence's whole table, within the decode bound
+max |err| <= 2e-3 x max|V| per sequence."""
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_215_gb300 import workloads as wl
+from tests.gpu_harness import GpuCase, assert_parity, oracle_side
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from paged_kv_cache_215_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+
+
+def _cases():
+    return [
+        # 64 query / 8 KV heads, lengths 512 .. 20000, first 4096 tokens' full blocks shared
+        (wl.llama70b_prefix(batch=6, lo=512, hi=20000, block_size=16, seed=16), [4096, 1024]),
+        (wl.llama70b_prefix(batch=6, lo=512, hi=20000, block_size=32, seed=17), [4096]),
+        # 32 / 8 heads; sequences wholly inside the prefix (256, 32), one shorter than it
+        (wl.make_case("casc_g4", [256, 100, 4096 + 17, 32, 1000], 32, 8, 128, 16, "bf16", "bf16",
+                      "bf16", seed=90, shared_prefix_tokens=256), [256, 128]),
+        (wl.make_case("casc_f16_bs64", [700, 129, 2000], 32, 8, 128, 64, "f16", "f16", "f16",
+                      seed=91, shared_prefix_tokens=640), [640]),
+    ]
+
+
+CASES = _cases()
+_SIDE = {}
+
+
+def _sides(case):
+    if case.name not in _SIDE:
+        tens = wl.make_tensors(case)
+        gc = GpuCase(case, tens)
+        pool, ref, seqs = oracle_side(case, tens, None, gc.k_scale, gc.v_scale)
+        gc.pool.append(case.layer, gc.k_new, gc.v_new, gc.tables, gc.new_pos)
+        _SIDE[case.name] = (gc, pool, ref, seqs)
+    return _SIDE[case.name]
+
+
+def _prefix(case, used):
+    table, used, lens = wl.prefix_args(case, used)
+    return torch.from_numpy(table).cuda(), used, torch.from_numpy(lens).cuda()
+
+
+@pytest.mark.parametrize("case,prefixes", CASES, ids=lambda c: getattr(c, "name", ""))
+def test_cascade_matches_oracle_and_plain_decode(case, prefixes):
+    from paged_kv_cache_215_gb300 import pkv
+    gc, pool, ref, seqs = _sides(case)
+    plain = gc.step(append=False)
+    for used in prefixes + [0]:
+        table, P, lens = _prefix(case, used)
+        out = torch.full_like(plain, float("nan"))
+        for _ in range(2):                                  # twice: reused workspace state
+            pkv.paged_decode_attention_cascade(out, gc.q, gc.pool, case.layer, table, P, lens,
+                                               gc.tables, gc.seq_lens, gc.max_seq_len,
+                                               case.scale)
+        torch.cuda.synchronize()
+        assert gc.status() == 0
+        assert_parity(case, out, ref, pool, seqs, gc.v_scale, f"{case.name} prefix {P}")
+        assert (out - plain).abs().max().item() <= 2e-3 * float(plain.abs().max())
+
+
+def test_cascade_reports_a_prefix_that_is_not_shared():
+    from paged_kv_cache_215_gb300 import pkv
+    case = CASES[2][0]
+    gc, _, _, _ = _sides(case)
+    table, P, lens = _prefix(case, 256)
+    bad = table.clone()
+    bad[3] = (bad[3] + 1) % case.num_blocks                 # no longer the sequences' block
+    out = torch.empty(case.batch, case.num_q_heads, case.head_dim, device="cuda")
+    pkv.paged_decode_attention_cascade(out, gc.q, gc.pool, case.layer, bad, P, lens, gc.tables,
+                                       gc.seq_lens, gc.max_seq_len, case.scale)
+    assert gc.status() == pkv.PKV_EINVAL
+    odd = lens.clone()
+    odd[1] = 8                                              # not a multiple of the block size
+    pkv.paged_decode_attention_cascade(out, gc.q, gc.pool, case.layer, table, P, odd, gc.tables,
+                                       gc.seq_lens, gc.max_seq_len, case.scale)
+    assert gc.status() == pkv.PKV_EINVAL
+
+
+def test_cascade_rejects_what_it_has_no_kernel_for():
+    from paged_kv_cache_215_gb300 import pkv
+    case = wl.make_case("casc_fp8", [300, 40], 32, 8, 128, 16, "e4m3", "bf16", "bf16", seed=92,
+                        shared_prefix_tokens=32)
+    gc = GpuCase(case)
+    table, P, lens = _prefix(case, 32)
+    out = torch.empty(case.batch, case.num_q_heads, case.head_dim, device="cuda")
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.paged_decode_attention_cascade(out, gc.q, gc.pool, case.layer, table, P, lens,
+                                           gc.tables, gc.seq_lens, gc.max_seq_len, case.scale)
+    assert e.value.code == pkv.PKV_EUNSUPPORTED

@@ -64,3 +64,26 @@ def test_full_size_sampled_parity(name):
     del g, tens, pool
     _gc.collect()
     torch.cuda.empty_cache()
+
+
+def test_full_size_shared_prefix_decode_sampled_parity():
+    """The shared-prefix (cascade) decode on the 64K-token shared-document
+    workload, whole batch on the GPU, sampled sequences against the oracle."""
+    from paged_kv_cache_215_gb300 import pkv
+    case = wl.FULL["shared_prefix_64k_b32"]()
+    tens = wl.make_tensors(case, device="cuda")
+    g = GpuCase(case, tens)
+    g.pool.append(case.layer, g.k_new, g.v_new, g.tables, g.new_pos)
+    table, P, lens = wl.prefix_args(case)
+    out = torch.full((case.batch, case.num_q_heads, case.head_dim), float("nan"), device="cuda")
+    pkv.paged_decode_attention_cascade(out, g.q, g.pool, case.layer, torch.from_numpy(table).cuda(),
+                                       P, torch.from_numpy(lens).cuda(), g.tables, g.seq_lens,
+                                       g.max_seq_len, case.scale)
+    torch.cuda.synchronize()
+    assert g.status() == 0
+    seqs = _extremes(case)
+    pool, ref, seqs = oracle_side(case, tens, seqs, g.k_scale, g.v_scale)
+    assert_parity(case, out, ref, pool, seqs, g.v_scale, case.name)
+    del g, tens, pool
+    _gc.collect()
+    torch.cuda.empty_cache()
