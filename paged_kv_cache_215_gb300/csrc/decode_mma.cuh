@@ -955,6 +955,8 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
     return;
   }
 
+  // a shared-prefix decode merges every row with its prefix partials
+  const bool whole_ok = a.ext_lse == nullptr;
   int stage = 0;
   uint32_t round = 0;
   while (cur.remaining > 0) {
@@ -995,8 +997,7 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
       bool whole;
       long long slot = 0;
       if (a.mode == 0) {
-        // (a shared-prefix decode merges every row with its prefix partials)
-        whole = first && unit_end && a.ext_lse == nullptr;
+        whole = first && unit_end && whole_ok;
         slot = (long long)blockIdx.x + u;
         if (first && w == 0 && lane == 0) {
           const long long unit_first_gb = cur.gb - cur.j;
