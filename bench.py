@@ -414,8 +414,10 @@ def aggregate_ranks(ms_per_step, kv_bytes_per_step, device="cpu"):
 
 def measure_multi_token(base, q_len, steps, device):
     """Multi-token decode (q_len new tokens per sequence, causal within the chunk)
-    on a full-size workload: store the chunk's tokens, then one attention launch
-    (+ merge), timed per step with CUDA events."""
+    on a full-size workload, the new tokens already stored: one attention launch
+    plus the merge per step, chained with programmatic dependent launch and
+    replayed from a CUDA graph (as the decode step); the attention kernel alone
+    is also timed with CUDA events (phase 1, for the roofline)."""
     from paged_kv_cache_215_gb300 import pkv
     w = Workload(base, device)
     c = w.case
@@ -427,26 +429,46 @@ def measure_multi_token(base, q_len, steps, device):
     nb = int(pkv.lib().paged_decode_workspace_bytes_mq(ctypes.byref(w.geom), c.batch, q_len,
                                                        w.max_len, 0))
     ws = torch.empty(nb, dtype=torch.uint8, device=device)
+    pdl, attn = pkv.launch_opts(pdl=1), pkv.launch_opts(phase=1)
 
-    def step():
+    def step(o):
         pkv.paged_decode_attention_mq(out, q, w.pool, c.layer, w.tables, w.seq_lens, w.max_len,
-                                      c.scale, w.ks, w.vs, 0, ws)
+                                      c.scale, w.ks, w.vs, 0, ws, opts=o)
+    stream = torch.cuda.current_stream()
     for _ in range(5):
-        step()
+        step(pdl)
+    torch.cuda.synchronize()
+    chunk = 10
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(chunk):
+            step(pdl)
+    reps = max(1, steps // chunk)
+    graph.replay()
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(steps):
-        step()
-    e.record()
+    s.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    e.record(stream)
     torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / steps
+    ms = s.elapsed_time(e) / (reps * chunk)
+    s.record(stream)
+    for _ in range(steps):
+        step(attn)
+    e.record(stream)
+    torch.cuda.synchronize()
+    attn_us = s.elapsed_time(e) / steps * 1e3
+    del graph
     w.close()
     del w
     torch.cuda.empty_cache()
-    return {"q_len": q_len, "ms_per_step": ms, "kv_gbs": kv_bytes(c) / (ms * 1e-3) / 1e9,
-            "roofline_frac": kv_bytes(c) / (ms * 1e-3) / 1e9 / peaks()[0],
-            "query_tokens_per_s_per_layer": c.batch * q_len / (ms * 1e-3), "batch": c.batch}
+    kvb = kv_bytes(c)
+    return {"q_len": q_len, "ms_per_step": ms, "attn_kernel_us": attn_us,
+            "kv_gbs": kvb / (ms * 1e-3) / 1e9,
+            "roofline_frac": kvb / (attn_us * 1e-6) / 1e9 / peaks()[0],
+            "query_tokens_per_s_per_layer": c.batch * q_len / (ms * 1e-3), "batch": c.batch,
+            "timing": "cuda-graph replay of 10-step chunks; attention kernel alone by CUDA events"}
 
 
 def measure_chunked_prefill(device, batch=4, context=16384, chunk=2048, steps=20):

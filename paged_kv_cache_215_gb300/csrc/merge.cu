@@ -10,10 +10,11 @@
 // sum_p w_p O_p / sum_p w_p.  A partial with lse_p = -inf (an empty key range)
 // has weight 0; a row with no finite partial is 0.
 //
-// One CTA of 512 threads merges one row: the partials' weights are computed
-// once into shared memory, each of the sixteen warps takes every sixteenth
-// partial with four rows in flight, lanes split the head dimension, and the
-// warps' sums meet in shared memory.
+// For few rows with many partials (one long sequence), one CTA of 512 threads
+// merges one row: the partials' weights are computed once into shared memory,
+// each of the sixteen warps takes every sixteenth partial with four rows in
+// flight, lanes split the head dimension, and the warps' sums meet in shared
+// memory.  For many rows with few partials each, one warp merges one row.
 #include "device.cuh"
 #include "launch.h"
 
@@ -155,6 +156,51 @@ __global__ void __launch_bounds__(kThreads) merge_units_kernel(const DecodeArgs 
             q_row * a.D, a.out_dtype);
 }
 
+// Many rows, few partials each (multi-token decode, large batches): one warp per
+// row, 8 rows per CTA; lane l holds columns 4l .. 4l+3 (+128 ...), every lane
+// reads each partial's lse (a broadcast) and computes its weight.
+constexpr int kRowsPerCta = 8;
+__global__ void __launch_bounds__(32 * kRowsPerCta) merge_units_warp_kernel(const DecodeArgs a) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int HGR = a.HG * a.R;
+  const long long row = (long long)blockIdx.x * kRowsPerCta + (threadIdx.x >> 5);
+  if (row >= (long long)a.B * a.NHG * HGR) return;
+  const int lane = threadIdx.x & 31;
+  const int u = (int)(row / HGR), hl = (int)(row % HGR);
+  const int2 info = a.unit_info[u];
+  if (info.y == 1) return;                      // the attention kernel wrote this row
+  const int s = u / a.NHG, hg = u % a.NHG;
+  const int w = hl / a.R, r = hl % a.R;
+  const int i = r / a.G, g = r % a.G;
+  const size_t q_row = ((size_t)s * a.q_len + i) * a.Hq + (size_t)(hg * a.HG + w) * a.G + g;
+  const size_t row0 = (size_t)info.x * HGR + hl;
+  float M = -INFINITY;
+  for (int p = lane; p < info.y; p += 32) M = fmaxf(M, a.part_lse[row0 + (size_t)p * HGR]);
+  M = warp_max(M);
+  for (int d0 = 4 * lane; d0 < a.D; d0 += 128) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float W = 0.f;
+    if (M != -INFINITY) {
+      for (int p = 0; p < info.y; ++p) {
+        const size_t pr = row0 + (size_t)p * HGR;
+        const float wt = exp2f((a.part_lse[pr] - M) * kLog2e);
+        const float4 v = *reinterpret_cast<const float4*>(a.part_o + pr * a.D + d0);
+        W += wt;
+        acc.x = fmaf(wt, v.x, acc.x);
+        acc.y = fmaf(wt, v.y, acc.y);
+        acc.z = fmaf(wt, v.z, acc.z);
+        acc.w = fmaf(wt, v.w, acc.w);
+      }
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    store_from_float(a.out, q_row * a.D + d0 + 0, a.out_dtype, acc.x * inv);
+    store_from_float(a.out, q_row * a.D + d0 + 1, a.out_dtype, acc.y * inv);
+    store_from_float(a.out, q_row * a.D + d0 + 2, a.out_dtype, acc.z * inv);
+    store_from_float(a.out, q_row * a.D + d0 + 3, a.out_dtype, acc.w * inv);
+  }
+}
+
 // [rows, S, D] partials (the layout of the public merge_partials).
 __global__ void __launch_bounds__(kThreads)
     merge_rows_kernel(void* out, int out_dtype, const float* part_o, const float* part_lse, int S,
@@ -190,6 +236,26 @@ cudaError_t launch_merge_units(const DecodeArgs& a, bool pdl, cudaStream_t strea
   if (units == 0) return cudaSuccess;
   DecodeArgs copy = a;
   void* args[] = {&copy};
+  const long long rows = (long long)units * a.HG * a.R;
+  // many rows (each with few partials): a warp per row; few rows (long sequences,
+  // many partials each): a CTA per row
+  if (rows >= 512 && a.D % 4 == 0) {
+    const long long ctas = (rows + kRowsPerCta - 1) / kRowsPerCta;
+    if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(32 * kRowsPerCta);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(merge_units_warp_kernel),
+                                        args);
+    if (e == cudaSuccess) count_launch();
+    return e;
+  }
   return launch_pdl(reinterpret_cast<const void*>(merge_units_kernel),
                     dim3(units, a.HG * a.R), args, pdl, stream);
 }
