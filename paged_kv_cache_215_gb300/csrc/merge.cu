@@ -275,39 +275,80 @@ cudaError_t launch_merge_rows(void* out, int out_dtype, const float* part_o, con
 namespace pkv {
 namespace {
 
-// One row per CTA (D threads): the decode's `count` partials of the row (slots
-// first .. first+count-1, stride HG*R rows) and the ext_count partials computed
-// over the shared prefix, combined by log-sum-exp as in merge_row.
-__global__ void __launch_bounds__(256) merge_units_ext_kernel(const DecodeArgs a) {
-  const int u = blockIdx.x, hl = blockIdx.y;
-  const int2 info = a.unit_info[u];
+// One CTA per row (a thread per column, D <= 256): the decode's `count`
+// partials of the row (slots first .. first+count-1, stride HG*R rows) and the
+// ext_count partials computed over the shared prefix, combined by log-sum-exp
+// as in merge_row.  The weights of up to kExtChunk partials at a time go to
+// shared memory; each thread then sums its column with eight partial rows in
+// flight.
+constexpr int kExtChunk = 512;
+__global__ void __launch_bounds__(128) merge_units_ext_kernel(const DecodeArgs a) {
+  __shared__ float wts[kExtChunk];
+  __shared__ const float* rowp[kExtChunk];
+  __shared__ float red[4];
   const int HGR = a.HG * a.R;
+  const long long row = blockIdx.x;
+  const int u = (int)(row / HGR), hl = (int)(row % HGR);
+  const int2 info = a.unit_info[u];
   const int s = u / a.NHG, hg = u % a.NHG;
   const int w = hl / a.R, r = hl % a.R;
   const int i = r / a.G, g = r % a.G;
   const size_t q_row = ((size_t)s * a.q_len + i) * a.Hq + (size_t)(hg * a.HG + w) * a.G + g;
   const size_t rows = (size_t)a.B * a.q_len * a.Hq;           // rows of one ext partial set
   const size_t row0 = (size_t)info.x * HGR + hl;
+  const int total = info.y + a.ext_count;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // partial p < count: the decode's; else the prefix split p - count
+  auto lse_of = [&](int p) {
+    return p < info.y ? a.part_lse[row0 + (size_t)p * HGR]
+                      : a.ext_lse[(size_t)(p - info.y) * rows + q_row];
+  };
+  auto o_of = [&](int p) {
+    return p < info.y ? a.part_o + (row0 + (size_t)p * HGR) * a.D
+                      : a.ext_o + ((size_t)(p - info.y) * rows + q_row) * a.D;
+  };
   float M = -INFINITY;
-  for (int p = 0; p < info.y; ++p) M = fmaxf(M, a.part_lse[row0 + (size_t)p * HGR]);
-  for (int p = 0; p < a.ext_count; ++p) M = fmaxf(M, a.ext_lse[(size_t)p * rows + q_row]);
-  for (int d = threadIdx.x; d < a.D; d += blockDim.x) {
-    float W = 0.f, v = 0.f;
-    if (M != -INFINITY) {
-      for (int p = 0; p < info.y; ++p) {
-        const size_t pr = row0 + (size_t)p * HGR;
-        const float wt = exp2f((a.part_lse[pr] - M) * kLog2e);
-        W += wt;
-        v = fmaf(wt, a.part_o[pr * a.D + d], v);
-      }
-      for (int p = 0; p < a.ext_count; ++p) {
-        const size_t pr = (size_t)p * rows + q_row;
-        const float wt = exp2f((a.ext_lse[pr] - M) * kLog2e);
-        W += wt;
-        v = fmaf(wt, a.ext_o[pr * a.D + d], v);
-      }
+  for (int p = threadIdx.x; p < total; p += blockDim.x) M = fmaxf(M, lse_of(p));
+  M = warp_max(M);
+  if (lane == 0) red[warp] = M;
+  __syncthreads();
+  M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  float acc[2] = {0.f, 0.f}, W = 0.f;
+  for (int base = 0; base < total && M != -INFINITY; base += kExtChunk) {
+    const int n = min(kExtChunk, total - base);
+    __syncthreads();
+    for (int p = threadIdx.x; p < n; p += blockDim.x) {
+      const float wt = exp2f((lse_of(base + p) - M) * kLog2e);
+      wts[p] = wt;
+      rowp[p] = o_of(base + p);
+      W += wt;
     }
-    store_from_float(a.out, q_row * a.D + d, a.out_dtype, W > 0.f ? v / W : 0.f);
+    __syncthreads();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int d = threadIdx.x + 128 * h;
+      if (d >= a.D) continue;
+      int p = 0;
+      for (; p + 8 <= n; p += 8) {
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = rowp[p + k][d];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[h] = fmaf(wts[p + k], v[k], acc[h]);
+      }
+      for (; p < n; ++p) acc[h] = fmaf(wts[p], rowp[p][d], acc[h]);
+    }
+  }
+  W = warp_sum(W);
+  __syncthreads();
+  if (lane == 0) red[warp] = W;
+  __syncthreads();
+  W = (red[0] + red[1]) + (red[2] + red[3]);
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int d = threadIdx.x + 128 * h;
+    if (d < a.D) store_from_float(a.out, q_row * a.D + d, a.out_dtype, acc[h] * inv);
   }
 }
 
@@ -339,9 +380,10 @@ __global__ void suffix_tables_kernel(const int32_t* tables, int max_blocks, cons
 }  // namespace
 
 cudaError_t launch_merge_units_ext(const DecodeArgs& a, cudaStream_t stream) {
-  const int units = a.B * a.NHG;
-  if (units == 0) return cudaSuccess;
-  merge_units_ext_kernel<<<dim3(units, a.HG * a.R), a.D <= 256 ? 128 : 256, 0, stream>>>(a);
+  const long long rows = (long long)a.B * a.NHG * a.HG * a.R;
+  if (rows == 0) return cudaSuccess;
+  if (rows > 0x7fffffffLL || a.D > 256) return cudaErrorInvalidValue;
+  merge_units_ext_kernel<<<(unsigned)rows, 128, 0, stream>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
   return e;
