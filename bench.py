@@ -276,34 +276,61 @@ def time_steps(w, steps, warmup, split_phases=False, graph_chunk=0):
 
 
 def time_e2e(w, steps, warmup):
-    """Through the C ABI from pinned host buffers: per step copy q, the new k and v
-    and the lengths host->device, run the decode step, copy out device->host."""
+    """Through the C ABI from pinned host memory: per step one host->device copy of
+    the step's inputs (q, the new k and v, the lengths, packed in one pinned
+    staging buffer the way a serving loop would stage them), the decode step
+    (its launches chained with programmatic dependent launch), and the output
+    copied device->host; ten such steps replayed as one CUDA graph.  Byte counts
+    are the staging buffer and the output."""
+    from paged_kv_cache_215_gb300 import pkv
     c = w.case
     t = w.tens
-    host = {k: getattr(t, k).cpu().pin_memory() for k in ("q", "k_new", "v_new")}
-    host["seq_lens"] = torch.from_numpy(c.seq_lens).pin_memory()
-    dev = {k: torch.empty_like(v, device="cuda") for k, v in host.items()}
+    parts = {k: getattr(t, k).contiguous() for k in ("q", "k_new", "v_new")}
+    parts["seq_lens"] = torch.from_numpy(c.seq_lens).to(w.seq_lens.device)
+    offs, total = {}, 0
+    for k, v in parts.items():
+        offs[k] = total
+        total += (v.numel() * v.element_size() + 255) // 256 * 256
+    host = torch.empty(total, dtype=torch.uint8).pin_memory()
+    for k, v in parts.items():
+        nb = v.numel() * v.element_size()
+        host[offs[k]:offs[k] + nb].copy_(v.cpu().contiguous().view(torch.uint8).reshape(-1))
+    dev = torch.empty(total, dtype=torch.uint8, device="cuda")
+    view = {k: dev[offs[k]:offs[k] + v.numel() * v.element_size()].view(v.dtype).view(v.shape)
+            for k, v in parts.items()}
     out_h = torch.empty(w.out.shape, dtype=w.out.dtype).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    h2d = total
     d2h = out_h.numel() * out_h.element_size()
     stream = torch.cuda.current_stream()
+    pdl = pkv.launch_opts(pdl=1)
 
     def step():
-        for k in host:
-            dev[k].copy_(host[k], non_blocking=True)
-        w.step(None, q=dev["q"], k=dev["k_new"], v=dev["v_new"], seq_lens=dev["seq_lens"])
+        dev.copy_(host, non_blocking=True)
+        w.step(pdl, q=view["q"], k=view["k_new"], v=view["v_new"], seq_lens=view["seq_lens"])
         out_h.copy_(w.out, non_blocking=True)
 
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
+    # the copies and launches of 10 steps replayed as one CUDA graph, as the
+    # device-timed loop does
+    chunk = 10
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(chunk):
+            step()
+    reps = max(1, steps // chunk)
+    graph.replay()
+    torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record(stream)
-    for _ in range(steps):
-        step()
+    for _ in range(reps):
+        graph.replay()
     e.record(stream)
     torch.cuda.synchronize()
-    return s.elapsed_time(e) / steps, h2d, d2h
+    ms = s.elapsed_time(e) / (reps * chunk)
+    del graph
+    return ms, h2d, d2h
 
 
 def cpu_baseline(w, budget_s=15.0):
