@@ -393,6 +393,7 @@ def measure(name, steps, warmup, device, with_clocks=False, gpu_index=0, e2e=Tru
         "kv_bytes": kv_bytes(c),
         "kv_gbs": kv_bytes(c) / (ms * 1e-3) / 1e9,
         "attn_kernel_us": attn_ms * 1e3,
+        "attn_kernel_median_us": float(np.median(attn)) * 1e3,
         "attn_kernel_p10_p90_us": [float(np.percentile(attn, 10)) * 1e3,
                                    float(np.percentile(attn, 90)) * 1e3],
         "algorithmic_bytes": alg,
@@ -665,6 +666,8 @@ def run_ours(args):
         "decode_tokens_per_s_per_layer": res["tokens_per_s_per_layer"],
         "roofline": res["roofline"],
         "attn_kernel_us": res["attn_kernel_us"],
+        "attn_kernel_median_us": res["attn_kernel_median_us"],
+        "attn_kernel_p10_p90_us": res["attn_kernel_p10_p90_us"],
         "ms_per_step_eager": res["ms_per_step_eager"],
         "ms_per_step_graph": res["ms_per_step_graph"],
         "timing": res["timing"],
