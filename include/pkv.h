@@ -53,7 +53,7 @@ typedef enum {
   PKV_ECUDA = -3,        /* a CUDA runtime call failed */
   PKV_EBOUNDS = -4,      /* (device) a block id or position outside the pool or table */
   PKV_ETIMEOUT = -5,     /* (device) a bounded wait inside a kernel ran out */
-  PKV_EUNSUPPORTED = -6  /* a valid combination this build has no kernel for */
+  PKV_EUNSUPPORTED = -6  /* a valid combination the library has no kernel for */
 } pkv_status;
 
 typedef enum { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2, PKV_FP8_E4M3 = 3 } pkv_dtype;
