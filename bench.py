@@ -499,30 +499,38 @@ def measure_multi_token(base, q_len, steps, device):
             "timing": "cuda-graph replay of 10-step chunks; attention kernel alone by CUDA events"}
 
 
-def measure_chunked_prefill(device, batch=4, context=16384, chunk=2048, steps=20):
+def measure_chunked_prefill(device, batch=4, context=16384, chunk=2048, steps=20, kv="bf16"):
     """Chunked prefill on the tcgen05 kernel: `batch` sequences of `context` tokens
-    (32 query / 8 KV heads, D 128, bf16, bs 16) whose last `chunk` tokens are the
-    new queries, causal within the chunk.  Work = 4 * D flops per (query head, visible key)."""
+    (32 query / 8 KV heads, D 128, bs 16, a bf16, f16 or E4M3 pool; f16 queries for
+    an f16 pool, else bf16) whose
+    last `chunk` tokens are the new queries, causal within the chunk.
+    Work = 4 * D flops per (query head, visible key)."""
     from paged_kv_cache_215_gb300 import pkv
-    case = wl.make_case(f"chunked_prefill_b{batch}_ctx{context}_chunk{chunk}", [context] * batch,
-                        32, 8, 128, 16, "bf16", "bf16", "bf16", seed=1007)
+    tag = "" if kv == "bf16" else f"_{kv}"
+    qd = "f16" if kv == "f16" else "bf16"
+    case = wl.make_case(f"chunked_prefill{tag}_b{batch}_ctx{context}_chunk{chunk}",
+                        [context] * batch, 32, 8, 128, 16, kv, qd, qd, seed=1007)
     t = wl.make_tensors(case, device=device)
-    geom = pkv.geometry(1, 32, 8, 128, 16, case.num_blocks, "bf16")
+    geom = pkv.geometry(1, 32, 8, 128, 16, case.num_blocks, kv)
     pool = pkv.KVPool(geom, device=device)
     pool.storage.zero_()
     ids = case.tables[case.tables >= 0]
     pool.reserve(np.unique(ids).tolist())
     tables = torch.from_numpy(case.tables).to(device)
     lens = torch.from_numpy(case.seq_lens).to(device)
-    pool.append_tokens(0, t.k_tokens, t.v_tokens, tables, t.tok_seq, t.tok_pos)
-    pool.append(0, t.k_new, t.v_new, tables, t.new_pos)
+    ks = vs = 1.0
+    if kv == "e4m3":
+        ks = pkv.fp8_scale(float(torch.maximum(t.k_tokens.abs().max(), t.k_new.abs().max())))
+        vs = pkv.fp8_scale(float(torch.maximum(t.v_tokens.abs().max(), t.v_new.abs().max())))
+    pool.append_tokens(0, t.k_tokens, t.v_tokens, tables, t.tok_seq, t.tok_pos, ks, vs)
+    pool.append(0, t.k_new, t.v_new, tables, t.new_pos, ks, vs)
     g = torch.Generator(device=device).manual_seed(78)
-    q = torch.randn(batch, chunk, 32, 128, generator=g, device=device).to(torch.bfloat16)
-    out = torch.empty(batch, chunk, 32, 128, dtype=torch.bfloat16, device=device)
+    q = torch.randn(batch, chunk, 32, 128, generator=g, device=device).to(wl.TORCH_DT[qd])
+    out = torch.empty(batch, chunk, 32, 128, dtype=wl.TORCH_DT[qd], device=device)
     ws = torch.empty(16, dtype=torch.uint8, device=device)
 
     def step():
-        pkv.paged_decode_attention_mq(out, q, pool, 0, tables, lens, context, case.scale,
+        pkv.paged_decode_attention_mq(out, q, pool, 0, tables, lens, context, case.scale, ks, vs,
                                       workspace=ws)
     for _ in range(3):
         step()
@@ -536,6 +544,7 @@ def measure_chunked_prefill(device, batch=4, context=16384, chunk=2048, steps=20
     ms = s.elapsed_time(e) / steps
     keys = sum(context - chunk + i + 1 for i in range(chunk))      # visible keys per query row
     flops = 4.0 * 128 * 32 * keys * batch
+    assert pool.check_status() == 0
     pool.close()
     peak = bf16_peak()
     return {"workload": case.name, "ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
@@ -643,8 +652,9 @@ def run_ours(args):
     if rank == 0 and not args.only_primary:
         for mq_name, (base, q_len) in wl.MULTI_TOKEN.items():
             others[mq_name] = measure_multi_token(base, q_len, max(50, args.steps // 20), device)
-        cp = measure_chunked_prefill(device)
-        others[cp.pop("workload")] = cp
+        for kv in ("bf16", "e4m3"):
+            cp = measure_chunked_prefill(device, kv=kv)
+            others[cp.pop("workload")] = cp
         for cname in CASCADE:
             others[f"{cname}_shared_prefix_decode"] = measure_cascade(cname, device)
     if ws > 1:
@@ -778,7 +788,8 @@ def main():
     elif args.prefill_only:
         from paged_kv_cache_215_gb300 import build
         build.build()
-        print(json.dumps(measure_chunked_prefill("cuda", steps=args.steps)), flush=True)
+        for kv in ("bf16", "e4m3"):
+            print(json.dumps(measure_chunked_prefill("cuda", steps=args.steps, kv=kv)), flush=True)
     else:
         run_ours(args)
 

@@ -269,10 +269,13 @@ PKV_API int paged_decode_step(void* d_out, pkv_dtype out_dtype, const void* d_q,
  * paged_decode_attention.  A query whose position is negative gets out = 0.
  * d_q and d_out: [batch, q_len, num_q_heads, head_dim].  The tensor-core kernel
  * (mma.sync) takes q_len * (num_q_heads / num_kv_heads) <= 16 rows per KV head
- * (<= 8 at block_size 64); larger chunks on bf16 / f16 pools (q in the pool's
- * dtype) run on the tcgen05 kernel: UMMA tiles of 128 query rows x 64 keys with
- * S and O in tensor memory (num_splits must be 0 there).  Other combinations
- * return PKV_EUNSUPPORTED.  Other arguments and errors as in
+ * (<= 8 at block_size 64); larger chunks run on the tcgen05 kernel: UMMA tiles
+ * of 128 query rows x 64 keys with S and O in tensor memory (num_splits must be
+ * 0 there), head_dim 128, num_q_heads / num_kv_heads dividing 128.  bf16 / f16
+ * pools take q in the pool's dtype; E4M3 pools take bf16 or f16 q, and each
+ * E4M3 tile is converted to f16 in shared memory (exactly with per-tensor
+ * scales; times its block's scales, rounded to f16, with per-block ones), q
+ * rounded to f16.  Other combinations return PKV_EUNSUPPORTED.  Other arguments and errors as in
  * paged_decode_attention_ex; the workspace is paged_decode_workspace_bytes_mq. */
 PKV_API int paged_decode_attention_mq(void* d_out, pkv_dtype out_dtype, const void* d_q,
                                       pkv_dtype q_dtype, int q_len, const pkv_pool* pool,

@@ -68,7 +68,6 @@ cudaError_t launch_decode_mma(const CUtensorMap* map, const DecodeArgs& a, int g
                               cudaStream_t stream);
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t stream);
 // Chunked prefill on tcgen05 (one CTA per 128-row query tile, KV head, sequence).
-size_t prefill_tc_smem_bytes();
 bool prefill_tc_supported(int kv_dtype, int q_dtype, int BS, int D, int G);
 cudaError_t launch_prefill_tc(const CUtensorMap* map, const DecodeArgs& a, cudaStream_t stream);
 // Merge of the balanced-mode partials, one CTA per (unit, head in the unit).

@@ -582,8 +582,12 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
     t.kv_dtype = g.kv_dtype;
     t.q_len = q_len;
     t.R = G * q_len;
-    t.qk_scale_log2 = (float)((double)scale * 1.4426950408889634);
-    t.v_scale = 1.f;
+    // E4M3 pools: per-tensor scales as for the decode kernel (k_scale on the
+    // softmax scale, v_scale on the output); per-block ones when each tile is
+    // converted to f16
+    t.qk_scale_log2 = (float)((double)scale * 1.4426950408889634 * (fp8 ? (double)k_scale : 1.0));
+    t.v_scale = fp8 ? v_scale : 1.f;
+    t.block_scales = bscales;
     return launch_prefill_tc(map, t, stream) == cudaSuccess ? PKV_OK : PKV_ECUDA;
   }
   bool use_mma;
@@ -799,7 +803,8 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
     return PKV_EINVAL;
   if ((long long)max_seq_len > (long long)max_blocks_per_seq * g.block_size) return PKV_EINVAL;
   if (!std::isfinite(scale)) return PKV_EINVAL;
-  if (!prefill_tc_supported(g.kv_dtype, q_dtype, g.block_size, g.head_dim, G) ||
+  if (g.kv_dtype == PKV_FP8_E4M3 ||   // (no dequantisation scales in this entry's arguments)
+      !prefill_tc_supported(g.kv_dtype, q_dtype, g.block_size, g.head_dim, G) ||
       !mma_supported(g.kv_dtype, g.block_size, g.head_dim, G, 1) || batch > 65535)
     return PKV_EUNSUPPORTED;
   DeviceInfo dev;

@@ -47,24 +47,42 @@ constexpr int kD = 128;
 constexpr int kM = 128;                      // query rows per query tile (one UMMA M)
 constexpr int kQT = 2;                       // query tiles per CTA
 constexpr int kN = 64;                       // keys per K/V tile
-constexpr int kStages = 5;                   // K/V tiles in flight
 constexpr int kSoftmaxWarps = 4 * kQT;
 constexpr int kWarpS = kSoftmaxWarps;        // S MMAs of query tile t: warp kWarpS + t
 constexpr int kWarpPV = kWarpS + kQT;        // P V MMAs of query tile t: warp kWarpPV + t
 constexpr int kWarpTMA = kWarpPV + kQT;      // K/V loads
-constexpr int kThreads = 32 * (kWarpTMA + 1);
+constexpr int kWarpConv = kWarpTMA + 1;      // E4M3 pools: warps converting K/V tiles to f16
 constexpr int kIssuers = 2 * kQT;            // MMA issuers committing each stage's release
 constexpr uint32_t kHalf = 16384;            // 128 rows x 128 B: one 64-column half of Q
 constexpr uint32_t kKVHalf = kN * 128;       // 64 rows x 128 B
 constexpr uint32_t kStageBytes = 4 * kKVHalf;        // K halves 0, 1 then V halves 0, 1
+constexpr uint32_t kStage8Bytes = 2 * kKVHalf;       // an E4M3 tile: K then V, 128 B a key
 constexpr uint32_t kSmemQ = 0;                        // [query tile][half]
 constexpr uint32_t kSmemKV = kSmemQ + kQT * 2 * kHalf;
-constexpr uint32_t kSmemBytes = kSmemKV + kStages * kStageBytes;
 constexpr uint32_t kTmemCols = 512;          // query tile t: S/P0 [256t, +64) S/P1 [+64, +128) O [+128, +256)
 constexpr uint32_t kAlignSlack = 1024;       // the tiles start on a 1024-byte boundary
+constexpr int kMaxStages = 5;
+
+// Per pool dtype.  bf16 / f16: TMA fills kStages tiles the MMAs read directly.
+// E4M3: TMA lands the E4M3 tile (one 128-byte line per key: half the boxes) in
+// the V half of its stage, and kConvWarps warps convert it in place into the
+// stage's f16 K and V; the MMAs then run as for an f16 pool.  Every E4M3 value is
+// an f16 value, so with per-tensor scales the conversion is exact (k_scale rides
+// on the softmax scale, v_scale on the output); per-block scales are multiplied
+// in before the f16 rounding (relative error 2^-11).
+template <int KVT>
+struct PfCfg {
+  static constexpr bool kFp8 = KVT == PKV_FP8_E4M3;
+  static constexpr bool kBf16 = KVT == PKV_BF16;      // else f16 operands (f16 and E4M3 pools)
+  static constexpr int kStages = 5;                   // K/V tiles in flight
+  static constexpr int kConvWarps = kFp8 ? 3 : 0;
+  static constexpr int kThreads = 32 * (kWarpConv + kConvWarps);
+  static constexpr uint32_t kSmemBytes = kSmemKV + kStages * kStageBytes;
+};
 
 struct Bars {
-  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t kv_full[kMaxStages], kv_empty[kMaxStages];
+  uint64_t s8_full[kMaxStages];               // E4M3: the stage's E4M3 tile has landed
   uint64_t s_full[kQT][2], p_full[kQT][2], p_free[kQT][2], o_done[kQT];
   uint64_t o_final[kQT];                      // query tile t's last P V has completed
   uint64_t v_zeroed;                          // the tail tile's V rows past the end are zero
@@ -85,14 +103,17 @@ __device__ __forceinline__ int key_tiles(const DecodeArgs& a, int n, int qt) {
   return p_last >= 0 ? (p_last + kN) / kN : 0;
 }
 
-template <bool kBf16>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int KVT>
+__global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeArgs a) {
+  using C = PfCfg<KVT>;
+  constexpr bool kBf16 = C::kBf16, kFp8 = C::kFp8;
+  constexpr int kStages = C::kStages;
   constexpr bool kSplitP = kBf16;            // f16 P (11 bits) needs no low term
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  Bars* bars = reinterpret_cast<Bars*>(sm + kSmemBytes);
+  Bars* bars = reinterpret_cast<Bars*>(sm + C::kSmemBytes);
   const uint32_t base = smem_u32(sm);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // shared-prefix mode: query token i is sequence i, one key table (the prefix),
@@ -128,9 +149,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&bars->kv_full[i], 1);
+      mbar_init(&bars->kv_full[i], kFp8 ? C::kConvWarps : 1);   // the converters, or TMA
       mbar_init(&bars->kv_empty[i], kIssuers);   // one commit from each MMA issuer
     }
+    if (kFp8)
+      for (int i = 0; i < kStages; ++i) mbar_init(&bars->s8_full[i], 1);
     for (int t = 0; t < kQT; ++t) {
       for (int b = 0; b < 2; ++b) {
         mbar_init(&bars->s_full[t][b], 1);
@@ -163,6 +186,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       uint4 v = live ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+      if (kFp8 && a.q_dtype == PKV_BF16) {
+        // the MMAs of an E4M3 pool run on f16 operands: q bf16 -> f16
+        uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = unpack2<true>(w[e]);
+          w[e] = pack_f16(f.x, f.y);
+        }
+      }
       v.x ^= flip;
       v.y ^= flip;
       v.z ^= flip;
@@ -235,6 +267,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                         &tmap, &bars->kv_full[st], h * 64, hkv * a.BS, z);
           }
         };
+        if constexpr (kFp8) {
+          // E4M3: one box per block and K/V (128 one-byte columns: the whole row)
+          // into the V half of the stage: E4M3 K where f16 V half 0 goes, E4M3 V
+          // where half 1 goes; the converters then fill the stage in place
+          auto load8 = [&](int j) {
+            const int st = j % kStages;
+            last_load[st] = j;
+            const int first = (jt0 + j) * bpt;
+            if (id_base < 0 || first + bpt > id_base + 32) {
+              id_base = first;
+              ids = id_base + lane < nblk ? __ldg(trow + id_base + lane) : 0;
+            }
+            const int jb = min(first + (lane >> 1), nblk - 1);
+            int blk = __shfl_sync(0xffffffffu, ids, jb - id_base);
+            if (leader) mbar_arrive_expect_tx(&bars->s8_full[st], kStage8Bytes);
+            __syncwarp();
+            if (lane < 2 * bpt) {
+              if (blk < 0 || blk >= a.num_blocks) {
+                record_error(a.status, PKV_EBOUNDS);
+                blk = 0;
+              }
+              const int kv = lane & 1;
+              const int z = (blk * 2 + kv) * a.L + a.layer;
+              tma_load_3d(sm + kSmemKV + st * kStageBytes + (2 + kv) * kKVHalf +
+                              (lane >> 1) * a.BS * 128,
+                          &tmap, &bars->s8_full[st], 0, hkv * a.BS, z);
+            }
+          };
+          for (int j = 0; j < T && j < kStages; ++j) load8(j);
+          for (int k = kStages; k < T && ok; ++k) {
+            ok = wait(&bars->kv_empty[(k - kStages) % kStages], ((k - kStages) / kStages) & 1);
+            if (!ok) break;
+            load8(k);
+          }
+          if (leader)
+            for (int st = 0; st < kStages; ++st)
+              if (last_load[st] >= 0)
+                mbar_wait_bounded(&bars->s8_full[st], (last_load[st] / kStages) & 1);
+        } else {
         for (int j = 0; j < T && j < kStages; ++j) load_tile(j);
         // key tile k goes into the stage of tile k - kStages once every issuer's
         // MMAs reading that tile have completed
@@ -267,6 +338,80 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int st = 0; st < kStages; ++st)
             if (last_load[st] >= 0)
               mbar_wait_bounded(&bars->kv_full[st], (last_load[st] / kStages) & 1);
+        }
+      } else if (warp >= kWarpConv) {
+        if constexpr (kFp8) {
+        // ---------------------------------------------------------- E4M3 -> f16
+        // A tile's 64 keys are 16 groups of 4 rows; converter c takes groups
+        // [16c/W, 16(c+1)/W) of K and of V, a group per step: 4 rows x 8 16-byte
+        // chunks (a conflict-free 128-byte line per quarter warp).  E4M3 K row r
+        // and V row r sit exactly where f16 V row r goes (half 0, half 1), so a
+        // group's f16 V rows overwrite only the bytes the same step has read.
+        constexpr int W = C::kConvWarps;
+        const int c = warp - kWarpConv, g0 = 16 * c / W, g1 = 16 * (c + 1) / W;
+        const int nblk = (n + a.BS - 1) / a.BS;
+        const int32_t* trow = a.tables + (size_t)s * a.max_blocks;
+        const int ch = lane & 7, up = ch >> 2;
+        // 16 E4M3 values d = 16ch .. 16ch+15 -> f16 (times a per-block scale), in
+        // store order: a lane of the upper f16 half (ch >= 4) writes its odd
+        // chunk first, so that a row's 8 lanes hit 8 distinct bank groups
+        auto convert = [&](const uint4 x, float sc, uint32_t (&o)[8]) {
+          const uint32_t xw[4] = {up ? x.z : x.x, up ? x.w : x.y, up ? x.x : x.z, up ? x.y : x.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) e4m3x4_to_f16x2x2(xw[e], o[2 * e], o[2 * e + 1]);
+          if (a.block_scales) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float2 f = unpack2<false>(o[e]);
+              o[e] = pack_f16(f.x * sc, f.y * sc);
+            }
+          }
+        };
+        // ... into f16 half `up` of K (kv 0) or V (kv 1): chunks 2(ch % 4) and +1
+        auto store = [&](uint8_t* dst, int kv, int row, const uint32_t (&o)[8]) {
+          uint8_t* half = dst + (kv * 2 + up) * kKVHalf;
+          *reinterpret_cast<uint4*>(half + sw128(row, 2 * (ch & 3) + up)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(half + sw128(row, 2 * (ch & 3) + 1 - up)) = make_uint4(o[4], o[5], o[6], o[7]);
+        };
+        for (int j = 0; j < T && ok; ++j) {
+          const int st = j % kStages;
+          ok = wait(&bars->s8_full[st], (j / kStages) & 1);
+          if (!ok) break;
+          uint8_t* dst = sm + kSmemKV + st * kStageBytes;
+          const uint8_t* src = dst + 2 * kKVHalf;              // E4M3 K rows, then V rows
+          const int valid = n - (jt0 + j) * kN;                // keys of the tile in the sequence
+#pragma unroll 1
+          for (int gr = g0; gr < g1; ++gr) {
+            const int row = 4 * gr + (lane >> 3);
+            const uint4 xk = *reinterpret_cast<const uint4*>(src + sw128(row, ch));
+            const uint4 xv = *reinterpret_cast<const uint4*>(src + kKVHalf + sw128(row, ch));
+            // per-block scales: those of the row's block (per-tensor: applied elsewhere)
+            float sk = 1.f, sv = 1.f;
+            if (a.block_scales) {
+              const int jb = min((jt0 + j) * (kN / a.BS) + row / a.BS, nblk - 1);
+              int blk = __ldg(trow + jb);
+              blk = (blk < 0 || blk >= a.num_blocks) ? 0 : blk;
+              const size_t k0 = ((size_t)blk * 2 * a.L + a.layer) * a.Hkv + hkv;
+              sk = __ldg(a.block_scales + k0);
+              sv = __ldg(a.block_scales + k0 + (size_t)a.L * a.Hkv);
+            }
+            __syncwarp();                                       // the group's E4M3 bytes are read
+            uint32_t o[8];
+            convert(xk, sk, o);
+            store(dst, 0, row, o);
+            convert(xv, sv, o);
+            if (row >= valid) {
+              // keys past the sequence end: zero V, so that P = 0 never meets NaN
+#pragma unroll
+              for (int e = 0; e < 8; ++e) o[e] = 0u;
+            }
+            store(dst, 1, row, o);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (leader) mbar_arrive(&bars->kv_full[st]);
+        }
+        }
       } else if (warp < kWarpPV) {
         const int t = warp - kWarpS;                           // this warp's query tile
         const uint64_t qb = d_k + ((kSmemQ + t * 2 * kHalf) >> 4);
@@ -298,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok && j < tiles[t]) {
             const int b = j & 1;
             ok = wait(&bars->p_full[t][b], (j >> 1) & 1);
-            if (ok && j == j_tail) ok = wait(&bars->v_zeroed, 0);
+            if (!kFp8 && ok && j == j_tail) ok = wait(&bars->v_zeroed, 0);
             if (!ok) break;
             tc_fence_after();
             if (leader) {
@@ -440,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int odt = casc ? PKV_F32 : a.out_dtype;
     if (ok && my_tiles > 0 && wait(&bars->o_final[t], 0)) {
       tc_fence_after();
-      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      const float inv = lsum > 0.f ? a.v_scale / lsum : 0.f;
 #pragma unroll
       for (int c = 0; c < kD; c += 32) {
         float o[32];
@@ -472,29 +617,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-size_t prefill_tc_smem_bytes() { return kSmemBytes + sizeof(Bars) + kAlignSlack; }
+template <int KVT>
+size_t smem_bytes_t() { return PfCfg<KVT>::kSmemBytes + sizeof(Bars) + kAlignSlack; }
+
+template <int KVT>
+cudaError_t launch_t(const CUtensorMap* map, const DecodeArgs& a, dim3 grid, cudaStream_t stream) {
+  const size_t smem = smem_bytes_t<KVT>();
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<KVT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess)
+    prefill_tc_kernel<KVT><<<grid, PfCfg<KVT>::kThreads, smem, stream>>>(*map, a);
+  return e;
+}
 
 bool prefill_tc_supported(int kv_dtype, int q_dtype, int BS, int D, int G) {
-  return (kv_dtype == PKV_BF16 || kv_dtype == PKV_F16) && q_dtype == kv_dtype && D == kD &&
-         (BS == 16 || BS == 32 || BS == 64) && G >= 1 && G <= kM && kM % G == 0;
+  const bool dt_ok = (kv_dtype == PKV_BF16 || kv_dtype == PKV_F16) ? q_dtype == kv_dtype
+                     : kv_dtype == PKV_FP8_E4M3 ? (q_dtype == PKV_BF16 || q_dtype == PKV_F16)
+                                                : false;
+  return dt_ok && D == kD && (BS == 16 || BS == 32 || BS == 64) && G >= 1 && G <= kM &&
+         kM % G == 0;
 }
 
 cudaError_t launch_prefill_tc(const CUtensorMap* map, const DecodeArgs& a, cudaStream_t stream) {
   const int QT = kM / a.G;
   const int qtiles = (a.q_len + QT - 1) / QT;
   if (qtiles == 0 || a.B == 0) return cudaSuccess;
-  const size_t smem = prefill_tc_smem_bytes();
-  cudaError_t e;
   if (a.key_limit && (a.S < 1 || a.S > 65535 || a.B != 1 || !a.out_lse)) return cudaErrorInvalidValue;
   dim3 grid((qtiles + kQT - 1) / kQT, a.Hkv, a.key_limit ? a.S : a.B);
-  if (a.kv_dtype == PKV_BF16) {
-    e = cudaFuncSetAttribute(prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-    if (e == cudaSuccess) prefill_tc_kernel<true><<<grid, kThreads, smem, stream>>>(*map, a);
-  } else {
-    e = cudaFuncSetAttribute(prefill_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-    if (e == cudaSuccess) prefill_tc_kernel<false><<<grid, kThreads, smem, stream>>>(*map, a);
+  cudaError_t e;
+  switch (a.kv_dtype) {
+    case PKV_BF16: e = launch_t<PKV_BF16>(map, a, grid, stream); break;
+    case PKV_F16: e = launch_t<PKV_F16>(map, a, grid, stream); break;
+    case PKV_FP8_E4M3: e = launch_t<PKV_FP8_E4M3>(map, a, grid, stream); break;
+    default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();

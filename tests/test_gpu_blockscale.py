@@ -69,20 +69,23 @@ def test_block_scales_and_pool_bit_exact(case):
     assert pool.check_status() == 0
 
 
-@pytest.mark.parametrize("mode", ["auto", "simt", "split3", "fused", "mq2"])
+@pytest.mark.parametrize("mode", ["auto", "simt", "split3", "fused", "mq2", "mq40"])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: c.name)
 def test_block_scaled_decode_parity(case, mode):
     from paged_kv_cache_215_gb300 import pkv
     tens, pool, scales, tables, lens, osc, opool = _setup(case)
     q = tens.q.cuda()
     maxlen = int(case.seq_lens.max())
-    if mode == "mq2":
+    if mode in ("mq2", "mq40"):
+        # 2 tokens: the mma.sync kernel; 40 tokens (160+ rows per KV head): the
+        # tcgen05 kernel, converting each E4M3 tile with its block's scale
+        ql = 2 if mode == "mq2" else 40
         pool.append(case.layer, tens.k_new.cuda(), tens.v_new.cuda(), tables, tens.new_pos.cuda())
         g = torch.Generator().manual_seed(3)
-        q2 = torch.randn(case.batch, 2, case.num_q_heads, case.head_dim, generator=g).bfloat16()
+        q2 = torch.randn(case.batch, ql, case.num_q_heads, case.head_dim, generator=g).bfloat16()
         ref, _ = oracle.decode_mq(np_raw(q2), "bf16", opool, "e4m3", case.geometry, case.layer,
-                                  case.tables, case.seq_lens, 2, case.scale, block_scales=osc)
-        out = torch.full((case.batch, 2, case.num_q_heads, case.head_dim), float("nan"),
+                                  case.tables, case.seq_lens, ql, case.scale, block_scales=osc)
+        out = torch.full((case.batch, ql, case.num_q_heads, case.head_dim), float("nan"),
                          device="cuda")
         pkv.paged_decode_attention_mq(out, q2.cuda(), pool, case.layer, tables, lens, maxlen,
                                       case.scale)

@@ -77,9 +77,9 @@ def test_multi_token_decode_with_one_token_equals_decode():
     assert torch.equal(out[:, 0], single)
 
 
-def test_large_chunks_route_to_tcgen05_or_are_refused():
-    """More than 16 query rows per KV head: bf16 pools run on the tcgen05 kernel
-    (checked against the oracle); E4M3 pools have no kernel for it."""
+def test_large_chunks_route_to_tcgen05():
+    """More than 16 query rows per KV head run on the tcgen05 kernel, bf16 and
+    E4M3 pools alike (checked against the oracle)."""
     from paged_kv_cache_215_gb300 import pkv
     case = wl.llama8b_batch(batch=2, lo=100, hi=200, seed=67)
     tens = wl.make_tensors(case)
@@ -98,10 +98,17 @@ def test_large_chunks_route_to_tcgen05_or_are_refused():
     for s_ in seqs:
         assert np.abs(got[s_] - ref[s_]).max() <= TOL["bf16"] * vm[s_]
     c8 = wl.make_case("mq_fp8_big", [300], 32, 8, 128, 16, "e4m3", "bf16", "bf16", seed=68)
-    g8 = GpuCase(c8)
-    q8 = torch.zeros(1, 5, 32, 128, dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(pkv.PkvError) as e:
-        pkv.paged_decode_attention_mq(torch.empty(1, 5, 32, 128, device="cuda"), q8, g8.pool, 0,
-                                      g8.tables, g8.seq_lens, g8.max_seq_len, c8.scale,
-                                      g8.k_scale, g8.v_scale)
-    assert e.value.code == pkv.PKV_EUNSUPPORTED
+    t8 = wl.make_tensors(c8)
+    g8 = GpuCase(c8, t8)
+    g8.pool.append(0, g8.k_new, g8.v_new, g8.tables, g8.new_pos, g8.k_scale, g8.v_scale)
+    pool8, _, seqs8 = oracle_side(c8, t8, None, g8.k_scale, g8.v_scale)
+    q8 = _q(c8, 5, seed=6)
+    ref8, _ = oracle.decode_mq(np_raw(q8), "bf16", pool8, "e4m3", c8.geometry, 0, c8.tables,
+                               c8.seq_lens, 5, c8.scale, g8.k_scale, g8.v_scale)
+    out8 = torch.empty(1, 5, 32, 128, device="cuda")
+    pkv.paged_decode_attention_mq(out8, q8.cuda(), g8.pool, 0, g8.tables, g8.seq_lens,
+                                  g8.max_seq_len, c8.scale, g8.k_scale, g8.v_scale)
+    torch.cuda.synchronize()
+    assert g8.status() == 0
+    vm8 = vmax_per_seq(c8, pool8, seqs8, g8.v_scale)
+    assert np.abs(out8.double().cpu().numpy()[0] - ref8[0]).max() <= TOL["e4m3"] * vm8[0]
