@@ -604,6 +604,41 @@ def measure_cascade(name, device, steps=20):
             "unique_kv_bytes": unique_kv_bytes(c)}
 
 
+APPEND = ["llama8b_b32_8k", "fp8_b8_32k"]
+
+
+def measure_append(name, device, calls=50, reps=4):
+    """Latency of kv_append alone (reshape_and_cache of one new token per sequence,
+    bf16 in, the pool's dtype stored) on the workload's pool: a CUDA graph of
+    `calls` back-to-back appends, replayed; microseconds per call."""
+    w = Workload(name, device)
+    c, t = w.case, w.tens
+
+    def app():
+        w.pool.append(c.layer, t.k_new, t.v_new, w.tables, t.new_pos, w.ks, w.vs)
+    app()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(calls):
+            app()
+    g.replay()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(reps):
+        g.replay()
+    e.record()
+    torch.cuda.synchronize()
+    us = s.elapsed_time(e) * 1e3 / (calls * reps)
+    assert w.pool.check_status() == 0
+    per_tok = 2 * c.num_kv_heads * c.head_dim
+    moved = c.batch * per_tok * (2 + c.kv_elem_bytes())       # bf16 in, pool dtype out
+    w.close()
+    return {"batch": c.batch, "kv_dtype": c.kv_dtype, "us_per_call": us,
+            "bytes_per_call": moved, "timing": f"CUDA graph of {calls} appends, {reps} replays"}
+
+
 def bf16_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -657,6 +692,8 @@ def run_ours(args):
             others[cp.pop("workload")] = cp
         for cname in CASCADE:
             others[f"{cname}_shared_prefix_decode"] = measure_cascade(cname, device)
+        for aname in APPEND:
+            others[f"{aname}_append"] = measure_append(aname, device)
     if ws > 1:
         dist.barrier()
     if rank != 0:
