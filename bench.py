@@ -572,15 +572,17 @@ def measure_cascade(name, device, steps=20):
     ws = torch.empty(pkv.cascade_workspace_bytes(w.geom, c.batch, c.max_blocks, w.max_len, P),
                      dtype=torch.uint8, device=device)
 
-    def cascade():
+    def cascade(route=0):
         pkv.paged_decode_attention_cascade(out, w.tens.q, w.pool, c.layer, table, P, lens,
-                                           w.tables, w.seq_lens, w.max_len, c.scale, workspace=ws)
+                                           w.tables, w.seq_lens, w.max_len, c.scale, workspace=ws,
+                                           opts=pkv.launch_opts(kernel=route))
 
     def plain():
         pkv.paged_decode_attention(w.out, w.tens.q, w.pool, c.layer, w.tables, w.seq_lens,
                                    w.max_len, c.scale, workspace=w.ws)
     res = {}
-    for nm, f in (("plain", plain), ("cascade", cascade)) * 2:
+    arms = (("plain", plain), ("cascade", cascade), ("prefix_pass", lambda: cascade(3)))
+    for nm, f in arms * 2:
         for _ in range(3):
             f()
         torch.cuda.synchronize()
@@ -598,6 +600,7 @@ def measure_cascade(name, device, steps=20):
     torch.cuda.empty_cache()
     return {"batch": c.batch, "shared_prefix_tokens": P, "status": status,
             "plain_us": res["plain"], "cascade_us": res["cascade"],
+            "prefix_pass_us": res["prefix_pass"],
             "speedup": res["plain"] / res["cascade"],
             "kv_gbs_plain": kvb / (res["plain"] * 1e-6) / 1e9,
             "kv_gbs_cascade": kvb / (res["cascade"] * 1e-6) / 1e9,

@@ -313,10 +313,17 @@ PKV_API size_t paged_decode_workspace_bytes_mq(const pkv_geometry* geom, int bat
  * paged_decode_workspace_bytes_cascade; other arguments, ownership and errors as
  * in paged_decode_attention_ex.
  * When it pays: the prefix pass replaces one read of the shared blocks per
- * sequence; a prefix that stays in L2 (a few thousand tokens per layer) was
- * read once from HBM anyway, and then the extra pass and merge cost a few
- * percent.  Measured on one GB300: 32 sequences sharing 64K tokens, 6x faster
- * than paged_decode_attention; 64 sequences sharing 4K tokens, 4% slower. */
+ * sequence.  A prefix whose K/V (prefix_len_max x 2 x num_kv_heads x head_dim
+ * elements) fill at most a quarter of the device's L2 is read from HBM about
+ * once by the plain decode too (the sequences reach their first blocks together
+ * and the repeats hit in L2); the extra pass and merge would then cost more than
+ * they save, so such a call runs steps 2-3 as paged_decode_attention over the
+ * sequences' own tables, after the same check of step 1.  opts->kernel (opts
+ * may be NULL): 0 that automatic choice, 2 always the plain decode, 3 always the
+ * prefix pass; other values PKV_EINVAL; the other fields are ignored.
+ * Measured on one GB300: 32 sequences sharing 64K tokens (268 MB of K/V), 6x
+ * faster than paged_decode_attention; 64 sequences sharing 4K tokens (17 MB),
+ * the prefix pass 6% slower than the plain decode. */
 PKV_API int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void* d_q,
                                            pkv_dtype q_dtype, const pkv_pool* pool, int layer,
                                            const int32_t* d_prefix_table, int prefix_blocks,
@@ -324,7 +331,7 @@ PKV_API int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, con
                                            const int32_t* d_block_tables, int max_blocks_per_seq,
                                            const int32_t* d_seq_lens, int batch, int max_seq_len,
                                            float scale, void* d_workspace, size_t ws_bytes,
-                                           cudaStream_t stream);
+                                           const pkv_launch_opts* opts, cudaStream_t stream);
 /* Workspace bytes of paged_decode_attention_cascade (an upper bound over launch plans). */
 PKV_API size_t paged_decode_workspace_bytes_cascade(const pkv_geometry* geom, int batch,
                                                     int max_blocks_per_seq, int max_seq_len,

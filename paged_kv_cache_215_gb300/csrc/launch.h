@@ -79,6 +79,7 @@ cudaError_t launch_merge_units_ext(const DecodeArgs& a, cudaStream_t stream);
 // with pb_s = prefix_lens[s] / BS, suffix_lens[s] = seq_lens[s] - prefix_lens[s];
 // n_prefix[0] = prefix_len_max.  A prefix that is not the shared table, not a
 // multiple of BS, or longer than the sequence is recorded as PKV_EINVAL.
+// suffix_tables == nullptr: only that check (suffix_lens, n_prefix untouched).
 cudaError_t launch_suffix_tables(const int32_t* tables, int max_blocks, const int32_t* seq_lens,
                                  const int32_t* prefix_table, int prefix_blocks,
                                  const int32_t* prefix_lens, int prefix_len_max, int B, int BS,

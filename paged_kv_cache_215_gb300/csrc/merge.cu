@@ -365,13 +365,16 @@ __global__ void suffix_tables_kernel(const int32_t* tables, int max_blocks, cons
                    pl / BS > prefix_blocks || n > max_blocks * BS;
   if (bad && threadIdx.x == 0 && blockIdx.x == 0) record_error(status, PKV_EINVAL);
   const int pb = bad ? 0 : pl / BS;
-  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < max_blocks; j += gridDim.x * blockDim.x) {
+  // suffix_tables == nullptr: the check alone, over the prefix entries
+  const int jn = suffix_tables ? max_blocks : pb;
+  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < jn; j += gridDim.x * blockDim.x) {
     if (j < pb && tables[(size_t)s * max_blocks + j] != prefix_table[j])
       record_error(status, PKV_EINVAL);                     // not the shared prefix
-    suffix_tables[(size_t)s * max_blocks + j] =
-        j + pb < max_blocks ? tables[(size_t)s * max_blocks + j + pb] : -1;
+    if (suffix_tables)
+      suffix_tables[(size_t)s * max_blocks + j] =
+          j + pb < max_blocks ? tables[(size_t)s * max_blocks + j + pb] : -1;
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
+  if (suffix_tables && blockIdx.x == 0 && threadIdx.x == 0) {
     suffix_lens[s] = bad ? 0 : n - pl;
     if (s == 0) n_prefix[0] = prefix_len_max;
   }
@@ -395,7 +398,8 @@ cudaError_t launch_suffix_tables(const int32_t* tables, int max_blocks, const in
                                  int32_t* suffix_tables, int32_t* suffix_lens, int32_t* n_prefix,
                                  int32_t* status, cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
-  const int gx = (max_blocks + 255) / 256;
+  const int span = suffix_tables ? max_blocks : std::min(max_blocks, prefix_blocks);
+  const int gx = std::max(1, (span + 255) / 256);
   suffix_tables_kernel<<<dim3(gx > 64 ? 64 : gx, B), 256, 0, stream>>>(
       tables, max_blocks, seq_lens, prefix_table, prefix_blocks, prefix_lens, prefix_len_max, B, BS,
       suffix_tables, suffix_lens, n_prefix, status);

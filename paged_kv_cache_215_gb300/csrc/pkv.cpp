@@ -39,7 +39,7 @@ static bool act_dtype(int dtype) { return dtype == PKV_F32 || dtype == PKV_F16 |
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct DeviceInfo {
-  int sms = 0, smem_optin = 0, smem_per_sm = 0;
+  int sms = 0, smem_optin = 0, smem_per_sm = 0, l2_bytes = 0;
 };
 
 static bool device_info(DeviceInfo* out) {
@@ -55,7 +55,8 @@ static bool device_info(DeviceInfo* out) {
         cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
             cudaSuccess ||
         cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
-            cudaSuccess)
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
       return false;
     it = cache.emplace(dev, d).first;
   }
@@ -787,7 +788,7 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
                                    const int32_t* d_block_tables, int max_blocks_per_seq,
                                    const int32_t* d_seq_lens, int batch, int max_seq_len,
                                    float scale, void* d_workspace, size_t ws_bytes,
-                                   cudaStream_t stream) {
+                                   const pkv_launch_opts* opts, cudaStream_t stream) {
   pkv_pool* p = const_cast<pkv_pool*>(pool);
   if (!p || batch < 0 || layer < 0 || layer >= p->g.num_layers || max_seq_len < 0 ||
       prefix_len_max < 0 || max_blocks_per_seq < 1)
@@ -807,10 +808,21 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
       !prefill_tc_supported(g.kv_dtype, q_dtype, g.block_size, g.head_dim, G) ||
       !mma_supported(g.kv_dtype, g.block_size, g.head_dim, G, 1) || batch > 65535)
     return PKV_EUNSUPPORTED;
+  const int kernel = opts ? opts->kernel : 0;
+  if (kernel != 0 && kernel != 2 && kernel != 3) return PKV_EINVAL;
   DeviceInfo dev;
   if (!device_info(&dev)) return PKV_ECUDA;
   const size_t dec = paged_decode_workspace_bytes(&g, batch, max_seq_len, 0);
   const CascadeWs w = cascade_ws(g, batch, max_blocks_per_seq, prefix_len_max, dev.sms, dec);
+  // A prefix whose K/V fill at most a quarter of L2 is already read from HBM
+  // about once by the plain decode: every sequence reaches its first blocks at
+  // the start of the launch and the repeats hit in L2.  There the prefix pass,
+  // its partials and the wider merge cost more than they save, so such a call
+  // (or kernel = 2) runs the plain decode over the sequences' own tables, after
+  // the same prefix check; kernel = 3 always takes the prefix pass.
+  const size_t prefix_bytes = (size_t)prefix_len_max * 2 * g.num_kv_heads * g.head_dim *
+                              elem_bytes(g.kv_dtype);
+  const bool plain = kernel == 2 || (kernel == 0 && prefix_bytes * 4 <= (size_t)dev.l2_bytes);
   if (ws_bytes < w.bytes) return PKV_ENOMEM;
   char* ws = static_cast<char*>(d_workspace);
   int32_t* n_prefix = reinterpret_cast<int32_t*>(ws + w.n_off);
@@ -819,13 +831,19 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
   float* ext_o = reinterpret_cast<float*>(ws + w.o_off);
   float* ext_lse = reinterpret_cast<float*>(ws + w.lse_off);
 
-  // 1. suffix tables and lengths (and the check that each prefix is the shared one)
+  // 1. suffix tables and lengths (and the check that each prefix is the shared
+  //    one; the plain route runs the check alone)
   if (launch_suffix_tables(d_block_tables, max_blocks_per_seq, d_seq_lens,
                            prefix_len_max > 0 ? d_prefix_table : d_block_tables,
                            prefix_len_max > 0 ? prefix_blocks : 0, d_prefix_lens, prefix_len_max,
-                           batch, g.block_size, suf_tab, suf_lens, n_prefix, p->d_status,
+                           batch, g.block_size, plain ? nullptr : suf_tab,
+                           plain ? nullptr : suf_lens, plain ? nullptr : n_prefix, p->d_status,
                            stream) != cudaSuccess)
     return PKV_ECUDA;
+  if (plain)
+    return decode_common(d_out, out_dtype, d_q, q_dtype, 1, nullptr, nullptr, 0, pool, layer,
+                         d_block_tables, max_blocks_per_seq, d_seq_lens, batch, max_seq_len, scale,
+                         1.f, 1.f, 0, ws + w.dec_off, ws_bytes - w.dec_off, nullptr, stream);
   // 2. the shared prefix once for every sequence: tcgen05 tiles of 128 query rows
   //    (sequences x heads of a KV head), key range cut into w.S splits
   if (prefix_len_max > 0) {

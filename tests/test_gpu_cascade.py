@@ -1,6 +1,7 @@
 """Shared-prefix decode (needs a GPU): paged_decode_attention_cascade reads the
 blocks shared by many sequences once (tcgen05 prefix pass) and their private
-suffixes through the decode kernel, then merges.  It must equal the fp64
+suffixes through the decode kernel, then merges; a prefix small enough to stay in
+L2 goes through the plain decode instead.  Every route must equal the fp64
 oracle's attention over each sequence's whole table, within the decode bound
 max |err| <= 2e-3 x max|V| per sequence."""
 import numpy as np
@@ -52,8 +53,9 @@ def _prefix(case, used):
     return torch.from_numpy(table).cuda(), used, torch.from_numpy(lens).cuda()
 
 
+@pytest.mark.parametrize("route", [3, 0, 2], ids=["prefix_pass", "auto", "plain"])
 @pytest.mark.parametrize("case,prefixes", CASES, ids=lambda c: getattr(c, "name", ""))
-def test_cascade_matches_oracle_and_plain_decode(case, prefixes):
+def test_cascade_matches_oracle_and_plain_decode(case, prefixes, route):
     from paged_kv_cache_215_gb300 import pkv
     gc, pool, ref, seqs = _sides(case)
     plain = gc.step(append=False)
@@ -63,14 +65,17 @@ def test_cascade_matches_oracle_and_plain_decode(case, prefixes):
         for _ in range(2):                                  # twice: reused workspace state
             pkv.paged_decode_attention_cascade(out, gc.q, gc.pool, case.layer, table, P, lens,
                                                gc.tables, gc.seq_lens, gc.max_seq_len,
-                                               case.scale)
+                                               case.scale, opts=pkv.launch_opts(kernel=route))
         torch.cuda.synchronize()
         assert gc.status() == 0
         assert_parity(case, out, ref, pool, seqs, gc.v_scale, f"{case.name} prefix {P}")
         assert (out - plain).abs().max().item() <= 2e-3 * float(plain.abs().max())
+        if route != 3:                                      # these prefixes all fit in L2
+            assert torch.equal(out, plain)
 
 
-def test_cascade_reports_a_prefix_that_is_not_shared():
+@pytest.mark.parametrize("route", [3, 0])
+def test_cascade_reports_a_prefix_that_is_not_shared(route):
     from paged_kv_cache_215_gb300 import pkv
     case = CASES[2][0]
     gc, _, _, _ = _sides(case)
@@ -78,13 +83,14 @@ def test_cascade_reports_a_prefix_that_is_not_shared():
     bad = table.clone()
     bad[3] = (bad[3] + 1) % case.num_blocks                 # no longer the sequences' block
     out = torch.empty(case.batch, case.num_q_heads, case.head_dim, device="cuda")
+    o = pkv.launch_opts(kernel=route)
     pkv.paged_decode_attention_cascade(out, gc.q, gc.pool, case.layer, bad, P, lens, gc.tables,
-                                       gc.seq_lens, gc.max_seq_len, case.scale)
+                                       gc.seq_lens, gc.max_seq_len, case.scale, opts=o)
     assert gc.status() == pkv.PKV_EINVAL
     odd = lens.clone()
     odd[1] = 8                                              # not a multiple of the block size
     pkv.paged_decode_attention_cascade(out, gc.q, gc.pool, case.layer, table, P, odd, gc.tables,
-                                       gc.seq_lens, gc.max_seq_len, case.scale)
+                                       gc.seq_lens, gc.max_seq_len, case.scale, opts=o)
     assert gc.status() == pkv.PKV_EINVAL
 
 
@@ -99,3 +105,12 @@ def test_cascade_rejects_what_it_has_no_kernel_for():
         pkv.paged_decode_attention_cascade(out, gc.q, gc.pool, case.layer, table, P, lens,
                                            gc.tables, gc.seq_lens, gc.max_seq_len, case.scale)
     assert e.value.code == pkv.PKV_EUNSUPPORTED
+    c16 = CASES[2][0]
+    g16, _, _, _ = _sides(c16)
+    table, P, lens = _prefix(c16, 256)
+    out = torch.empty(c16.batch, c16.num_q_heads, c16.head_dim, device="cuda")
+    with pytest.raises(pkv.PkvError) as e:                  # not a route of this entry
+        pkv.paged_decode_attention_cascade(out, g16.q, g16.pool, c16.layer, table, P, lens,
+                                           g16.tables, g16.seq_lens, g16.max_seq_len, c16.scale,
+                                           opts=pkv.launch_opts(kernel=1))
+    assert e.value.code == pkv.PKV_EINVAL
