@@ -388,6 +388,14 @@ PKV_API int paged_decode_attention_static(void* d_out, pkv_dtype out_dtype, cons
 PKV_API int pkv_check_status(const pkv_pool* pool, cudaStream_t stream);
 /* A static string naming a pkv_status. */
 PKV_API const char* pkv_strerror(int status);
+/* Failure-detection self-test.  One warp waits, through the bounded wait every
+ * kernel of this library uses on its mbarriers, on a barrier that nothing
+ * arrives on; when the bound runs out (1 s of the GPU's global timer) it
+ * records PKV_ETIMEOUT in the pool's status word and the kernel exits, so the
+ * next pkv_check_status returns PKV_ETIMEOUT and the context stays usable.
+ * Asynchronous on `stream`; returns PKV_EINVAL for a NULL pool or one without a
+ * status word, PKV_ECUDA if the launch fails. */
+PKV_API int pkv_wait_selftest(const pkv_pool* pool, cudaStream_t stream);
 /* Number of kernel launches this library has issued in this process (a
  * counter the benchmark reads to report its launches). */
 PKV_API uint64_t pkv_launch_count(void);

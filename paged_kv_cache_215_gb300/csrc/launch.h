@@ -112,4 +112,8 @@ cudaError_t launch_absmax(const void* x, int dtype, int64_t n, float* amax, cuda
 // Launch counter shared by every launcher.
 void count_launch();
 
+// One warp waits (bounded) on a barrier nothing arrives on and records
+// PKV_ETIMEOUT in `status`: the failure-detection self-test.
+cudaError_t launch_wait_selftest(int32_t* status, cudaStream_t stream);
+
 }  // namespace pkv

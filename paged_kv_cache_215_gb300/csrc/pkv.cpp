@@ -958,6 +958,11 @@ int pkv_check_status(const pkv_pool* p, cudaStream_t stream) {
   return w[0];
 }
 
+int pkv_wait_selftest(const pkv_pool* p, cudaStream_t stream) {
+  if (!p || !p->d_status) return PKV_EINVAL;
+  return launch_wait_selftest(p->d_status, stream) == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
 const char* pkv_strerror(int s) {
   switch (s) {
     case PKV_OK: return "ok";

@@ -87,6 +87,7 @@ def _load() -> ctypes.CDLL:
                                                Z, ctypes.POINTER(LaunchOpts), P]),
         "paged_decode_workspace_bytes_cascade": (Z, [G, I, I, I, I]),
         "pkv_check_status": (I, [P, P]),
+        "pkv_wait_selftest": (I, [P, P]),
         "pkv_strerror": (ctypes.c_char_p, [I]),
         "pkv_launch_count": (ctypes.c_uint64, []),
     }
@@ -107,7 +108,7 @@ EXPORTS = ("kv_pool_bytes", "kv_pool_create", "kv_pool_destroy", "kv_pool_geomet
            "paged_decode_attention_static", "paged_decode_step",
            "paged_decode_attention_mq", "paged_decode_workspace_bytes_mq",
            "paged_decode_attention_cascade", "paged_decode_workspace_bytes_cascade",
-           "pkv_check_status", "pkv_strerror", "pkv_launch_count")
+           "pkv_check_status", "pkv_wait_selftest", "pkv_strerror", "pkv_launch_count")
 
 
 def lib() -> ctypes.CDLL:
@@ -255,6 +256,11 @@ class KVPool:
 
     def check_status(self, stream=None) -> int:
         return int(_lib.pkv_check_status(self.handle, _stream(stream)))
+
+    def wait_selftest(self, stream=None):
+        """Launch the failure-detection self-test (a bounded wait that runs out,
+        about 1 s); the next check_status returns PKV_ETIMEOUT."""
+        _check(_lib.pkv_wait_selftest(self.handle, _stream(stream)), "pkv_wait_selftest")
 
 
 def kv_absmax(x: torch.Tensor, out: torch.Tensor, stream=None):
