@@ -87,3 +87,44 @@ def test_full_size_shared_prefix_decode_sampled_parity():
     del g, tens, pool
     _gc.collect()
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_full_size_chunked_prefill_sampled_parity(kv):
+    """The chunked-prefill workload the benchmark times (4 sequences x 16,384
+    tokens whose last 2,048 are new, 32/8 heads, D 128, bs 16; bf16 or E4M3
+    pool) on the tcgen05 kernel, whole batch on the GPU.  The oracle computes
+    the first and the last 16 query tokens of two sequences: the last ones as
+    the last 16 tokens of the sequence, the first ones as the last 16 tokens of
+    the sequence cut right after them (the same causal key range)."""
+    import oracle
+    from paged_kv_cache_215_gb300 import pkv
+    from tests.gpu_harness import TOL, vmax_per_seq
+    from tests.helpers import np_raw
+    B, ctx, chunk, m = 4, 16384, 2048, 16
+    case = wl.make_case(f"fullsize_prefill_{kv}", [ctx] * B, 32, 8, 128, 16, kv, "bf16", "bf16",
+                        seed=1007)
+    tens = wl.make_tensors(case, device="cuda")
+    g = GpuCase(case, tens)
+    g.pool.append(case.layer, g.k_new, g.v_new, g.tables, g.new_pos, g.k_scale, g.v_scale)
+    q = torch.randn(B, chunk, 32, 128, generator=torch.Generator().manual_seed(78)).bfloat16()
+    out = torch.full((B, chunk, 32, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pkv.paged_decode_attention_mq(out, q.cuda(), g.pool, case.layer, g.tables, g.seq_lens,
+                                  g.max_seq_len, case.scale, g.k_scale, g.v_scale)
+    torch.cuda.synchronize()
+    assert g.status() == 0
+    pool, _, seqs = oracle_side(case, tens, [0, 3], g.k_scale, g.v_scale)
+    vm = vmax_per_seq(case, pool, seqs, g.v_scale)
+    got = out.double().cpu().numpy()
+    for s in seqs:
+        for first, n in ((0, ctx - chunk + m), (chunk - m, ctx)):
+            ref, _ = oracle.decode_mq(np_raw(q[s:s + 1, first:first + m]), "bf16", pool, kv,
+                                      case.geometry, case.layer, case.tables[s:s + 1],
+                                      np.array([n], dtype=np.int32), m, case.scale, g.k_scale,
+                                      g.v_scale)
+            err = np.abs(got[s, first:first + m] - ref[0])
+            bound = TOL[kv] * vm[s] + 2.0 ** -8 * np.abs(ref[0])   # + half a bf16 ulp
+            assert np.all(err <= bound), f"{kv} seq {s} tokens {first}+: {err.max():.3e}"
+    del g, tens, pool
+    _gc.collect()
+    torch.cuda.empty_cache()

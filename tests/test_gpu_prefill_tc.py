@@ -110,9 +110,12 @@ def test_tcgen05_kernel_forced_on_short_chunks():
     _check(case, [1, 2, 7], kernel=3)
 
 
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
 @pytest.mark.parametrize("scale", [-0.125, 0.3])
-def test_tcgen05_softmax_scale_sign_and_size(scale):
+def test_tcgen05_softmax_scale_sign_and_size(scale, kv):
     """A negative scale (carried on Q by the kernel) and a large one (frequent
-    rescales of O) against the oracle at the same scale."""
-    case = wl.make_case("tc_scale", [400, 129], 32, 8, 128, 16, "bf16", "bf16", "bf16", seed=85)
+    rescales of O) against the oracle at the same scale; on E4M3 pools the scale
+    also carries k_scale."""
+    case = wl.make_case(f"tc_scale_{kv}", [400, 129], 32, 8, 128, 16, kv, "bf16", "bf16",
+                        seed=85)
     _check(case, [64, 100], kernel=0, scale=scale)
