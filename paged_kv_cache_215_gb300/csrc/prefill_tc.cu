@@ -90,6 +90,38 @@ struct Bars {
   volatile int abort_flag;
 };
 
+// Two FP32 lanes in one 64-bit register, for the f32x2 instructions (each lane
+// rounds exactly as the scalar instruction does).
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fsub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// max of three (one instruction)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
   return (uint32_t)row * 128u + ((uint32_t)(chunk ^ (row & 7)) << 4);
 }
@@ -507,13 +539,13 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
       if (__all_sync(0xffffffffu, live && kpos0 + kN - 1 <= pos)) {
         // the warp's rows see every key of the tile: no mask
 #pragma unroll
-        for (int c = 0; c < kN; ++c) mp[c & 7] = fmaxf(mp[c & 7], sv[c]);
+        for (int c = 0; c < kN; c += 2) mp[(c >> 1) & 7] = fmax3(mp[(c >> 1) & 7], sv[c], sv[c + 1]);
       } else {
 #pragma unroll
-        for (int c = 0; c < kN; ++c) {
-          const bool vis = live && kpos0 + c <= pos;
-          sv[c] = vis ? sv[c] : -INFINITY;
-          mp[c & 7] = fmaxf(mp[c & 7], sv[c]);
+        for (int c = 0; c < kN; c += 2) {
+          sv[c] = live && kpos0 + c <= pos ? sv[c] : -INFINITY;
+          sv[c + 1] = live && kpos0 + c + 1 <= pos ? sv[c + 1] : -INFINITY;
+          mp[(c >> 1) & 7] = fmax3(mp[(c >> 1) & 7], sv[c], sv[c + 1]);
         }
       }
       const float mx = qs * fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
@@ -526,9 +558,9 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
         rescale = j > 0;
       }
       const float ref = mref == -INFINITY ? 0.f : mref;
-      float pp[8];
+      uint64_t pp[4];                   // partial row sums, two lanes each
 #pragma unroll
-      for (int e = 0; e < 8; ++e) pp[e] = 0.f;
+      for (int e = 0; e < 4; ++e) pp[e] = 0ull;
       // a rescale needs O stable: P_{t,j-1} V_{j-1} done (its phase is the only
       // one pending here: P_tj is not yet written, and S_tj came after P_t,j-2 V)
       if (__any_sync(0xffffffffu, rescale)) {
@@ -551,26 +583,44 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
         }
       }
       // P over S_tj in TMEM, packed pairs: hi in columns 0..31 of the buffer, lo
-      // in 32..63; computed and stored 16 keys at a time (fewer live registers)
+      // in 32..63; computed and stored 16 keys at a time (fewer live registers).
+      // Two keys per FP32 instruction (f32x2 FMA / add / sub).
+      const uint64_t qs2 = f2_pack(qs, qs), nref2 = f2_pack(-ref, -ref);
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t phi[8], plo[8];
 #pragma unroll
         for (int c2 = 0; c2 < 8; ++c2) {
           const int c = q4 * 16 + 2 * c2;
-          // p = 2^(s * scale - ref): one FMA and the SFU per key
-          const float p0 = ex2_ftz(fmaf(sv[c], qs, -ref)), p1 = ex2_ftz(fmaf(sv[c + 1], qs, -ref));
-          pp[c2] += p0 + p1;
-          phi[c2] = pack2<kBf16>(p0, p1);
+          // p = 2^(s * scale - ref): one FMA per two keys and the SFU per key
+          float x0, x1;
+          f2_unpack(ffma2(f2_pack(sv[c], sv[c + 1]), qs2, nref2), x0, x1);
+          const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
+          const uint64_t p2 = f2_pack(p0, p1);
+          pp[c2 & 3] = fadd2(pp[c2 & 3], p2);
           if (kSplitP) {
-            const float2 h = unpack2<true>(phi[c2]);
-            plo[c2] = pack_bf16(p0 - h.x, p1 - h.y);
+            // hi = p with the low 16 bits cut (bf16 truncation), lo = p - hi exactly,
+            // then rounded to bf16: |lo| < 2^-8 p, so P carries 2^-17 relative error
+            const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+            phi[c2] = __byte_perm(b0, b1, 0x7632u);
+            float l0, l1;
+            f2_unpack(fsub2(p2, f2_pack(__uint_as_float(b0 & 0xffff0000u),
+                                        __uint_as_float(b1 & 0xffff0000u))), l0, l1);
+            plo[c2] = pack_bf16(l0, l1);
+          } else {
+            phi[c2] = pack2<kBf16>(p0, p1);
           }
         }
         tmem_st8(tcol + b * kN + q4 * 8, phi);
         if (kSplitP) tmem_st8(tcol + b * kN + 32 + q4 * 8, plo);
       }
-      const float ps = ((pp[0] + pp[1]) + (pp[2] + pp[3])) + ((pp[4] + pp[5]) + (pp[6] + pp[7]));
+      float ps = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float u0, u1;
+        f2_unpack(pp[e], u0, u1);
+        ps += u0 + u1;
+      }
       lsum = lsum * alpha + ps;
       tmem_st_wait();
       tc_fence_before();
