@@ -306,10 +306,12 @@ PKV_API size_t paged_decode_workspace_bytes_mq(const pkv_geometry* geom, int bat
  *      suffix table built in the workspace, and one merge combines all partials
  *      by log-sum-exp ([SEQPAR] incremental softmax).
  * d_prefix_table: int32 [prefix_blocks], prefix_len_max <= prefix_blocks *
- * block_size (0: plain decode through the same path).  bf16 / f16 pools, q in
- * the pool's dtype, head_dim 128, num_q_heads / num_kv_heads dividing 128 and at
- * most 8 (16 at block size <= 32); otherwise PKV_EUNSUPPORTED.  No E4M3 scales
- * (the pool must not be E4M3).  The workspace (caller-owned, 16-byte aligned) is
+ * block_size (0: plain decode through the same path).  bf16 / f16 pools with q
+ * in the pool's dtype, or E4M3 pools with bf16 / f16 q (k_scale / v_scale as in
+ * paged_decode_attention, > 0, ignored for other pools and when the pool has
+ * per-block scales attached); head_dim 128, num_q_heads / num_kv_heads dividing
+ * 128 and at most 8 (16 at block size <= 32); otherwise PKV_EUNSUPPORTED (bad
+ * scales: PKV_EINVAL).  The workspace (caller-owned, 16-byte aligned) is
  * paged_decode_workspace_bytes_cascade; other arguments, ownership and errors as
  * in paged_decode_attention_ex.
  * When it pays: the prefix pass replaces one read of the shared blocks per
@@ -330,7 +332,8 @@ PKV_API int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, con
                                            int prefix_len_max, const int32_t* d_prefix_lens,
                                            const int32_t* d_block_tables, int max_blocks_per_seq,
                                            const int32_t* d_seq_lens, int batch, int max_seq_len,
-                                           float scale, void* d_workspace, size_t ws_bytes,
+                                           float scale, float k_scale, float v_scale,
+                                           void* d_workspace, size_t ws_bytes,
                                            const pkv_launch_opts* opts, cudaStream_t stream);
 /* Workspace bytes of paged_decode_attention_cascade (an upper bound over launch plans). */
 PKV_API size_t paged_decode_workspace_bytes_cascade(const pkv_geometry* geom, int batch,

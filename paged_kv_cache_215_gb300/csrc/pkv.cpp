@@ -787,8 +787,9 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
                                    int prefix_len_max, const int32_t* d_prefix_lens,
                                    const int32_t* d_block_tables, int max_blocks_per_seq,
                                    const int32_t* d_seq_lens, int batch, int max_seq_len,
-                                   float scale, void* d_workspace, size_t ws_bytes,
-                                   const pkv_launch_opts* opts, cudaStream_t stream) {
+                                   float scale, float k_scale, float v_scale, void* d_workspace,
+                                   size_t ws_bytes, const pkv_launch_opts* opts,
+                                   cudaStream_t stream) {
   pkv_pool* p = const_cast<pkv_pool*>(pool);
   if (!p || batch < 0 || layer < 0 || layer >= p->g.num_layers || max_seq_len < 0 ||
       prefix_len_max < 0 || max_blocks_per_seq < 1)
@@ -804,8 +805,13 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
     return PKV_EINVAL;
   if ((long long)max_seq_len > (long long)max_blocks_per_seq * g.block_size) return PKV_EINVAL;
   if (!std::isfinite(scale)) return PKV_EINVAL;
-  if (g.kv_dtype == PKV_FP8_E4M3 ||   // (no dequantisation scales in this entry's arguments)
-      !prefill_tc_supported(g.kv_dtype, q_dtype, g.block_size, g.head_dim, G) ||
+  const bool fp8 = g.kv_dtype == PKV_FP8_E4M3;
+  const float* bscales = fp8 ? p->d_block_scales : nullptr;
+  if (fp8 && !bscales &&
+      (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale)))
+    return PKV_EINVAL;
+  if (!fp8 || bscales) k_scale = v_scale = 1.f;   // unused, or the per-block scales instead
+  if (!prefill_tc_supported(g.kv_dtype, q_dtype, g.block_size, g.head_dim, G) ||
       !mma_supported(g.kv_dtype, g.block_size, g.head_dim, G, 1) || batch > 65535)
     return PKV_EUNSUPPORTED;
   const int kernel = opts ? opts->kernel : 0;
@@ -843,7 +849,7 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
   if (plain)
     return decode_common(d_out, out_dtype, d_q, q_dtype, 1, nullptr, nullptr, 0, pool, layer,
                          d_block_tables, max_blocks_per_seq, d_seq_lens, batch, max_seq_len, scale,
-                         1.f, 1.f, 0, ws + w.dec_off, ws_bytes - w.dec_off, nullptr, stream);
+                         k_scale, v_scale, 0, ws + w.dec_off, ws_bytes - w.dec_off, nullptr, stream);
   // 2. the shared prefix once for every sequence: tcgen05 tiles of 128 query rows
   //    (sequences x heads of a KV head), key range cut into w.S splits
   if (prefix_len_max > 0) {
@@ -873,14 +879,17 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
     t.q_len = batch;
     t.R = G * batch;
     t.S = w.S;
-    t.qk_scale_log2 = (float)((double)scale * 1.4426950408889634);
-    t.v_scale = 1.f;
+    // E4M3: per-tensor scales on the softmax scale and the partial O (as the
+    // decode kernel's partials carry them), per-block ones in the tile conversion
+    t.qk_scale_log2 = (float)((double)scale * 1.4426950408889634 * (double)k_scale);
+    t.v_scale = v_scale;
+    t.block_scales = bscales;
     if (launch_prefill_tc(map, t, stream) != cudaSuccess) return PKV_ECUDA;
   }
   // 3. the private suffixes, merged with the prefix partials
   const ExtPartials ext{ext_o, ext_lse, prefix_len_max > 0 ? w.S : 0};
   return decode_common(d_out, out_dtype, d_q, q_dtype, 1, nullptr, nullptr, 0, pool, layer, suf_tab,
-                       max_blocks_per_seq, suf_lens, batch, max_seq_len, scale, 1.f, 1.f, 0,
+                       max_blocks_per_seq, suf_lens, batch, max_seq_len, scale, k_scale, v_scale, 0,
                        ws + w.dec_off, ws_bytes - w.dec_off, nullptr, stream, &ext);
 }
 

@@ -83,8 +83,8 @@ def _load() -> ctypes.CDLL:
         "paged_decode_step": (I, [P, I, P, I, P, P, I, P, I, P, I, P, I, I, F, F, F, I, P, Z,
                                   ctypes.POINTER(LaunchOpts), P]),
         "paged_decode_attention_static": (I, [P, I, P, I, P, I, P, I, P, I, I, F, F, F, I, P]),
-        "paged_decode_attention_cascade": (I, [P, I, P, I, P, I, P, I, I, P, P, I, P, I, I, F, P,
-                                               Z, ctypes.POINTER(LaunchOpts), P]),
+        "paged_decode_attention_cascade": (I, [P, I, P, I, P, I, P, I, I, P, P, I, P, I, I, F, F,
+                                               F, P, Z, ctypes.POINTER(LaunchOpts), P]),
         "paged_decode_workspace_bytes_cascade": (Z, [G, I, I, I, I]),
         "pkv_check_status": (I, [P, P]),
         "pkv_wait_selftest": (I, [P, P]),
@@ -351,7 +351,8 @@ def cascade_workspace_bytes(geom: Geometry, batch: int, max_blocks: int, max_seq
 
 def paged_decode_attention_cascade(out, q, pool: KVPool, layer, prefix_table, prefix_len_max,
                                    prefix_lens, tables, seq_lens, max_seq_len, scale,
-                                   workspace=None, opts=None, stream=None):
+                                   k_scale=1.0, v_scale=1.0, workspace=None, opts=None,
+                                   stream=None):
     """Decode attention of sequences sharing a prefix of blocks: the prefix
     (prefix_table [P] int32, prefix_lens [B] int32 tokens per sequence) is read
     once for all of them; the result equals paged_decode_attention.  opts.kernel:
@@ -365,7 +366,7 @@ def paged_decode_attention_cascade(out, q, pool: KVPool, layer, prefix_table, pr
         _ptr(out), TORCH_CODE[out.dtype], _ptr(q), TORCH_CODE[q.dtype], pool.handle, layer,
         _ptr(prefix_table), int(prefix_table.numel()) if prefix_table is not None else 0,
         prefix_len_max, _ptr(prefix_lens), _ptr(tables), tables.shape[1], _ptr(seq_lens), B,
-        max_seq_len, scale, _ptr(workspace), workspace.numel(),
+        max_seq_len, scale, k_scale, v_scale, _ptr(workspace), workspace.numel(),
         ctypes.byref(opts) if opts is not None else None, _stream(stream)),
         "paged_decode_attention_cascade")
     return out

@@ -69,7 +69,7 @@ def test_block_scales_and_pool_bit_exact(case):
     assert pool.check_status() == 0
 
 
-@pytest.mark.parametrize("mode", ["auto", "simt", "split3", "fused", "mq2", "mq40"])
+@pytest.mark.parametrize("mode", ["auto", "simt", "split3", "fused", "mq2", "mq40", "cascade"])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: c.name)
 def test_block_scaled_decode_parity(case, mode):
     from paged_kv_cache_215_gb300 import pkv
@@ -98,6 +98,18 @@ def test_block_scaled_decode_parity(case, mode):
         if mode == "fused":
             pkv.paged_decode_step(out, q, tens.k_new.cuda(), tens.v_new.cuda(), pool, case.layer,
                                   tables, lens, maxlen, case.scale)
+        elif mode == "cascade":
+            # sequence 0's full blocks as a "shared" prefix that only it uses, on the
+            # forced prefix pass (tcgen05, each tile scaled by its block's scales)
+            pool.append(case.layer, tens.k_new.cuda(), tens.v_new.cuda(), tables,
+                        tens.new_pos.cuda())
+            kb = int(case.seq_lens[0]) // case.block_size
+            ptab = torch.from_numpy(case.tables[0, :max(kb, 1)].copy()).cuda()
+            plens = torch.zeros(case.batch, dtype=torch.int32, device="cuda")
+            plens[0] = kb * case.block_size
+            pkv.paged_decode_attention_cascade(out, q, pool, case.layer, ptab,
+                                               kb * case.block_size, plens, tables, lens, maxlen,
+                                               case.scale, opts=pkv.launch_opts(kernel=3))
         else:
             pool.append(case.layer, tens.k_new.cuda(), tens.v_new.cuda(), tables,
                         tens.new_pos.cuda())
