@@ -35,6 +35,8 @@
 // converted to f16 in registers (exact) and the per-tensor scales are applied
 // to the scores and to the output.
 #pragma once
+#include <algorithm>
+
 #include "device.cuh"
 #include "launch.h"
 
@@ -1022,7 +1024,9 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
 template <int KVT, int BS, int NT, bool kCausal>
 cudaError_t launch_t(const CUtensorMap* map, const DecodeArgs& a, int gx, int gy,
                      cudaStream_t stream) {
-  const size_t smem = mma_smem_bytes(KVT, BS, a.HG, a.stages);
+  // the ring needs mma_smem_bytes; a larger request (a.smem_bytes) caps how many
+  // CTAs can share an SM
+  const size_t smem = std::max(mma_smem_bytes(KVT, BS, a.HG, a.stages), (size_t)a.smem_bytes);
   auto kern = decode_mma_kernel<KVT, BS, NT, kCausal>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

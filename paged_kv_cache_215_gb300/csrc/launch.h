@@ -27,6 +27,7 @@ struct DecodeArgs {
   int HG;                    // kv heads per CTA (tensor-core kernel)
   int NHG;                   // Hkv / HG
   int stages;                // shared-memory pipeline depth
+  int smem_bytes;            // dynamic shared memory to request, if above what the ring needs
   int mode;                  // 0 balanced token stream, 1 fixed S partitions per sequence
   int S;                     // partitions per sequence in mode 1
   int q_len;                 // query tokens per sequence (1: decode; >1: causal chunk)

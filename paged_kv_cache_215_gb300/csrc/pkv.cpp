@@ -128,7 +128,15 @@ static bool plan_mma(const pkv_geometry& g, const DeviceInfo& dev, const pkv_lau
   p->ctas_per_sm = ctas;
   p->grid = dev.sms * ctas;
   p->smem = mma_smem_bytes(g.kv_dtype, g.block_size, hg, stages);
-  return p->smem <= (size_t)dev.smem_optin;
+  if (p->smem > (size_t)dev.smem_optin) return false;
+  // Request the SM's share of shared memory even when the ring needs less, so
+  // that at most `ctas` CTAs share an SM.  The balanced split gives every CTA
+  // the same bytes; small CTAs (one KV head each at block size 64) otherwise fit
+  // three or more to an SM, and a launch that starts while the previous grid
+  // drains (programmatic dependent launch) then stacks them unevenly.
+  const size_t share = (size_t)dev.smem_per_sm / ctas - 1024;
+  if (p->smem < share && share <= (size_t)dev.smem_optin) p->smem = share;
+  return true;
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -672,6 +680,7 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
     a.HG = plan.HG;
     a.NHG = plan.NHG;
     a.stages = plan.stages;
+    a.smem_bytes = (int)plan.smem;
     a.pdl = pdl;
     if (fused_append) {
       a.k_new = d_k_new;
