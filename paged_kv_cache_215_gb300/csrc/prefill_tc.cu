@@ -376,19 +376,21 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
         // ---------------------------------------------------------- E4M3 -> f16
         // A tile's 64 keys are 16 groups of 4 rows; converter c takes groups
         // [16c/W, 16(c+1)/W) of K and of V, a group per step: 4 rows x 8 16-byte
-        // chunks (a conflict-free 128-byte line per quarter warp).  E4M3 K row r
-        // and V row r sit exactly where f16 V row r goes (half 0, half 1), so a
-        // group's f16 V rows overwrite only the bytes the same step has read.
+        // chunks.  A quarter warp takes chunks 0-3 of one row and 4-7 of the next
+        // (rows of opposite parity, so their swizzles differ in the low bit): its
+        // 16-byte loads and both of its 16-byte stores (f16 halves 0 and 1) then
+        // hit 8 distinct bank groups.  E4M3 K row r and V row r sit exactly where
+        // f16 V row r goes (half 0, half 1), so a group's f16 V rows overwrite
+        // only the bytes the same step has read.
         constexpr int W = C::kConvWarps;
         const int c = warp - kWarpConv, g0 = 16 * c / W, g1 = 16 * (c + 1) / W;
         const int nblk = (n + a.BS - 1) / a.BS;
         const int32_t* trow = a.tables + (size_t)s * a.max_blocks;
-        const int ch = lane & 7, up = ch >> 2;
-        // 16 E4M3 values d = 16ch .. 16ch+15 -> f16 (times a per-block scale), in
-        // store order: a lane of the upper f16 half (ch >= 4) writes its odd
-        // chunk first, so that a row's 8 lanes hit 8 distinct bank groups
+        const int up = (lane >> 2) & 1, ch = 4 * up + (lane & 3);   // f16 half, source chunk
+        const int rsub = 2 * (lane >> 4) + (up ^ ((lane >> 3) & 1));  // row within the group
+        // 16 E4M3 values d = 16ch .. 16ch+15 -> f16 (times a per-block scale)
         auto convert = [&](const uint4 x, float sc, uint32_t (&o)[8]) {
-          const uint32_t xw[4] = {up ? x.z : x.x, up ? x.w : x.y, up ? x.x : x.z, up ? x.y : x.w};
+          const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) e4m3x4_to_f16x2x2(xw[e], o[2 * e], o[2 * e + 1]);
           if (a.block_scales) {
@@ -402,8 +404,8 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
         // ... into f16 half `up` of K (kv 0) or V (kv 1): chunks 2(ch % 4) and +1
         auto store = [&](uint8_t* dst, int kv, int row, const uint32_t (&o)[8]) {
           uint8_t* half = dst + (kv * 2 + up) * kKVHalf;
-          *reinterpret_cast<uint4*>(half + sw128(row, 2 * (ch & 3) + up)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(half + sw128(row, 2 * (ch & 3) + 1 - up)) = make_uint4(o[4], o[5], o[6], o[7]);
+          *reinterpret_cast<uint4*>(half + sw128(row, 2 * (ch & 3))) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(half + sw128(row, 2 * (ch & 3) + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
         };
         for (int j = 0; j < T && ok; ++j) {
           const int st = j % kStages;
@@ -414,7 +416,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
           const int valid = n - (jt0 + j) * kN;                // keys of the tile in the sequence
 #pragma unroll 1
           for (int gr = g0; gr < g1; ++gr) {
-            const int row = 4 * gr + (lane >> 3);
+            const int row = 4 * gr + rsub;
             const uint4 xk = *reinterpret_cast<const uint4*>(src + sw128(row, ch));
             const uint4 xv = *reinterpret_cast<const uint4*>(src + kKVHalf + sw128(row, ch));
             // per-block scales: those of the row's block (per-tensor: applied elsewhere)
