@@ -414,32 +414,52 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
           uint8_t* dst = sm + kSmemKV + st * kStageBytes;
           const uint8_t* src = dst + 2 * kKVHalf;              // E4M3 K rows, then V rows
           const int valid = n - (jt0 + j) * kN;                // keys of the tile in the sequence
+          // two groups a step (eight loads in flight a lane before the warp syncs)
 #pragma unroll 1
-          for (int gr = g0; gr < g1; ++gr) {
-            const int row = 4 * gr + rsub;
-            const uint4 xk = *reinterpret_cast<const uint4*>(src + sw128(row, ch));
-            const uint4 xv = *reinterpret_cast<const uint4*>(src + kKVHalf + sw128(row, ch));
-            // per-block scales: those of the row's block (per-tensor: applied elsewhere)
-            float sk = 1.f, sv = 1.f;
-            if (a.block_scales) {
-              const int jb = min((jt0 + j) * (kN / a.BS) + row / a.BS, nblk - 1);
-              int blk = __ldg(trow + jb);
-              blk = (blk < 0 || blk >= a.num_blocks) ? 0 : blk;
-              const size_t k0 = ((size_t)blk * 2 * a.L + a.layer) * a.Hkv + hkv;
-              sk = __ldg(a.block_scales + k0);
-              sv = __ldg(a.block_scales + k0 + (size_t)a.L * a.Hkv);
+          for (int gr = g0; gr < g1; gr += 2) {
+            const bool two = gr + 1 < g1;
+            const int row0 = 4 * gr + rsub, row1 = row0 + 4;
+            const uint4 xk0 = *reinterpret_cast<const uint4*>(src + sw128(row0, ch));
+            const uint4 xv0 = *reinterpret_cast<const uint4*>(src + kKVHalf + sw128(row0, ch));
+            uint4 xk1 = make_uint4(0, 0, 0, 0), xv1 = xk1;
+            if (two) {
+              xk1 = *reinterpret_cast<const uint4*>(src + sw128(row1, ch));
+              xv1 = *reinterpret_cast<const uint4*>(src + kKVHalf + sw128(row1, ch));
             }
-            __syncwarp();                                       // the group's E4M3 bytes are read
+            // per-block scales: those of the row's block (per-tensor: applied elsewhere)
+            float sk[2] = {1.f, 1.f}, sv[2] = {1.f, 1.f};
+            if (a.block_scales) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int jb = min((jt0 + j) * (kN / a.BS) + (row0 + 4 * h) / a.BS, nblk - 1);
+                int blk = __ldg(trow + jb);
+                blk = (blk < 0 || blk >= a.num_blocks) ? 0 : blk;
+                const size_t k0 = ((size_t)blk * 2 * a.L + a.layer) * a.Hkv + hkv;
+                sk[h] = __ldg(a.block_scales + k0);
+                sv[h] = __ldg(a.block_scales + k0 + (size_t)a.L * a.Hkv);
+              }
+            }
+            __syncwarp();                                       // the step's E4M3 bytes are read
             uint32_t o[8];
-            convert(xk, sk, o);
-            store(dst, 0, row, o);
-            convert(xv, sv, o);
-            if (row >= valid) {
+            convert(xk0, sk[0], o);
+            store(dst, 0, row0, o);
+            convert(xv0, sv[0], o);
+            if (row0 >= valid) {
               // keys past the sequence end: zero V, so that P = 0 never meets NaN
 #pragma unroll
               for (int e = 0; e < 8; ++e) o[e] = 0u;
             }
-            store(dst, 1, row, o);
+            store(dst, 1, row0, o);
+            if (two) {
+              convert(xk1, sk[1], o);
+              store(dst, 0, row1, o);
+              convert(xv1, sv[1], o);
+              if (row1 >= valid) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = 0u;
+              }
+              store(dst, 1, row1, o);
+            }
           }
           fence_proxy_async_smem();
           __syncwarp();
