@@ -217,8 +217,9 @@ PKV_API int paged_decode_attention(void* d_out, pkv_dtype out_dtype, const void*
  * means "automatic" for every field. */
 typedef struct {
   int32_t kernel;          /* 0 auto, 1 the SIMT kernel, 2 the mma.sync tensor-core kernel,
-                              3 the tcgen05 chunked-prefill kernel (multi-token calls,
-                              bf16/f16 pools, q dtype = pool dtype, num_splits = 0) */
+                              3 the tcgen05 chunked-prefill kernel (multi-token calls with
+                              num_splits = 0; the shared-prefix entry reads 2 / 3 as its
+                              plain / prefix-pass route) */
   int32_t ctas_per_sm;     /* 0 auto; the persistent grid is SMs x this */
   int32_t kv_heads_per_cta;/* 0 auto */
   int32_t stages;          /* 0 auto; shared-memory pipeline depth */
