@@ -149,3 +149,51 @@ def test_append_rejects_dtype_mismatch(pkv):
 def test_strerror_names_every_status(pkv):
     names = {pkv.strerror(c) for c in range(-6, 1)}
     assert len(names) == 7 and "unknown status" not in names
+
+
+def _c_kind(ctype):
+    t = " ".join(ctype.replace("const", " ").split())
+    if "*" in t or t in ("cudaStream_t",):
+        return "ptr"
+    if t in ("float",):
+        return "f32"
+    if t in ("double",):
+        return "f64"
+    if t in ("size_t",):
+        return "u64"                            # ctypes.c_size_t is c_uint64 on LP64
+    if t in ("int64_t", "long long"):
+        return "i64"
+    if t in ("uint64_t", "unsigned long long"):
+        return "u64"
+    if t in ("int", "int32_t", "pkv_dtype"):
+        return "i32"
+    raise AssertionError(f"unclassified C type {ctype!r}")
+
+
+def _ct_kind(ct):
+    if ct in (ctypes.c_void_p, ctypes.c_char_p) or (isinstance(ct, type) and
+                                                     issubclass(ct, ctypes._Pointer)):
+        return "ptr"
+    table = {ctypes.c_float: "f32", ctypes.c_double: "f64", ctypes.c_size_t: "u64",
+             ctypes.c_int64: "i64", ctypes.c_uint64: "u64", ctypes.c_int: "i32",
+             ctypes.c_int32: "i32"}
+    return table[ct]
+
+
+def test_binding_argument_lists_match_the_header(pkv):
+    """Every prototype in include/pkv.h against the ctypes argument list the
+    binding installs: same count, and pointer / 32-bit int / float / 64-bit
+    unsigned (size_t) / 64-bit int in every position (a stale binding would pass
+    wrong values)."""
+    hdr = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    hdr = re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)
+    protos = re.findall(r"PKV_API\s+[\w\s\*]+?\b(\w+)\s*\(([^)]*)\)\s*;", hdr)
+    assert len(protos) == len(pkv.EXPORTS)
+    lib = pkv.lib()
+    for name, params in protos:
+        params = " ".join(params.split())
+        args = [] if params in ("", "void") else [p.strip() for p in params.split(",")]
+        # drop the parameter name: the last identifier of each declaration
+        kinds = [_c_kind(re.sub(r"\b\w+$", "", a).strip() or a) for a in args]
+        got = [_ct_kind(t) for t in (getattr(lib, name).argtypes or [])]
+        assert kinds == got, f"{name}: header {kinds} binding {got}"
