@@ -664,8 +664,24 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
         tmem_ld32(tcol + 128 + c, o);
         tmem_ld_wait();
         if (live) {
+          // 16-byte stores of the row's 32 values (rows start on 256-byte
+          // boundaries of the 16-byte-aligned output)
+          if (odt == PKV_F32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow + c);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) store_from_float(a.out, orow + c + e, odt, o[e] * inv);
+            for (int e = 0; e < 8; ++e)
+              dst[e] = make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv,
+                                   o[4 * e + 3] * inv);
+          } else {
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              w[e] = odt == PKV_BF16 ? pack_bf16(o[2 * e] * inv, o[2 * e + 1] * inv)
+                                     : pack_f16(o[2 * e] * inv, o[2 * e + 1] * inv);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow + c);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          }
         }
       }
       if (casc && live)
