@@ -324,9 +324,9 @@ PKV_API size_t paged_decode_workspace_bytes_mq(const pkv_geometry* geom, int bat
  * sequences' own tables, after the same check of step 1.  opts->kernel (opts
  * may be NULL): 0 that automatic choice, 2 always the plain decode, 3 always the
  * prefix pass; other values PKV_EINVAL; the other fields are ignored.
- * Measured on one GB300: 32 sequences sharing 64K tokens (268 MB of K/V), 6x
+ * Measured on one GB300: 32 sequences sharing 64K tokens (268 MB of K/V), 7x
  * faster than paged_decode_attention; 64 sequences sharing 4K tokens (17 MB),
- * the prefix pass 6% slower than the plain decode. */
+ * the prefix pass 2% slower than the plain decode. */
 PKV_API int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void* d_q,
                                            pkv_dtype q_dtype, const pkv_pool* pool, int layer,
                                            const int32_t* d_prefix_table, int prefix_blocks,
