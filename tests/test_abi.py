@@ -136,6 +136,28 @@ def test_decode_rejects_bad_arguments_before_device_work(pkv):
     p.close()
 
 
+def test_shared_prefix_decode_rejects_bad_arguments_before_device_work(pkv):
+    p = FakePool(pkv, nb=8)                                # bf16, head_dim 64, bs 16
+    L = pkv.lib()
+    x = ctypes.c_void_p(1 << 20)
+    common = dict(ptab=x, pblocks=2, plen=32, plens=x, B=2, maxlen=64, ks=1.0, vs=1.0)
+
+    def call(**kw):
+        a = dict(common, **kw)
+        return L.paged_decode_attention_cascade(x, pkv.PKV_BF16, x, pkv.PKV_BF16, p.h, 0,
+                                                a["ptab"], a["pblocks"], a["plen"], a["plens"],
+                                                x, 4, x, a["B"], a["maxlen"], 0.125, a["ks"],
+                                                a["vs"], x, 1 << 20, None, None)
+    assert call(B=0) == 0                                  # empty batch: no-op
+    assert call(plen=8) == pkv.PKV_EINVAL                  # not a multiple of the block size
+    assert call(pblocks=1) == pkv.PKV_EINVAL               # longer than the prefix table
+    assert call(ptab=None) == pkv.PKV_EINVAL
+    assert call(plens=None) == pkv.PKV_EINVAL
+    assert call(maxlen=65) == pkv.PKV_EINVAL               # longer than the tables hold
+    assert call() == pkv.PKV_EUNSUPPORTED                  # head_dim 64: no tcgen05 kernel
+    p.close()
+
+
 def test_append_rejects_dtype_mismatch(pkv):
     p = FakePool(pkv, nb=8)
     x = ctypes.c_void_p(1 << 20)
