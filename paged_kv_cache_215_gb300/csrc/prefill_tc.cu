@@ -89,6 +89,11 @@ struct Bars {
   uint32_t tmem;
   volatile int abort_flag;
 };
+// the ring, the barriers and the alignment slack fit the 227 KB a CTA may opt into
+static_assert(PfCfg<PKV_BF16>::kSmemBytes + sizeof(Bars) + kAlignSlack <= 227u * 1024u, "smem");
+static_assert(PfCfg<PKV_FP8_E4M3>::kSmemBytes + sizeof(Bars) + kAlignSlack <= 227u * 1024u, "smem");
+// 16 warps at most: four to a scheduler keeps 128 registers a thread
+static_assert(PfCfg<PKV_FP8_E4M3>::kThreads <= 512, "threads");
 
 // Two FP32 lanes in one 64-bit register, for the f32x2 instructions (each lane
 // rounds exactly as the scalar instruction does).
