@@ -36,3 +36,21 @@ def test_reference_arm_prints_one_contract_line():
 def test_fewer_than_three_warmup_steps_are_refused():
     r = _bench("--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "2")
     assert r.returncode != 0 and "warmup" in r.stderr
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """Launched the way a multi-GPU run launches it (one process per rank),
+    rank 0 alone prints the line; the other ranks exit 0 without work."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                        "--nproc-per-node", "2", "--master-addr", "127.0.0.1", "--master-port",
+                        str(port), os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny", "--gpus", "2", "--steps", "3", "--warmup", "3"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    assert json.loads(lines[0])["impl"] == "reference"
