@@ -188,12 +188,7 @@ class Workload:
         self.max_len = int(c.seq_lens.max())
         self.ks = self.vs = 1.0
         if c.kv_dtype == "e4m3":
-            amax = torch.zeros(4, dtype=torch.float32, device=device)
-            for i, x in enumerate((t.k_tokens, t.k_new, t.v_tokens, t.v_new)):
-                pkv.kv_absmax(x, amax[i:i + 1])
-            a = amax.cpu().numpy()
-            self.ks = pkv.fp8_scale(float(max(a[0], a[1])))
-            self.vs = pkv.fp8_scale(float(max(a[2], a[3])))
+            self.ks, self.vs = pkv.fp8_scales((t.k_tokens, t.k_new), (t.v_tokens, t.v_new))
         self.pool.append_tokens(c.layer, t.k_tokens, t.v_tokens, self.tables, t.tok_seq,
                                 t.tok_pos, self.ks, self.vs)
         # the logical token arrays are no longer needed on the device
@@ -520,8 +515,7 @@ def measure_chunked_prefill(device, batch=4, context=16384, chunk=2048, steps=20
     lens = torch.from_numpy(case.seq_lens).to(device)
     ks = vs = 1.0
     if kv == "e4m3":
-        ks = pkv.fp8_scale(float(torch.maximum(t.k_tokens.abs().max(), t.k_new.abs().max())))
-        vs = pkv.fp8_scale(float(torch.maximum(t.v_tokens.abs().max(), t.v_new.abs().max())))
+        ks, vs = pkv.fp8_scales((t.k_tokens, t.k_new), (t.v_tokens, t.v_new))
     pool.append_tokens(0, t.k_tokens, t.v_tokens, tables, t.tok_seq, t.tok_pos, ks, vs)
     pool.append(0, t.k_new, t.v_new, tables, t.new_pos, ks, vs)
     g = torch.Generator(device=device).manual_seed(78)
@@ -748,8 +742,7 @@ def run_reference(args):
     if c.kv_dtype == "e4m3":
         ka = max(oracle.absmax(raw(tens.k_tokens), "bf16"), oracle.absmax(raw(tens.k_new), "bf16"))
         va = max(oracle.absmax(raw(tens.v_tokens), "bf16"), oracle.absmax(raw(tens.v_new), "bf16"))
-        ks = float(np.float32(ka) / np.float32(448)) if ka > 0 else 1.0
-        vs = float(np.float32(va) / np.float32(448)) if va > 0 else 1.0
+        ks, vs = oracle.fp8_scale(ka), oracle.fp8_scale(va)
     eb = c.kv_elem_bytes()
     pool = np.zeros(oracle.kv_bytes(c.num_layers, c.num_kv_heads, c.head_dim,
                                     c.num_blocks * c.block_size, eb), dtype=np.uint8)

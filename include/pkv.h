@@ -170,11 +170,22 @@ PKV_API int kv_block_scales(pkv_pool* pool, int layer, const void* d_k, const vo
                             int max_blocks_per_seq, int batch, const int32_t* d_seq_ids,
                             const int32_t* d_positions, int64_t num_tokens, cudaStream_t stream);
 
-/* Largest |x| over n elements of d_x (f32/f16/bf16; NaN ignored), written to
- * *d_amax (device float) on `stream`.  The per-tensor FP8 scale is amax / 448
- * (amax = 0 -> scale 1). */
+/* Absolute maximum behind the per-tensor FP8 scale ([UNLOCK] 3.2): the largest
+ * |x| over the finite elements of d_x (n elements of f32/f16/bf16; NaN and +-Inf
+ * are left out, 0 if none is finite), written to *d_amax (device float) on
+ * `stream`.  PKV_EINVAL for a NULL pointer, n < 0 or another dtype. */
 PKV_API int kv_absmax(const void* d_x, pkv_dtype dtype, int64_t n, float* d_amax,
                       cudaStream_t stream);
+
+/* Per-tensor FP8 E4M3 scale ([UNLOCK] 3.2, "per-tensor" FP8 with one fp32 scale
+ * for K and one for V): *d_scale = amax / 448 in IEEE fp32 (round to nearest),
+ * where amax is the largest of d_amax[0 .. n) -- the kv_absmax results of the
+ * pieces a tensor is held in (for example the cached tokens and the new ones) --
+ * and 448 is the largest finite E4M3 value, so the largest element is stored as
+ * +-448.  amax = 0 gives 1.  Both pointers are device floats; asynchronous on
+ * `stream`.  The result is what kv_append, kv_append_tokens and the decode calls
+ * take as k_scale / v_scale.  PKV_EINVAL for a NULL pointer or n < 1. */
+PKV_API int kv_fp8_scale(const float* d_amax, int n, float* d_scale, cudaStream_t stream);
 
 /* ---------------------------------------------------------------- decode attention */
 

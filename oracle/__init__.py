@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
             L.or_merge.argtypes = [P, P, P, P, LL, I, I]
             L.or_absmax.restype = D
             L.or_absmax.argtypes = [P, I, LL]
+            L.or_fp8_scale.restype = F
+            L.or_fp8_scale.argtypes = [D]
             L.or_to_f64.restype = None
             L.or_to_f64.argtypes = [P, P, I, LL, D]
             L.or_e4m3_encode.restype = ctypes.c_uint8
@@ -144,6 +146,11 @@ def absmax(raw, dtype: str) -> float:
     raw = np.ascontiguousarray(raw)
     n = raw.size * raw.itemsize // ELEM_BYTES[dtype]
     return float(lib().or_absmax(_ptr(raw), DT[dtype], n))
+
+
+def fp8_scale(amax: float) -> float:
+    """[UNLOCK 3.2] per-tensor E4M3 scale amax / 448 in fp32 (amax 0 gives 1)."""
+    return float(lib().or_fp8_scale(float(amax)))
 
 
 def decode(q, q_dtype, pool, kv_dtype, geom, layer, tables, seq_lens, scale,

@@ -144,6 +144,8 @@ uint8_t or_e4m3_encode(float x, float scale) {
   return sign | (uint8_t)(e << 3) | (uint8_t)m;
 }
 
+float or_fp8_scale(double amax);
+
 /* ---- [MHPN 3.1] / [ENG26 1.1] KV bytes: 2 x layers x kv_heads x head_dim x tokens x bytes ---- */
 uint64_t or_kv_bytes(uint64_t layers, uint64_t kv_heads, uint64_t head_dim, uint64_t tokens,
                      uint64_t elem_bytes) {
@@ -260,12 +262,12 @@ int or_block_scales(float* scales, int NB, int L, int Hkv, int bs, int D, int la
         touched[tile] = 1;
         for (int d = 0; d < D; ++d) {
           double x = fabs(or_load(kv ? v : k, ((size_t)i * Hkv + h) * D + d, in_dtype));
-          if (x > amax[tile]) amax[tile] = x;      /* NaN is ignored */
+          if (isfinite(x) && x > amax[tile]) amax[tile] = x;   /* NaN, +-Inf left out */
         }
       }
   }
   for (size_t t = 0; t < tiles; ++t)
-    if (touched[t]) scales[t] = amax[t] > 0 ? (float)amax[t] / 448.0f : 1.0f;
+    if (touched[t]) scales[t] = or_fp8_scale(amax[t]);
   free(amax);
   free(touched);
   return 0;
@@ -481,14 +483,26 @@ void or_merge(double* out, double* out_lse, const double* part_o, const double* 
   }
 }
 
-/* Largest |x| over n elements (NaN ignored); the per-tensor FP8 scale is amax / 448. */
+/* Largest |x| over the n elements' finite values ([UNLOCK 3.2] per-tensor FP8:
+ * the scale comes from the tensor's absolute maximum).  NaN and +-Inf are left
+ * out: the encoder already maps them to 0x7F and +-448, and a scale must be
+ * finite.  0 when no element is finite and nonzero. */
 double or_absmax(const void* x, int dtype, long long n) {
   double m = 0.0;
   for (long long i = 0; i < n; ++i) {
     double a = fabs(or_load(x, (size_t)i, dtype));
-    if (a > m) m = a;
+    if (isfinite(a) && a > m) m = a;
   }
   return m;
+}
+
+/* [UNLOCK 3.2] per-tensor FP8 scale from the absolute maximum: amax / 448 (448 is
+ * the largest finite E4M3 value, [OFP8]) in IEEE single precision, so that the
+ * largest element is stored as +-448; amax = 0 (an all-zero tensor) gives 1. */
+float or_fp8_scale(double amax) {
+  if (!(amax > 0.0)) return 1.0f;
+  float a = (float)amax;                 /* exact: amax is an f32/f16/bf16 value */
+  return a / 448.0f;
 }
 
 /* Decode an array of elements to fp64 (used by the tests to read pools). */

@@ -1,5 +1,5 @@
-// append.cu -- write new tokens' k and v into their pool slots, and the amax
-// reduction behind the per-tensor FP8 scale.
+// append.cu -- write new tokens' k and v into their pool slots, the amax
+// reduction behind the per-tensor FP8 scale, and the scale itself.
 //
 // "The engineering truth of long-context inference 2026", section 2.2
 // (append_token): block_id = pos // block_size, offset = pos % block_size,
@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(256) scales_amax_kernel(const AppendArgs a, fl
     const long long t = tile_of(a, tok, kv, h);
     if (t < 0) continue;
     const float x = fabsf(load_as_float(kv ? a.v : a.k, ((size_t)tok * a.Hkv + h) * a.D + d, IN));
-    if (isnan(x)) continue;
+    if (!isfinite(x)) continue;   // NaN and +-Inf do not set a scale
     atomicMax(reinterpret_cast<unsigned int*>(scales) + t, 0x80000000u | __float_as_uint(x));
   }
 }
@@ -124,10 +124,19 @@ __global__ void __launch_bounds__(256) absmax_kernel(const void* x, int64_t n, f
     if constexpr (IN == PKV_F32) v = static_cast<const float*>(x)[i];
     else if constexpr (IN == PKV_F16) v = __half2float(static_cast<const __half*>(x)[i]);
     else v = __bfloat162float(static_cast<const __nv_bfloat16*>(x)[i]);
-    m = fmaxf(m, fabsf(v));   // fmaxf ignores NaN
+    if (isfinite(v)) m = fmaxf(m, fabsf(v));   // NaN and +-Inf do not set a scale
   }
   m = warp_max(m);
   if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<int*>(amax), __float_as_int(m));
+}
+
+// Per-tensor scale of a tensor held in n pieces: amax = the largest of the
+// pieces' amax values, scale = amax / 448 (IEEE fp32 division), 1 when amax is 0.
+__global__ void fp8_scale_kernel(const float* amax, int n, float* scale) {
+  float m = 0.f;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) m = fmaxf(m, amax[i]);
+  m = warp_max(m);
+  if (threadIdx.x == 0) *scale = m > 0.f ? __fdiv_rn(m, 448.f) : 1.f;
 }
 
 template <int IN, int KV>
@@ -197,6 +206,13 @@ cudaError_t launch_absmax(const void* x, int dtype, int64_t n, float* amax, cuda
     default: return cudaErrorInvalidValue;
   }
   e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  return e;
+}
+
+cudaError_t launch_fp8_scale(const float* amax, int n, float* scale, cudaStream_t stream) {
+  fp8_scale_kernel<<<1, 32, 0, stream>>>(amax, n, scale);
+  const cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
   return e;
 }

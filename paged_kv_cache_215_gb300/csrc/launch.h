@@ -21,6 +21,7 @@ struct DecodeArgs {
   float* part_o;             // partial outputs (layout depends on mode)
   float* part_lse;           // partial natural log-sum-exp
   int2* unit_info;           // balanced mode: per unit (first slot, piece count)
+  int slots;                 // balanced mode: partial slots in the workspace (grid + units)
   int32_t* status;           // device error word or nullptr
   int B, Hq, Hkv, G, D, BS, L, layer, max_blocks, num_blocks;
   int q_dtype, out_dtype, kv_dtype;
@@ -109,6 +110,8 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 // Per-tile E4M3 scales amax / 448 of the tiles the tokens land in (three launches).
 cudaError_t launch_block_scales(const AppendArgs& a, float* scales, cudaStream_t stream);
 cudaError_t launch_absmax(const void* x, int dtype, int64_t n, float* amax, cudaStream_t stream);
+// scale = max(amax[0..n)) / 448 (1 when that is 0), one thread block.
+cudaError_t launch_fp8_scale(const float* amax, int n, float* scale, cudaStream_t stream);
 
 // Launch counter shared by every launcher.
 void count_launch();

@@ -135,6 +135,14 @@ __device__ void merge_row(const float* __restrict__ lse, size_t lse_stride,
   }
 }
 
+// A unit's (first slot, count) record names slots inside the workspace.  The
+// attention kernel writes every record before the merge runs; a record outside
+// that range can only be left over from a call whose attention kernel gave up
+// (a bounded wait ran out): its row is skipped instead of read out of range.
+__device__ __forceinline__ bool info_ok(const DecodeArgs& a, int2 info) {
+  return info.x >= 0 && info.y >= 0 && (long long)info.x + info.y <= (long long)a.slots;
+}
+
 // Balanced-stream partials: unit u = (s, hg) has `count` partials in slots
 // first .. first+count-1, each with HG*R rows (R = q_len * G); count 1 means the
 // attention kernel already wrote the output.
@@ -145,6 +153,10 @@ __global__ void __launch_bounds__(kThreads) merge_units_kernel(const DecodeArgs 
   const int u = blockIdx.x, hl = blockIdx.y;
   const int2 info = a.unit_info[u];
   if (info.y == 1) return;
+  if (!info_ok(a, info)) {
+    if (hl == 0 && threadIdx.x == 0) record_error(a.status, PKV_EBOUNDS);
+    return;
+  }
   // row hl of a unit: KV head w of the group, column r = i * G + g (query token i, head g)
   const int HGR = a.HG * a.R;
   const int s = u / a.NHG, hg = u % a.NHG;
@@ -170,6 +182,10 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) merge_units_warp_kernel(cons
   const int u = (int)(row / HGR), hl = (int)(row % HGR);
   const int2 info = a.unit_info[u];
   if (info.y == 1) return;                      // the attention kernel wrote this row
+  if (!info_ok(a, info)) {
+    if (hl == 0 && lane == 0) record_error(a.status, PKV_EBOUNDS);
+    return;
+  }
   const int s = u / a.NHG, hg = u % a.NHG;
   const int w = hl / a.R, r = hl % a.R;
   const int i = r / a.G, g = r % a.G;
@@ -289,7 +305,11 @@ __global__ void __launch_bounds__(128) merge_units_ext_kernel(const DecodeArgs a
   const int HGR = a.HG * a.R;
   const long long row = blockIdx.x;
   const int u = (int)(row / HGR), hl = (int)(row % HGR);
-  const int2 info = a.unit_info[u];
+  int2 info = a.unit_info[u];
+  if (!info_ok(a, info)) {
+    if (hl == 0 && threadIdx.x == 0) record_error(a.status, PKV_EBOUNDS);
+    info = make_int2(0, 0);                                   // the prefix partials alone
+  }
   const int s = u / a.NHG, hg = u % a.NHG;
   const int w = hl / a.R, r = hl % a.R;
   const int i = r / a.G, g = r % a.G;

@@ -477,6 +477,11 @@ int kv_absmax(const void* d_x, pkv_dtype dtype, int64_t n, float* d_amax, cudaSt
   return launch_absmax(d_x, dtype, n, d_amax, stream) == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
+int kv_fp8_scale(const float* d_amax, int n, float* d_scale, cudaStream_t stream) {
+  if (!d_amax || !d_scale || n < 1) return PKV_EINVAL;
+  return launch_fp8_scale(d_amax, n, d_scale, stream) == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
 size_t paged_decode_workspace_bytes_mq(const pkv_geometry* g, int batch, int q_len,
                                        int max_seq_len, int num_splits) {
   if (!geometry_ok(g) || batch < 0 || q_len < 1 || max_seq_len < 0 || num_splits < 0) return 0;
@@ -487,7 +492,7 @@ size_t paged_decode_workspace_bytes_mq(const pkv_geometry* g, int batch, int q_l
                          nullptr);
   for (int hg = 1; hg <= 8; ++hg) {
     if (!hg_ok(*g, hg)) continue;
-    for (int c = 1; c <= 4; ++c) {
+    for (int c = 1; c <= 8; ++c) {   // every CTAs-per-SM count plan_mma accepts
       MmaPlan p;
       p.HG = hg;
       p.NHG = g->num_kv_heads / hg;
@@ -696,6 +701,7 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
       a.part_o = reinterpret_cast<float*>(ws + w.o_off);
       a.part_lse = reinterpret_cast<float*>(ws + w.lse_off);
       a.unit_info = reinterpret_cast<int2*>(ws + w.info_off);
+      a.slots = plan.grid + batch * plan.NHG;
       if (ext) {
         a.ext_o = ext->o;
         a.ext_lse = ext->lse;

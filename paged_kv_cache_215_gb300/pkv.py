@@ -70,6 +70,7 @@ def _load() -> ctypes.CDLL:
         "kv_append": (I, [P, I, P, P, I, P, I, P, I, F, F, P]),
         "kv_append_tokens": (I, [P, I, P, P, I, P, I, I, P, P, I64, F, F, P]),
         "kv_absmax": (I, [P, I, I64, P, P]),
+        "kv_fp8_scale": (I, [P, I, P, P]),
         "kv_pool_set_block_scales": (I, [P, P]),
         "kv_block_scales": (I, [P, I, P, P, I, P, I, I, P, P, I64, P]),
         "paged_decode_workspace_bytes": (Z, [G, I, I, I]),
@@ -102,7 +103,7 @@ _lib = _load()
 EXPORTS = ("kv_pool_bytes", "kv_pool_create", "kv_pool_destroy", "kv_pool_geometry",
            "kv_pool_alloc", "kv_pool_reserve", "kv_pool_free", "kv_pool_share",
            "kv_pool_refcount", "kv_pool_num_free", "kv_pool_cow", "kv_append",
-           "kv_append_tokens", "kv_absmax", "paged_decode_workspace_bytes",
+           "kv_append_tokens", "kv_absmax", "kv_fp8_scale", "paged_decode_workspace_bytes",
            "kv_pool_set_block_scales", "kv_block_scales",
            "paged_decode_attention", "paged_decode_attention_ex", "merge_partials",
            "paged_decode_attention_static", "paged_decode_step",
@@ -268,10 +269,27 @@ def kv_absmax(x: torch.Tensor, out: torch.Tensor, stream=None):
            "kv_absmax")
 
 
-def fp8_scale(amax: float) -> float:
-    """Per-tensor E4M3 scale: amax / 448 in fp32 (amax = 0 gives 1)."""
-    import numpy as np
-    return float(np.float32(amax) / np.float32(448.0)) if amax > 0 else 1.0
+def kv_fp8_scale(amax: torch.Tensor, out: torch.Tensor, stream=None):
+    """The library's per-tensor E4M3 scale of a tensor whose pieces' kv_absmax
+    results are `amax` (float32, device), written to out[0]."""
+    _check(_lib.kv_fp8_scale(_ptr(amax), amax.numel(), _ptr(out), _stream(stream)),
+           "kv_fp8_scale")
+
+
+def fp8_scales(k_parts, v_parts, stream=None):
+    """Per-tensor E4M3 scales (k_scale, v_scale) of K and V held in pieces (for
+    example the cached tokens and the new ones): kv_absmax of every piece, then
+    kv_fp8_scale of each tensor, on the device; the two floats are read back."""
+    dev = k_parts[0].device
+    amax = torch.zeros(len(k_parts) + len(v_parts), dtype=torch.float32, device=dev)
+    for i, x in enumerate(list(k_parts) + list(v_parts)):
+        kv_absmax(x, amax[i:i + 1], stream)
+    sc = torch.empty(2, dtype=torch.float32, device=dev)
+    nk = len(k_parts)
+    kv_fp8_scale(amax[:nk], sc[0:1], stream)
+    kv_fp8_scale(amax[nk:], sc[1:2], stream)
+    k, v = sc.cpu().tolist()
+    return k, v
 
 
 def workspace_bytes(geom: Geometry, batch: int, max_seq_len: int, num_splits: int = 0) -> int:

@@ -42,14 +42,9 @@ class GpuCase:
         self.max_seq_len = int(case.seq_lens.max()) if case.batch else 0
         self.k_scale = self.v_scale = 1.0
         if case.kv_dtype == "e4m3":
-            amax = torch.zeros(4, dtype=torch.float32, device=device)
-            pkv.kv_absmax(self.k_tokens, amax[0:1])
-            pkv.kv_absmax(self.k_new, amax[1:2])
-            pkv.kv_absmax(self.v_tokens, amax[2:3])
-            pkv.kv_absmax(self.v_new, amax[3:4])
-            a = amax.cpu().numpy()
-            self.k_scale = pkv.fp8_scale(float(max(a[0], a[1])))
-            self.v_scale = pkv.fp8_scale(float(max(a[2], a[3])))
+            # the library's per-tensor scales over the cached and the new tokens
+            self.k_scale, self.v_scale = pkv.fp8_scales((self.k_tokens, self.k_new),
+                                                        (self.v_tokens, self.v_new))
         if self.tok_seq.numel():
             self.pool.append_tokens(case.layer, self.k_tokens, self.v_tokens, self.tables,
                                     self.tok_seq, self.tok_pos, self.k_scale, self.v_scale)

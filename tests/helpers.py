@@ -28,11 +28,12 @@ def oracle_pool(case, tens, k_scale=1.0, v_scale=1.0, include_new=False):
 
 
 def fp8_scales(tens):
-    """Per-tensor scales amax / 448 over all K (resp. V) tokens, amax 0 -> 1."""
+    """The oracle's per-tensor scales of all K (resp. V) tokens: its amax over the
+    cached tokens and the new ones, then its scale rule."""
     ks = []
     for a, b in ((tens.k_tokens, tens.k_new), (tens.v_tokens, tens.v_new)):
         amax = max(oracle.absmax(np_raw(a), "bf16"), oracle.absmax(np_raw(b), "bf16"))
-        ks.append(np.float32(amax) / np.float32(448.0) if amax > 0 else np.float32(1.0))
+        ks.append(oracle.fp8_scale(amax))
     return float(ks[0]), float(ks[1])
 
 

@@ -84,11 +84,48 @@ def test_append_is_bit_exact(case):
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: c.name)
 def test_fp8_scales_match_oracle(case):
+    """The library's per-tensor scales (kv_absmax of the cached and the new tokens,
+    then kv_fp8_scale) equal the oracle's absmax and scale rule bit for bit."""
     if case.kv_dtype != "e4m3":
         pytest.skip("per-tensor scales exist only for E4M3 pools")
     gc, _, _, _ = _sides(case)
     ks, vs = fp8_scales(gc.tens)
     assert (gc.k_scale, gc.v_scale) == (ks, vs)
+
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16, torch.float16])
+def test_fp8_scale_matches_oracle_on_awkward_tensors(dt):
+    """kv_absmax + kv_fp8_scale against oracle.absmax + oracle.fp8_scale, bit for
+    bit, on tensors held in three pieces with NaN, +-Inf, -0, subnormals and a
+    negative maximum planted, on magnitudes from 2^-20 to 2^20, and on all-zero
+    and all-non-finite tensors (scale 1)."""
+    from paged_kv_cache_215_gb300 import pkv
+    name = {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}[dt]
+    g = torch.Generator().manual_seed(7)
+    exps = [-20, -3, 0, 9, 20] if dt != torch.float16 else [-10, -3, 0, 4, 9]
+    for e in exps:
+        parts = [(torch.randn(n, generator=g) * 2.0 ** e).to(dt) for n in (4097, 1, 333)]
+        parts[0][5] = float("nan")
+        parts[0][6] = float("inf")
+        parts[2][7] = float("-inf")
+        parts[2][8] = -0.0
+        parts[2][9] = torch.finfo(dt).tiny / 4
+        parts[1][0] = -float(parts[0].float().nan_to_num(0, 0, 0).abs().max()) * 1.5
+        amax = torch.zeros(3, dtype=torch.float32, device="cuda")
+        for i, x in enumerate(parts):
+            pkv.kv_absmax(x.cuda(), amax[i:i + 1])
+        sc = torch.zeros(1, dtype=torch.float32, device="cuda")
+        pkv.kv_fp8_scale(amax, sc)
+        want_amax = max(oracle.absmax(np_raw(x), name) for x in parts)
+        assert amax.cpu().tolist() == [oracle.absmax(np_raw(x), name) for x in parts]
+        assert float(sc.item()) == oracle.fp8_scale(want_amax), (e, float(sc.item()))
+    for x in (torch.zeros(100, dtype=dt),
+              torch.tensor([float("nan"), float("inf"), -float("inf")] * 10).to(dt)):
+        amax = torch.zeros(1, dtype=torch.float32, device="cuda")
+        pkv.kv_absmax(x.cuda(), amax)
+        sc = torch.zeros(1, dtype=torch.float32, device="cuda")
+        pkv.kv_fp8_scale(amax, sc)
+        assert float(amax.item()) == 0.0 and float(sc.item()) == 1.0
 
 
 @pytest.mark.parametrize("splits", [0, 1, 3])
@@ -279,6 +316,7 @@ def test_absmax_matches_oracle(dt):
     from paged_kv_cache_215_gb300 import pkv
     x = (torch.randn(1 << 20, generator=torch.Generator().manual_seed(3)) * 7).to(dt)
     x[12345] = float("nan")
+    x[2345] = float("inf")
     out = torch.zeros(1, dtype=torch.float32, device="cuda")
     pkv.kv_absmax(x.cuda(), out)
     name = {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}[dt]

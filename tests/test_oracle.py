@@ -116,6 +116,70 @@ def test_e4m3_encode_special_cases():
     assert enc(896.0, 2.0) == 0x7E          # x / scale = 448
 
 
+# --------------------------------------------------------------------------- per-tensor scale
+def _specials_array(dt, seed):
+    """Random values of a dtype with the awkward ones planted: NaN, +-Inf, -0,
+    subnormals of the dtype, and a largest magnitude that is negative."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(4099, generator=g, dtype=torch.float32) * 3.0
+    x = x.to(dt)
+    tiny = torch.finfo(dt).tiny                   # smallest normal: halve it for a subnormal
+    plant = [float("nan"), float("inf"), float("-inf"), -0.0, tiny / 2, -tiny / 4, -37.25]
+    for i, v in enumerate(plant):
+        x[97 * (i + 1)] = v
+    return x
+
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.float16, torch.bfloat16])
+def test_absmax_is_the_largest_finite_magnitude(dt):
+    """The per-tensor FP8 scale starts from the tensor's absolute maximum
+    ("Unlocking long context" section 3.2).  Checked against numpy on the values
+    torch decodes: NaN and +-Inf are left out, -0 and subnormals are ordinary
+    values, and a negative element can hold the maximum magnitude."""
+    name = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}[dt]
+    x = _specials_array(dt, seed=41)
+    vals = x.to(torch.float64).numpy()
+    want = float(np.abs(vals[np.isfinite(vals)]).max())
+    assert want == 37.25                          # the planted negative maximum
+    assert oracle.absmax(np_raw(x), name) == want
+    # only non-finite values, only zeros, and the empty tensor: 0
+    bad = torch.tensor([float("nan"), float("inf"), float("-inf")], dtype=torch.float32).to(dt)
+    assert oracle.absmax(np_raw(bad), name) == 0.0
+    assert oracle.absmax(np_raw(torch.tensor([0.0, -0.0]).to(dt)), name) == 0.0
+    assert oracle.absmax(np_raw(torch.zeros(0, dtype=dt)), name) == 0.0
+    # a lone subnormal is the maximum
+    sub = torch.tensor([0.0, torch.finfo(dt).tiny / 8]).to(dt)
+    assert oracle.absmax(np_raw(sub), name) == float(sub[1].double())
+
+
+def test_fp8_scale_closed_forms():
+    """scale = amax / 448 in fp32 ("Unlocking long context" section 3.2; 448 is the
+    largest finite E4M3 value): exact values where the quotient is a power of
+    two, exact scaling by powers of two, and 1 for an all-zero tensor."""
+    assert oracle.fp8_scale(0.0) == 1.0
+    assert oracle.fp8_scale(448.0) == 1.0
+    assert oracle.fp8_scale(896.0) == 2.0
+    assert oracle.fp8_scale(3.5) == 2.0 ** -7
+    assert oracle.fp8_scale(7.0 * 2.0 ** -20) == 2.0 ** -26
+    for k in range(-30, 31):
+        assert oracle.fp8_scale(37.25 * 2.0 ** k) == oracle.fp8_scale(37.25) * 2.0 ** k
+
+
+def test_fp8_scale_stores_the_largest_value_as_448():
+    """With the scale, the tensor's largest magnitude encodes to the largest E4M3
+    code (0x7E, or 0xFE for a negative value) and nothing saturates beyond it;
+    the scale is the correctly rounded quotient (within half an fp32 ulp)."""
+    rng = np.random.default_rng(5)
+    amax = np.concatenate([rng.lognormal(0.0, 6.0, 2000), [1e-30, 3e-5, 65504.0, 3e38]])
+    amax = amax.astype(np.float32)
+    for a in amax:
+        sc = oracle.fp8_scale(float(a))
+        assert int(oracle.e4m3_encode(np.array([a], np.float32), sc)[0]) == 0x7E
+        assert int(oracle.e4m3_encode(np.array([-a], np.float32), sc)[0]) == 0xFE
+        exact = float(a) / 448.0
+        assert abs(sc - exact) <= 0.5 * np.spacing(np.float32(exact)) * (1 + 1e-12)
+
+
 # --------------------------------------------------------------------------- attention
 def _naive(q, K, V, scale):
     """Library naive attention on unpaged arrays: softmax(q K^T * scale) V, the
