@@ -201,7 +201,9 @@ PKV_API size_t paged_decode_workspace_bytes(const pkv_geometry* geom, int batch,
  *   s_j = scale * <q[s,h,:], K_s[j,:]>,  w = softmax(s),  out[s,h,:] = sum_j w_j V_s[j,:]
  * where token j of sequence s is read from pool[table[s][j / bs], *, layer, kv, j % bs, :]
  * and E4M3 elements are dequantised as value x k_scale (K) or x v_scale (V).
- * A sequence with n = 0 gets out = 0.
+ * A sequence with n = 0 gets out = 0.  On E4M3 pools bf16 / f16 q run on f16
+ * tensor-core operands after an exact power-of-two prescale; f32 q runs on the
+ * fp32 CUDA-core kernel.
  * The key range of each sequence is cut into partitions whose partial results
  * are merged by log-sum-exp ([SEQPAR] incremental softmax, [ENG26] 3.1):
  *   num_splits = 0: automatic.  The token stream of all sequences is cut into
@@ -284,10 +286,14 @@ PKV_API int paged_decode_step(void* d_out, pkv_dtype out_dtype, const void* d_q,
  * (<= 8 at block_size 64); larger chunks run on the tcgen05 kernel: UMMA tiles
  * of 128 query rows x 64 keys with S and O in tensor memory (num_splits must be
  * 0 there), head_dim 128, num_q_heads / num_kv_heads dividing 128.  bf16 / f16
- * pools take q in the pool's dtype; E4M3 pools take bf16 or f16 q, and each
- * E4M3 tile is converted to f16 in shared memory (exactly with per-tensor
- * scales; times its block's scales, rounded to f16, with per-block ones), q
- * rounded to f16.  Other combinations return PKV_EUNSUPPORTED.  Other arguments and errors as in
+ * pools take q in the pool's dtype; E4M3 pools take bf16 or f16 q (f32 q only
+ * for q_len = 1, on the fp32 CUDA-core kernel).  E4M3 tiles become f16 operands
+ * (exactly with per-tensor scales; with per-block ones each value times its
+ * block's scale over the largest power of two among the blocks read, rounded to
+ * f16), and q is multiplied by a power of two that puts its largest magnitude
+ * just below f16's maximum before it is rounded to f16 (exact for bf16 and f16
+ * values), so any finite q and any positive scales stay in range.  Other
+ * combinations return PKV_EUNSUPPORTED.  Other arguments and errors as in
  * paged_decode_attention_ex; the workspace is paged_decode_workspace_bytes_mq. */
 PKV_API int paged_decode_attention_mq(void* d_out, pkv_dtype out_dtype, const void* d_q,
                                       pkv_dtype q_dtype, int q_len, const pkv_pool* pool,

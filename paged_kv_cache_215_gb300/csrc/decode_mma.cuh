@@ -132,11 +132,21 @@ struct Consumer {
   using T = KvTraits<KVT>;
   static constexpr int kTiles = BS / 16;
   static constexpr bool kSplitP = T::kBf16Mma;   // bf16 P is split into hi + lo parts
+  // f16 P (f16 and E4M3 pools) is computed as 2^(s - m + kPOff): the largest
+  // weight of a block is 2^kPOff instead of 1, so weights down to 2^-28 of the
+  // running maximum stay normal f16 numbers (a long tail of small weights would
+  // otherwise round in f16's subnormal range); the factor cancels in O / l.
+  static constexpr float kPOff = kSplitP ? 0.f : 14.f;
 
   uint32_t qf[NT][8][2];   // B fragments of the query rows (8 k-steps of 16)
   float acc[8][NT][4];     // O^T fragments: 8 tiles of 16 d x 8 rows, per n-tile
   float m[NT][2], l[NT][2];// running max (log2 units) and per-thread partial sums
   int lim[NT][2];          // last key position each of the thread's columns may see
+  // E4M3 with block-wise scales: acc is held in units of 2^ev_ref_, the largest
+  // power-of-two exponent of the V block scales seen in the current piece, and
+  // each block's P carries its scale's remaining factor (at most 2), so that
+  // P x scale never leaves f16's range whatever the scales' magnitudes.
+  int ev_ref_;
 
   __device__ __forceinline__ void reset() {
 #pragma unroll
@@ -150,7 +160,24 @@ struct Consumer {
       m[nt][0] = m[nt][1] = -INFINITY;
       l[nt][0] = l[nt][1] = 0.f;
     }
+    ev_ref_ = -100000;
   }
+
+  // Block-wise E4M3 scales: split vs_b = mant x 2^ev (mant in [1, 2)); a block
+  // whose exponent exceeds the piece's reference raises it, and acc (in units of
+  // the old reference) is rescaled by 2^(old - new) through *acc_f.  Returns the
+  // factor P carries for this block: mant x 2^(ev - reference) <= 2.
+  __device__ __forceinline__ float v_block_factor(float vs_b, float* acc_f) {
+    int ev;
+    const float mant = 2.f * frexpf(vs_b, &ev);
+    --ev;
+    if (ev > ev_ref_) {
+      *acc_f = ldexpf(1.f, max(ev_ref_ - ev, -300));   // 0 for the piece's first block
+      ev_ref_ = ev;
+    }
+    return ldexpf(mant, max(ev - ev_ref_, -300));
+  }
+
 
   // q row of column r (query token r / G, head r % G of this KV head), -1 if padding.
   __device__ __forceinline__ static long long q_row(const DecodeArgs& a, int s, int hkv, int r) {
@@ -165,6 +192,26 @@ struct Consumer {
       return;
     }
     const int c = lane & 3;
+    float qscale = 1.f;
+    if constexpr (T::kFp8) {
+      // E4M3 pools run f16 MMAs: q x 2^e with the warp's largest |q| over all its
+      // rows setting e (f16_fit_exponent), and 2^-e folded into the softmax scale
+      float amax = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const long long qr = q_row(a, s, hkv, nt * 8 + (lane >> 2));
+        if (qr < 0) continue;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            amax = fmaxf(amax, fabsf(load_as_float(a.q, (size_t)qr * kD + 16 * kk + 4 * c + i,
+                                                   a.q_dtype)));
+      }
+      const int e = f16_fit_exponent(warp_max(amax));
+      qscale = pow2i(e);
+      qk_scale_log2_ = a.qk_scale_log2 * pow2i(-e);
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const long long qr = q_row(a, s, hkv, nt * 8 + (lane >> 2));
@@ -179,8 +226,8 @@ struct Consumer {
           float x1 = live ? load_as_float(a.q, row + d + 1, a.q_dtype) : 0.f;
           float x2 = live ? load_as_float(a.q, row + d + 2, a.q_dtype) : 0.f;
           float x3 = live ? load_as_float(a.q, row + d + 3, a.q_dtype) : 0.f;
-          qf[nt][kk][0] = pack_f16(x0, x1);
-          qf[nt][kk][1] = pack_f16(x2, x3);
+          qf[nt][kk][0] = pack_f16(x0 * qscale, x1 * qscale);
+          qf[nt][kk][1] = pack_f16(x2 * qscale, x3 * qscale);
         } else {
           const uint32_t* qp = reinterpret_cast<const uint32_t*>(
               static_cast<const uint16_t*>(a.q) + row + 16 * kk + 2 * c);
@@ -263,33 +310,37 @@ struct Consumer {
     const float al0 = exp2f(m[0][0] - mn0), al1 = exp2f(m[0][1] - mn1);
     m[0][0] = mn0;
     m[0][1] = mn1;
+    const float ref0 = mn0 - kPOff, ref1 = mn1 - kPOff;
     float p[kTiles][4];
     float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
     for (int mt = 0; mt < kTiles; ++mt) {
-      p[mt][0] = exp2f(s[mt][0] - mn0);
-      p[mt][1] = exp2f(s[mt][1] - mn1);
-      p[mt][2] = exp2f(s[mt][2] - mn0);
-      p[mt][3] = exp2f(s[mt][3] - mn1);
+      p[mt][0] = exp2f(s[mt][0] - ref0);
+      p[mt][1] = exp2f(s[mt][1] - ref1);
+      p[mt][2] = exp2f(s[mt][2] - ref0);
+      p[mt][3] = exp2f(s[mt][3] - ref1);
       ps0 += p[mt][0] + p[mt][2];
       ps1 += p[mt][1] + p[mt][3];
     }
     l[0][0] = l[0][0] * al0 + ps0;
     l[0][1] = l[0][1] * al1 + ps1;
+    // E4M3 block-wise scales: the block's V scale rides on P (the row sums l keep
+    // unscaled p), split so that P stays in f16's range
+    float pv = 1.f, acc_f = 1.f;
+    if (T::kFp8 && bscaled_) pv = v_block_factor(vs_b, &acc_f);
+    const float a0 = al0 * acc_f, a1 = al1 * acc_f;
 #pragma unroll
     for (int dt = 0; dt < 8; ++dt) {
-      acc[dt][0][0] *= al0;
-      acc[dt][0][1] *= al1;
-      acc[dt][0][2] *= al0;
-      acc[dt][0][3] *= al1;
+      acc[dt][0][0] *= a0;
+      acc[dt][0][1] *= a1;
+      acc[dt][0][2] *= a0;
+      acc[dt][0][3] *= a1;
     }
 
     // ---- P^T as B operand: movmatrix transposes the 8x8 (token, head) quadrants
     uint32_t bh[kTiles][2], bl[kTiles][2];
 #pragma unroll
     for (int mt = 0; mt < kTiles; ++mt) {
-      // E4M3: the block's V scale rides on P (the row sums l keep unscaled p)
-      const float pv = T::kFp8 ? vs_b : 1.f;
       const uint32_t x0 = pack2<T::kBf16Mma>(p[mt][0] * pv, p[mt][1] * pv);
       const uint32_t x1 = pack2<T::kBf16Mma>(p[mt][2] * pv, p[mt][3] * pv);
       bh[mt][0] = movmatrix_t(x0);
@@ -370,18 +421,30 @@ struct Consumer {
     const int g = lane >> 2, c = lane & 3;
     const bool live = g < a.G;
     const size_t row = ((size_t)s * a.Hq + (size_t)hkv * a.G + (live ? g : 0)) * kD;
+    if constexpr (T::kFp8) {
+      // q x 2^e in f16 (f16_fit_exponent over the warp's q), 2^-e on the softmax
+      // scale; k-slot permutation matching the E4M3 A fragment: thread c holds
+      // d = 16kk + 4c .. 4c+3
+      float x[8][4];
+      float amax = 0.f;
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      if constexpr (T::kFp8) {
-        // k-slot permutation matching the E4M3 A fragment: thread c holds d = 16kk + 4c .. 4c+3
-        const int d = 16 * kk + 4 * c;
-        float x0 = live ? load_as_float(a.q, row + d + 0, a.q_dtype) : 0.f;
-        float x1 = live ? load_as_float(a.q, row + d + 1, a.q_dtype) : 0.f;
-        float x2 = live ? load_as_float(a.q, row + d + 2, a.q_dtype) : 0.f;
-        float x3 = live ? load_as_float(a.q, row + d + 3, a.q_dtype) : 0.f;
-        qf[0][kk][0] = pack_f16(x0, x1);
-        qf[0][kk][1] = pack_f16(x2, x3);
-      } else {
+      for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          x[kk][i] = live ? load_as_float(a.q, row + 16 * kk + 4 * c + i, a.q_dtype) : 0.f;
+          amax = fmaxf(amax, fabsf(x[kk][i]));
+        }
+      const int e = f16_fit_exponent(warp_max(amax));
+      const float qscale = pow2i(e);
+      qk_scale_log2_ = a.qk_scale_log2 * pow2i(-e);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        qf[0][kk][0] = pack_f16(x[kk][0] * qscale, x[kk][1] * qscale);
+        qf[0][kk][1] = pack_f16(x[kk][2] * qscale, x[kk][3] * qscale);
+      }
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
         const uint32_t* qp = reinterpret_cast<const uint32_t*>(
             static_cast<const uint16_t*>(a.q) + row + 16 * kk + 2 * c);
         qf[0][kk][0] = live ? __ldg(qp) : 0u;
@@ -400,7 +463,11 @@ struct Consumer {
       L1 += __shfl_xor_sync(0xffffffffu, L1, o);
     }
     const int c = lane & 3;
-    const float inv0 = a.v_scale / L0, inv1 = a.v_scale / L1;
+    float inv0 = a.v_scale / L0, inv1 = a.v_scale / L1;
+    if (T::kFp8 && bscaled_) {
+      inv0 = ldexpf(inv0, ev_ref_);
+      inv1 = ldexpf(inv1, ev_ref_);
+    }
     const int g0 = 2 * c, g1 = 2 * c + 1;
     if (whole) {
       const size_t ob = ((size_t)s * a.Hq + (size_t)hkv * a.G) * kD;
@@ -424,8 +491,8 @@ struct Consumer {
                 acc[dt][0][k] * ((k & 1) ? inv1 : inv0);
         }
       if ((lane >> 2) == 0) {
-        if (g0 < a.G) a.part_lse[part_row_base + (size_t)g0 * part_row_stride] = (m[0][0] + __log2f(L0)) * kLn2;
-        if (g1 < a.G) a.part_lse[part_row_base + (size_t)g1 * part_row_stride] = (m[0][1] + __log2f(L1)) * kLn2;
+        if (g0 < a.G) a.part_lse[part_row_base + (size_t)g0 * part_row_stride] = (m[0][0] + __log2f(L0) - kPOff) * kLn2;
+        if (g1 < a.G) a.part_lse[part_row_base + (size_t)g1 * part_row_stride] = (m[0][1] + __log2f(L1) - kPOff) * kLn2;
       }
     }
     reset();
@@ -535,6 +602,10 @@ struct Consumer {
         mx[nt][1] = fmaxf(mx[nt][1], __shfl_xor_sync(0xffffffffu, mx[nt][1], o));
       }
     float p[kTiles][NT][4];
+    // E4M3 block-wise scales: the block's V scale rides on P, split so that P
+    // stays in f16's range (see v_block_factor)
+    float pv = 1.f, acc_f = 1.f;
+    if (T::kFp8 && bscaled_) pv = v_block_factor(vs_b, &acc_f);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -546,18 +617,20 @@ struct Consumer {
         if constexpr (kCausal) ref = mn == -INFINITY ? 0.f : mn;
         const float al = exp2f(m[nt][h] - ref);
         m[nt][h] = mn;
+        const float pref = ref - kPOff;
         float ps = 0.f;
 #pragma unroll
         for (int mt = 0; mt < kTiles; ++mt) {
-          p[mt][nt][h] = exp2f(s[mt][nt][h] - ref);
-          p[mt][nt][h + 2] = exp2f(s[mt][nt][h + 2] - ref);
+          p[mt][nt][h] = exp2f(s[mt][nt][h] - pref);
+          p[mt][nt][h + 2] = exp2f(s[mt][nt][h + 2] - pref);
           ps += p[mt][nt][h] + p[mt][nt][h + 2];
         }
         l[nt][h] = l[nt][h] * al + ps;
+        const float alv = al * acc_f;
 #pragma unroll
         for (int dt = 0; dt < 8; ++dt) {
-          acc[dt][nt][h] *= al;
-          acc[dt][nt][h + 2] *= al;
+          acc[dt][nt][h] *= alv;
+          acc[dt][nt][h + 2] *= alv;
         }
       }
     }
@@ -568,7 +641,6 @@ struct Consumer {
     for (int mt = 0; mt < kTiles; ++mt)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const float pv = T::kFp8 ? vs_b : 1.f;   // E4M3: the block's V scale rides on P
         const uint32_t x0 = pack2<T::kBf16Mma>(p[mt][nt][0] * pv, p[mt][nt][1] * pv);
         const uint32_t x1 = pack2<T::kBf16Mma>(p[mt][nt][2] * pv, p[mt][nt][3] * pv);
         bh[mt][nt][0] = movmatrix_t(x0);
@@ -683,7 +755,8 @@ struct Consumer {
         if (qr < 0) continue;
         // a column that saw no key (a query before the sequence start) is empty
         const bool empty = m[nt][h] == -INFINITY;
-        const float inv = empty ? 0.f : a.v_scale / L[h];
+        float inv = empty ? 0.f : a.v_scale / L[h];
+        if (T::kFp8 && bscaled_) inv = ldexpf(inv, ev_ref_);
         const size_t prow = balanced ? part_base + (size_t)r : part_base + (size_t)qr * a.S;
 #pragma unroll
         for (int dt = 0; dt < 8; ++dt)
@@ -695,13 +768,14 @@ struct Consumer {
             else a.part_o[prow * kD + d] = v;
           }
         if (!whole && (lane >> 2) == 0)
-          a.part_lse[prow] = empty ? -INFINITY : (m[nt][h] + __log2f(L[h])) * kLn2;
+          a.part_lse[prow] = empty ? -INFINITY : (m[nt][h] + __log2f(L[h]) - kPOff) * kLn2;
       }
     }
     reset();
   }
 
   float qk_scale_log2_;
+  bool bscaled_;           // E4M3 pool with block-wise scales attached
 };
 
 // First partial row of a piece: balanced mode rows are slot * HG*R + w*R + column;
@@ -934,6 +1008,7 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
   // ---------------------------------------------------------------- consumers
   Consumer<KVT, BS, NT, kCausal> cons;
   cons.qk_scale_log2_ = a.qk_scale_log2;
+  cons.bscaled_ = T::kFp8 && a.block_scales != nullptr;
   cons.reset();
   const int w = warp;
   bool waited = false;

@@ -399,6 +399,18 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// q of an E4M3 pool feeds f16 tensor-core operands.  2^e with e from this
+// function puts a set of values whose largest magnitude is amax into
+// [2^14, 2^15): scaled by it, bf16 and f16 values keep every bit (down to 2^-32
+// of amax) and none overflows f16; 2^-e then rides on the softmax scale.
+// amax = 0 or non-finite gives 0.
+__device__ __forceinline__ int f16_fit_exponent(float amax) {
+  if (!(amax > 0.f) || !isfinite(amax)) return 0;
+  return min(14 - ilogbf(amax), 120);
+}
+// 2^e for e in [-126, 127] (a normal fp32 number, built from its exponent field).
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) << 23); }
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

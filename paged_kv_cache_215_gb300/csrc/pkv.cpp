@@ -561,7 +561,10 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
   if (!device_info(&dev)) return PKV_ECUDA;
 
   const int G = g.num_q_heads / g.num_kv_heads;
-  const bool q_ok_mma = fp8 ? true
+  // the tensor-core kernel runs f16 MMAs on E4M3 pools: bf16 and f16 q fit them
+  // exactly after a power-of-two prescale, f32 q would be rounded, so it goes to
+  // the CUDA-core kernel (fp32) instead
+  const bool q_ok_mma = fp8 ? (q_dtype == PKV_BF16 || q_dtype == PKV_F16)
                             : (g.kv_dtype == PKV_BF16 ? q_dtype == PKV_BF16 : q_dtype == PKV_F16);
   const bool mma_ok = mma_supported(g.kv_dtype, g.block_size, g.head_dim, G, q_len) && q_ok_mma;
   const bool simt_ok = g.head_dim % 32 == 0 && g.head_dim <= 256 && G <= 16 && q_len == 1;

@@ -86,6 +86,8 @@ struct Bars {
   uint64_t s_full[kQT][2], p_full[kQT][2], p_free[kQT][2], o_done[kQT];
   uint64_t o_final[kQT];                      // query tile t's last P V has completed
   uint64_t v_zeroed;                          // the tail tile's V rows past the end are zero
+  uint64_t eref_ready;                        // E4M3 per-block scales: the reference exponent is in
+  int eref[4];                                // per converter warp: largest exponent of the V scales
   uint32_t tmem;
   volatile int abort_flag;
 };
@@ -147,6 +149,11 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
   constexpr bool kBf16 = C::kBf16, kFp8 = C::kFp8;
   constexpr int kStages = C::kStages;
   constexpr bool kSplitP = kBf16;            // f16 P (11 bits) needs no low term
+  // f16 P is 2^(s - ref + kPOff) <= 2^15: weights down to 2^-21 of the row's
+  // reference stay normal f16 numbers (a long tail of small weights would
+  // otherwise round in f16's subnormal range); the factor cancels in O / l.
+  // bf16 P has fp32's exponent range and needs none.
+  constexpr float kPOff = kSplitP ? 0.f : 7.f;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -201,6 +208,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
       mbar_init(&bars->o_final[t], 1);
     }
     mbar_init(&bars->v_zeroed, 1);
+    mbar_init(&bars->eref_ready, kFp8 ? C::kConvWarps : 1);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -208,7 +216,11 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
     tmem_alloc(&bars->tmem, kTmemCols);
     tmem_relinquish();
   }
-  // Q tiles: thread (t, r) stages row r = (token t0 + r / G, head hkv*G + r % G), swizzled
+  // Q tiles: thread (t, r) stages row r = (token t0 + r / G, head hkv*G + r % G), swizzled.
+  // E4M3 pools run f16 MMAs: a bf16 q row is scaled by 2^q_e (f16_fit_exponent of
+  // its largest |q|) before the f16 rounding, exactly, and the same thread's
+  // softmax takes 2^-q_e onto the scale.
+  int q_e = 0;
   if (warp < kSoftmaxWarps) {
     const int t = warp / 4, r = tid - 128 * t, i = r / G, g = r % G;
     const int tok = (blockIdx.x * kQT + t) * QT + i;
@@ -220,16 +232,33 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
     // a negative softmax scale is moved onto Q (an exact sign flip), so that the
     // softmax may take its row max over the unscaled scores
     const uint32_t flip = a.qk_scale_log2 < 0.f ? 0x80008000u : 0u;
+    const bool to_f16 = kFp8 && a.q_dtype == PKV_BF16;
+    float qscale = 1.f;
+    if (to_f16 && live) {
+      float amax = 0.f;
+#pragma unroll 4
+      for (int c = 0; c < 16; ++c) {
+        uint4 v = __ldg(src + c);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = unpack2<true>(w[e]);
+          amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+      }
+      q_e = f16_fit_exponent(amax);
+      qscale = pow2i(q_e);
+    }
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       uint4 v = live ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-      if (kFp8 && a.q_dtype == PKV_BF16) {
-        // the MMAs of an E4M3 pool run on f16 operands: q bf16 -> f16
+      if (to_f16) {
+        // the MMAs of an E4M3 pool run on f16 operands: q bf16 x 2^q_e -> f16
         uint32_t* w = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 f = unpack2<true>(w[e]);
-          w[e] = pack_f16(f.x, f.y);
+          w[e] = pack_f16(f.x * qscale, f.y * qscale);
         }
       }
       v.x ^= flip;
@@ -393,12 +422,13 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
         const int32_t* trow = a.tables + (size_t)s * a.max_blocks;
         const int up = (lane >> 2) & 1, ch = 4 * up + (lane & 3);   // f16 half, source chunk
         const int rsub = 2 * (lane >> 4) + (up ^ ((lane >> 3) & 1));  // row within the group
-        // 16 E4M3 values d = 16ch .. 16ch+15 -> f16 (times a per-block scale)
-        auto convert = [&](const uint4 x, float sc, uint32_t (&o)[8]) {
+        // 16 E4M3 values d = 16ch .. 16ch+15 -> f16 (V with per-block scales:
+        // times the block's scale over 2^EV)
+        auto convert = [&](const uint4 x, float sc, bool scaled, uint32_t (&o)[8]) {
           const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) e4m3x4_to_f16x2x2(xw[e], o[2 * e], o[2 * e + 1]);
-          if (a.block_scales) {
+          if (scaled) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const float2 f = unpack2<false>(o[e]);
@@ -412,6 +442,34 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
           *reinterpret_cast<uint4*>(half + sw128(row, 2 * (ch & 3))) = make_uint4(o[0], o[1], o[2], o[3]);
           *reinterpret_cast<uint4*>(half + sw128(row, 2 * (ch & 3) + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
         };
+        // Per-block scales.  K stays exact (E4M3 -> f16); its block scales
+        // multiply the scores in fp32 in the softmax.  V's scales are applied here,
+        // each divided by 2^EV, the largest power-of-two exponent among the V
+        // scales of the CTA's blocks, so the f16 values stay below 2 x 448 whatever
+        // the scales' magnitudes; 2^EV rides on the output.  The three converter
+        // warps find EV over the CTA's blocks first.
+        int ev_ref = 0;
+        if (a.block_scales) {
+          const int bpt = kN / a.BS;
+          const int b1 = min((jt0 + T) * bpt, nblk);
+          int ev = -100000;
+          for (int b = jt0 * bpt + c * 32 + lane; b < b1; b += W * 32) {
+            int blk = __ldg(trow + b);
+            blk = (blk < 0 || blk >= a.num_blocks) ? 0 : blk;
+            const float vs =
+                __ldg(a.block_scales + ((size_t)(blk * 2 + 1) * a.L + a.layer) * a.Hkv + hkv);
+            if (vs > 0.f && isfinite(vs)) ev = max(ev, ilogbf(vs));
+          }
+          ev = __reduce_max_sync(0xffffffffu, ev);
+          if (leader) {
+            bars->eref[c] = ev;
+            mbar_arrive(&bars->eref_ready);
+          }
+          ok = wait(&bars->eref_ready, 0);
+          ev = -100000;
+          for (int w = 0; w < W; ++w) ev = max(ev, bars->eref[w]);
+          ev_ref = ev == -100000 ? 0 : ev;
+        }
         for (int j = 0; j < T && ok; ++j) {
           const int st = j % kStages;
           ok = wait(&bars->s8_full[st], (j / kStages) & 1);
@@ -431,24 +489,25 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
               xk1 = *reinterpret_cast<const uint4*>(src + sw128(row1, ch));
               xv1 = *reinterpret_cast<const uint4*>(src + kKVHalf + sw128(row1, ch));
             }
-            // per-block scales: those of the row's block (per-tensor: applied elsewhere)
-            float sk[2] = {1.f, 1.f}, sv[2] = {1.f, 1.f};
-            if (a.block_scales) {
+            // per-block V scales: those of the row's block (per-tensor: applied elsewhere)
+            const bool scaled = a.block_scales != nullptr;
+            float sv[2] = {1.f, 1.f};
+            if (scaled) {
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
                 const int jb = min((jt0 + j) * (kN / a.BS) + (row0 + 4 * h) / a.BS, nblk - 1);
                 int blk = __ldg(trow + jb);
                 blk = (blk < 0 || blk >= a.num_blocks) ? 0 : blk;
-                const size_t k0 = ((size_t)blk * 2 * a.L + a.layer) * a.Hkv + hkv;
-                sk[h] = __ldg(a.block_scales + k0);
-                sv[h] = __ldg(a.block_scales + k0 + (size_t)a.L * a.Hkv);
+                sv[h] = ldexpf(
+                    __ldg(a.block_scales + ((size_t)(blk * 2 + 1) * a.L + a.layer) * a.Hkv + hkv),
+                    -ev_ref);
               }
             }
             __syncwarp();                                       // the step's E4M3 bytes are read
             uint32_t o[8];
-            convert(xk0, sk[0], o);
+            convert(xk0, 1.f, false, o);
             store(dst, 0, row0, o);
-            convert(xv0, sv[0], o);
+            convert(xv0, sv[0], scaled, o);
             if (row0 >= valid) {
               // keys past the sequence end: zero V, so that P = 0 never meets NaN
 #pragma unroll
@@ -456,9 +515,9 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
             }
             store(dst, 1, row0, o);
             if (two) {
-              convert(xk1, sk[1], o);
+              convert(xk1, 1.f, false, o);
               store(dst, 0, row1, o);
-              convert(xv1, sv[1], o);
+              convert(xv1, sv[1], scaled, o);
               if (row1 >= valid) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o[e] = 0u;
@@ -538,7 +597,8 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
     // this query's last visible key: causal within the chunk, or its prefix length
     const int pos = casc ? (live ? __ldg(a.key_limit + tok) : 0) - 1 : n - a.q_len + tok;
     const int my_tiles = tiles[t];
-    const float qs = fabsf(a.qk_scale_log2);                  // Q carries the sign
+    // Q carries the sign; 2^-q_e undoes the row's f16 prescale (E4M3 pools)
+    float qs = fabsf(a.qk_scale_log2) * pow2i(-q_e);
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tcol = tmem + lane_base + t * 256;
     float mref = -INFINITY, lsum = 0.f;
@@ -548,8 +608,31 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
       const bool got = mbar_wait_bounded(bar, parity);
       return __all_sync(0xffffffffu, got) && !bars->abort_flag;
     };
-    for (int j = 0; j < my_tiles; ++j) {
+    // E4M3 per-block scales: each 16-key group's scores take their block's K
+    // scale in fp32 (qsb), and the V tiles were divided by 2^EV
+    const bool bscaled = kFp8 && a.block_scales != nullptr;
+    int ev_ref = 0;
+    if (bscaled && my_tiles > 0) {
+      ok = wait(&bars->eref_ready, 0);
+      int ev = -100000;
+      for (int w = 0; w < C::kConvWarps; ++w) ev = max(ev, bars->eref[w]);
+      if (ev != -100000) ev_ref = ev;
+    }
+    const int32_t* trow = a.tables + (size_t)s * a.max_blocks;
+    const int nblk = (n + a.BS - 1) / a.BS;
+    for (int j = 0; j < my_tiles && ok; ++j) {
       const int b = j & 1;
+      const int kpos0 = (jt0 + j) * kN;
+      float qsb[4] = {qs, qs, qs, qs};
+      if (bscaled) {
+        // issued before the wait for S, so the loads overlap it
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) {
+          int blk = __ldg(trow + min((kpos0 + 16 * g4) / a.BS, nblk - 1));
+          blk = (blk < 0 || blk >= a.num_blocks) ? 0 : blk;
+          qsb[g4] = qs * __ldg(a.block_scales + ((size_t)blk * 2 * a.L + a.layer) * a.Hkv + hkv);
+        }
+      }
       if (!wait(&bars->s_full[t][b], (j >> 1) & 1)) {
         ok = false;
         break;
@@ -557,26 +640,30 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
       tc_fence_after();
       float sv[kN];
       tmem_ld64_sync(tcol + b * kN, sv);
-      // causal mask and row max (8 partial maxima: short dependency chains),
-      // over the raw scores: the scale is positive, so it commutes
-      const int kpos0 = (jt0 + j) * kN;
+      // causal mask and row max over the raw scores (8 partial maxima, two per
+      // 16-key group: short dependency chains); the scales are positive, so each
+      // group's scale commutes with its max
       float mp[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) mp[e] = -INFINITY;
       if (__all_sync(0xffffffffu, live && kpos0 + kN - 1 <= pos)) {
         // the warp's rows see every key of the tile: no mask
 #pragma unroll
-        for (int c = 0; c < kN; c += 2) mp[(c >> 1) & 7] = fmax3(mp[(c >> 1) & 7], sv[c], sv[c + 1]);
+        for (int c = 0; c < kN; c += 2) {
+          const int e = 2 * (c >> 4) + ((c >> 1) & 1);
+          mp[e] = fmax3(mp[e], sv[c], sv[c + 1]);
+        }
       } else {
 #pragma unroll
         for (int c = 0; c < kN; c += 2) {
+          const int e = 2 * (c >> 4) + ((c >> 1) & 1);
           sv[c] = live && kpos0 + c <= pos ? sv[c] : -INFINITY;
           sv[c + 1] = live && kpos0 + c + 1 <= pos ? sv[c + 1] : -INFINITY;
-          mp[(c >> 1) & 7] = fmax3(mp[(c >> 1) & 7], sv[c], sv[c + 1]);
+          mp[e] = fmax3(mp[e], sv[c], sv[c + 1]);
         }
       }
-      const float mx = qs * fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                                  fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+      const float mx = fmaxf(fmaxf(qsb[0] * fmaxf(mp[0], mp[1]), qsb[1] * fmaxf(mp[2], mp[3])),
+                             fmaxf(qsb[2] * fmaxf(mp[4], mp[5]), qsb[3] * fmaxf(mp[6], mp[7])));
       bool rescale = false;
       float alpha = 1.f;
       if (mx > mref + 8.f) {            // also the first visible key (mref = -inf)
@@ -612,9 +699,10 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
       // P over S_tj in TMEM, packed pairs: hi in columns 0..31 of the buffer, lo
       // in 32..63; computed and stored 16 keys at a time (fewer live registers).
       // Two keys per FP32 instruction (f32x2 FMA / add / sub).
-      const uint64_t qs2 = f2_pack(qs, qs), nref2 = f2_pack(-ref, -ref);
+      const uint64_t nref2 = f2_pack(kPOff - ref, kPOff - ref);
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
+        const uint64_t qs2 = f2_pack(qsb[q4], qsb[q4]);
         uint32_t phi[8], plo[8];
 #pragma unroll
         for (int c2 = 0; c2 < 8; ++c2) {
@@ -662,7 +750,8 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
     const int odt = casc ? PKV_F32 : a.out_dtype;
     if (ok && my_tiles > 0 && wait(&bars->o_final[t], 0)) {
       tc_fence_after();
-      const float inv = lsum > 0.f ? a.v_scale / lsum : 0.f;
+      float inv = lsum > 0.f ? a.v_scale / lsum : 0.f;
+      if (kFp8 && a.block_scales) inv = ldexpf(inv, ev_ref);
 #pragma unroll
       for (int c = 0; c < kD; c += 32) {
         float o[32];
@@ -690,8 +779,9 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
         }
       }
       if (casc && live)
-        a.out_lse[hrow] = lsum > 0.f ? ((mref == -INFINITY ? 0.f : mref) + __log2f(lsum)) * kLn2
-                                     : -INFINITY;
+        a.out_lse[hrow] = lsum > 0.f
+                              ? ((mref == -INFINITY ? 0.f : mref) + __log2f(lsum) - kPOff) * kLn2
+                              : -INFINITY;
     } else if (my_tiles == 0) {
       if (live) {
         for (int e = 0; e < kD; ++e) store_from_float(a.out, orow + e, odt, 0.f);
