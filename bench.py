@@ -8,9 +8,11 @@ seeded synthetic tensors resident in HBM; the KV pool of the headline workload
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-N > 1 runs under torchrun: every rank runs the same workload on its own GPU
-(data-parallel decode has no exchange between sequences), the time is the max
-over ranks and `value` is the sum of all ranks' KV bytes over that time.
+N > 1 runs under torchrun: one global batch of N times the single-GPU workload
+is split by sequence across the ranks (paged_kv_cache_215_gb300.dp: contiguous
+ranges balanced by token count; decode has no exchange between sequences), the
+time is the max over ranks and `value` is the sum of all ranks' KV bytes over
+that time (weak scaling).
 `--impl reference` times the fp64 CPU oracle on the host cores instead.
 Rank 0 prints one JSON line.
 """
@@ -35,6 +37,7 @@ sys.path.insert(0, ROOT)
 import numpy as np
 import torch
 
+from paged_kv_cache_215_gb300 import dp
 from paged_kv_cache_215_gb300 import workloads as wl
 
 METRIC = "paged decode attn KV GB/s (fraction of HBM peak); decode tokens/s at 128K"
@@ -154,6 +157,12 @@ def algorithmic_attn_bytes(case):
     return kv_bytes(case) + q + out + tables + new
 
 
+def algorithmic_unique_bytes(case):
+    """algorithmic_attn_bytes with every shared block counted once: what one
+    launch must read from HBM at the least."""
+    return algorithmic_attn_bytes(case) - kv_bytes(case) + unique_kv_bytes(case)
+
+
 def unique_kv_bytes(case):
     if not case.shared_prefix_tokens:
         return kv_bytes(case)
@@ -166,11 +175,11 @@ def unique_kv_bytes(case):
 
 # ---------------------------------------------------------------------------- our arm
 class Workload:
-    def __init__(self, name, device):
+    def __init__(self, name, device, case=None):
         from paged_kv_cache_215_gb300 import pkv
         self.pkv = pkv
         self.name = name
-        self.case = wl.FULL[name]()
+        self.case = case if case is not None else wl.FULL[name]()
         c = self.case
         self.tens = wl.make_tensors(c, device=device)
         t = self.tens
@@ -198,6 +207,7 @@ class Workload:
         nb = pkv.workspace_bytes(self.geom, c.batch, self.max_len, 0)
         self.ws = torch.empty(nb, dtype=torch.uint8, device=device)
         self.o_attn = pkv.launch_opts(phase=1)
+        self.o_attn_pdl = pkv.launch_opts(phase=1, pdl=1)
         self.o_merge = pkv.launch_opts(phase=2)
         torch.cuda.synchronize()
 
@@ -270,14 +280,42 @@ def time_steps(w, steps, warmup, split_phases=False, graph_chunk=0):
     return start.elapsed_time(end), [a.elapsed_time(b) for a, b in ev], per_step
 
 
+def time_attention_graph(w, steps, chunk=10):
+    """The attention kernel alone, as it runs inside the step: `chunk` launches
+    chained with programmatic dependent launch, captured in one CUDA graph and
+    replayed; milliseconds per launch."""
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        w.step(w.o_attn_pdl)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(chunk):
+            w.step(w.o_attn_pdl)
+    reps = max(1, steps // chunk)
+    g.replay()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e.record(stream)
+    torch.cuda.synchronize()
+    del g
+    return s.elapsed_time(e) / (reps * chunk)
+
+
 def time_e2e(w, steps, warmup):
-    """Through the C ABI from pinned host memory: per step one host->device copy of
-    the step's inputs (q, the new k and v, the lengths, packed in one pinned
-    staging buffer the way a serving loop would stage them), the decode step
-    (its launches chained with programmatic dependent launch), and the output
-    copied device->host; ten such steps replayed as one CUDA graph.  Byte counts
-    are the staging buffer and the output."""
-    from paged_kv_cache_215_gb300 import pkv
+    """Through the C ABI from pinned host memory, every step: the host->device copy
+    of that step's inputs (q, the new k and v, the lengths, packed in one pinned
+    staging buffer the way a serving loop stages them), the decode step (store +
+    attention + merge, its launches chained with programmatic dependent launch),
+    and the device->host copy of its output.  Steps are pipelined over two
+    staging slots and two output buffers on three streams: step i+1's inputs
+    travel while step i computes, and step i's output travels while step i+1
+    computes; each slot is reused only after the step that last used it has
+    finished with it.  Ten steps are captured in one CUDA graph and replayed.
+    Byte counts are the staging buffer and the output, per step."""
     c = w.case
     t = w.tens
     parts = {k: getattr(t, k).contiguous() for k in ("q", "k_new", "v_new")}
@@ -286,37 +324,72 @@ def time_e2e(w, steps, warmup):
     for k, v in parts.items():
         offs[k] = total
         total += (v.numel() * v.element_size() + 255) // 256 * 256
-    host = torch.empty(total, dtype=torch.uint8).pin_memory()
-    for k, v in parts.items():
-        nb = v.numel() * v.element_size()
-        host[offs[k]:offs[k] + nb].copy_(v.cpu().contiguous().view(torch.uint8).reshape(-1))
-    dev = torch.empty(total, dtype=torch.uint8, device="cuda")
-    view = {k: dev[offs[k]:offs[k] + v.numel() * v.element_size()].view(v.dtype).view(v.shape)
-            for k, v in parts.items()}
-    out_h = torch.empty(w.out.shape, dtype=w.out.dtype).pin_memory()
+    hosts, devs, views, outs, outs_h = [], [], [], [], []
+    for _ in range(2):
+        host = torch.empty(total, dtype=torch.uint8).pin_memory()
+        for k, v in parts.items():
+            nb = v.numel() * v.element_size()
+            host[offs[k]:offs[k] + nb].copy_(v.cpu().contiguous().view(torch.uint8).reshape(-1))
+        dev = torch.empty(total, dtype=torch.uint8, device="cuda")
+        hosts.append(host)
+        devs.append(dev)
+        views.append({k: dev[offs[k]:offs[k] + v.numel() * v.element_size()].view(v.dtype)
+                      .view(v.shape) for k, v in parts.items()})
+        outs.append(torch.empty_like(w.out))
+        outs_h.append(torch.empty(w.out.shape, dtype=w.out.dtype).pin_memory())
     h2d = total
-    d2h = out_h.numel() * out_h.element_size()
-    stream = torch.cuda.current_stream()
-    pdl = pkv.launch_opts(pdl=1)
+    d2h = outs_h[0].numel() * outs_h[0].element_size()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    ev_in = [ev(), ev()]        # slot's inputs are on the device
+    ev_done = [ev(), ev()]      # slot's step finished (inputs read, output written)
+    ev_out = [ev(), ev()]       # slot's output is on the host
+    pdl = w.pkv.launch_opts(pdl=1)
+    saved_out = w.out
 
-    def step():
-        dev.copy_(host, non_blocking=True)
-        w.step(pdl, q=view["q"], k=view["k_new"], v=view["v_new"], seq_lens=view["seq_lens"])
-        out_h.copy_(w.out, non_blocking=True)
+    def step(i, first, comp):
+        k = i % 2
+        with torch.cuda.stream(s_in):
+            if not first[k]:
+                s_in.wait_event(ev_done[k])
+            devs[k].copy_(hosts[k], non_blocking=True)
+            ev_in[k].record(s_in)
+        comp.wait_event(ev_in[k])
+        if not first[k]:
+            comp.wait_event(ev_out[k])
+        w.out = outs[k]
+        v = views[k]
+        w.step(pdl, q=v["q"], k=v["k_new"], v=v["v_new"], seq_lens=v["seq_lens"])
+        ev_done[k].record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[k])
+            outs_h[k].copy_(outs[k], non_blocking=True)
+            ev_out[k].record(s_out)
+        first[k] = False
+
+    def run(n):
+        # the copy streams fork from the stream that runs the steps (the capture
+        # stream inside a graph capture) and join it again at the end
+        comp = torch.cuda.current_stream()
+        s_in.wait_stream(comp)
+        s_out.wait_stream(comp)
+        first = [True, True]
+        for i in range(n):
+            step(i, first, comp)
+        comp.wait_event(ev_out[0])
+        comp.wait_event(ev_out[1])
 
     for _ in range(warmup):
-        step()
+        run(2)
     torch.cuda.synchronize()
-    # the copies and launches of 10 steps replayed as one CUDA graph, as the
-    # device-timed loop does
     chunk = 10
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        for _ in range(chunk):
-            step()
+        run(chunk)
     reps = max(1, steps // chunk)
     graph.replay()
     torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record(stream)
     for _ in range(reps):
@@ -325,6 +398,7 @@ def time_e2e(w, steps, warmup):
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / (reps * chunk)
     del graph
+    w.out = saved_out
     return ms, h2d, d2h
 
 
@@ -360,8 +434,9 @@ def cpu_baseline(w, budget_s=15.0):
                       f"fp64, {spent:.1f} s; GB/s counts each row's share of the KV bytes"}
 
 
-def measure(name, steps, warmup, device, with_clocks=False, gpu_index=0, e2e=True, graph=True):
-    w = Workload(name, device)
+def measure(name, steps, warmup, device, with_clocks=False, gpu_index=0, e2e=True, graph=True,
+            case=None):
+    w = Workload(name, device, case)
     c = w.case
     peak, peak_kind = peaks()
     sampler = ClockSampler(gpu_index) if with_clocks else None
@@ -372,13 +447,18 @@ def measure(name, steps, warmup, device, with_clocks=False, gpu_index=0, e2e=Tru
     eager_ms, _, per_step = time_steps(w, steps, warmup)
     graph_ms = time_steps(w, steps, 3, graph_chunk=10)[0] if graph else None
     clocks = sampler.stop() if sampler else None
-    # the attention kernel alone, timed per launch with events on its stream
+    # the attention kernel alone: back to back inside a CUDA graph (as in the
+    # step), and per launch with events around it on its stream
+    attn_graph_ms = time_attention_graph(w, steps) if graph else None
     _, attn, _ = time_steps(w, steps, 3, split_phases=True)
     eager = eager_ms / steps
     gstep = graph_ms / steps if graph_ms else None
     ms = min(eager, gstep) if gstep else eager
-    attn_ms = float(np.mean(attn))
-    alg = algorithmic_attn_bytes(c)
+    attn_iso_ms = float(np.mean(attn))
+    attn_ms = attn_graph_ms if attn_graph_ms else attn_iso_ms
+    # the roofline counts what one launch must read from HBM: blocks shared by
+    # several sequences once (their repeats come from L2)
+    alg = algorithmic_unique_bytes(c)
     res = {
         "ms_per_step": ms,
         "ms_per_step_eager": eager,
@@ -386,11 +466,14 @@ def measure(name, steps, warmup, device, with_clocks=False, gpu_index=0, e2e=Tru
         "timing": "cuda-graph replay of 10-step chunks" if (gstep and gstep <= eager)
                   else "eager launches",
         "kv_bytes": kv_bytes(c),
-        "kv_gbs": kv_bytes(c) / (ms * 1e-3) / 1e9,
+        "kv_gbs": unique_kv_bytes(c) / (ms * 1e-3) / 1e9,
         "attn_kernel_us": attn_ms * 1e3,
-        "attn_kernel_median_us": float(np.median(attn)) * 1e3,
-        "attn_kernel_p10_p90_us": [float(np.percentile(attn, 10)) * 1e3,
-                                   float(np.percentile(attn, 90)) * 1e3],
+        "attn_kernel_timing": "10 launches chained with PDL in a CUDA graph, replayed"
+                              if attn_graph_ms else "CUDA events around each launch",
+        "attn_kernel_isolated_us": attn_iso_ms * 1e3,
+        "attn_kernel_isolated_median_us": float(np.median(attn)) * 1e3,
+        "attn_kernel_isolated_p10_p90_us": [float(np.percentile(attn, 10)) * 1e3,
+                                            float(np.percentile(attn, 90)) * 1e3],
         "algorithmic_bytes": alg,
         "roofline": {
             "bound": "hbm",
@@ -411,8 +494,9 @@ def measure(name, steps, warmup, device, with_clocks=False, gpu_index=0, e2e=Tru
         "block_waste": wl.block_waste(c),
     }
     if c.shared_prefix_tokens:
+        # every sequence's whole KV counted, shared blocks once per sequence
+        res["logical_kv_gbs"] = kv_bytes(c) / (ms * 1e-3) / 1e9
         res["unique_kv_bytes"] = unique_kv_bytes(c)
-        res["unique_kv_gbs"] = unique_kv_bytes(c) / (ms * 1e-3) / 1e9
     if e2e:
         e_ms, h2d, d2h = time_e2e(w, max(10, steps // 10), 3)
         res["e2e"] = {"value": kv_bytes(c) / (e_ms * 1e-3) / 1e9, "unit": UNIT,
@@ -554,28 +638,34 @@ def measure_cascade(name, device, steps=20):
     """Decode attention (no append) of a batch whose sequences share a prefix of
     blocks: the plain path (every sequence reads the prefix) against the
     shared-prefix path (the prefix read once for all sequences on the tcgen05
-    kernel, the private suffixes through the decode kernel).  Logical GB/s
-    counts every sequence's whole KV, like the plain decode's metric."""
+    kernel, the private suffixes through the decode kernel).  Reported: times of
+    the plain decode, the automatic route and the forced prefix pass; GB/s of
+    the unique KV bytes (every block once: what the HBM must deliver) and of the
+    logical bytes (every sequence's whole KV); and the prefix pass's own rate
+    (phase 1: the suffix-table build and the tcgen05 pass over the prefix) in
+    TFLOP/s, 4 x head_dim flops per (query head of a sequence, prefix key)."""
     from paged_kv_cache_215_gb300 import pkv
     w = Workload(name, device)
     c = w.case
     table, P, lens = wl.prefix_args(c)
+    prefix_flops = 4.0 * c.head_dim * c.num_q_heads * float(lens.astype(np.int64).sum())
     table = torch.from_numpy(table).to(device)
     lens = torch.from_numpy(lens).to(device)
     out = torch.empty_like(w.out)
     ws = torch.empty(pkv.cascade_workspace_bytes(w.geom, c.batch, c.max_blocks, w.max_len, P),
                      dtype=torch.uint8, device=device)
 
-    def cascade(route=0):
+    def cascade(route=0, phase=0):
         pkv.paged_decode_attention_cascade(out, w.tens.q, w.pool, c.layer, table, P, lens,
                                            w.tables, w.seq_lens, w.max_len, c.scale, workspace=ws,
-                                           opts=pkv.launch_opts(kernel=route))
+                                           opts=pkv.launch_opts(kernel=route, phase=phase))
 
     def plain():
         pkv.paged_decode_attention(w.out, w.tens.q, w.pool, c.layer, w.tables, w.seq_lens,
                                    w.max_len, c.scale, workspace=w.ws)
     res = {}
-    arms = (("plain", plain), ("cascade", cascade), ("prefix_pass", lambda: cascade(3)))
+    arms = (("plain", plain), ("cascade", cascade), ("prefix_pass", lambda: cascade(3)),
+            ("prefix_pass_phase1", lambda: cascade(3, 1)))
     for nm, f in arms * 2:
         for _ in range(3):
             f()
@@ -588,17 +678,21 @@ def measure_cascade(name, device, steps=20):
         torch.cuda.synchronize()
         res[nm] = min(res.get(nm, 1e9), s.elapsed_time(e) / steps * 1e3)
     status = w.pool.check_status()
-    kvb = kv_bytes(c)
+    kvb, ukv = kv_bytes(c), unique_kv_bytes(c)
     w.close()
     del w
     torch.cuda.empty_cache()
     return {"batch": c.batch, "shared_prefix_tokens": P, "status": status,
             "plain_us": res["plain"], "cascade_us": res["cascade"],
-            "prefix_pass_us": res["prefix_pass"],
+            "forced_prefix_route_us": res["prefix_pass"],
+            "prefix_pass_us": res["prefix_pass_phase1"],
+            "prefix_pass_tflops": prefix_flops / (res["prefix_pass_phase1"] * 1e-6) / 1e12,
             "speedup": res["plain"] / res["cascade"],
-            "kv_gbs_plain": kvb / (res["plain"] * 1e-6) / 1e9,
-            "kv_gbs_cascade": kvb / (res["cascade"] * 1e-6) / 1e9,
-            "unique_kv_bytes": unique_kv_bytes(c)}
+            "unique_kv_bytes": ukv,
+            "unique_kv_gbs_plain": ukv / (res["plain"] * 1e-6) / 1e9,
+            "unique_kv_gbs_cascade": ukv / (res["cascade"] * 1e-6) / 1e9,
+            "logical_kv_gbs_plain": kvb / (res["plain"] * 1e-6) / 1e9,
+            "logical_kv_gbs_cascade": kvb / (res["cascade"] * 1e-6) / 1e9}
 
 
 APPEND = ["llama8b_b32_8k", "fp8_b8_32k"]
@@ -656,7 +750,10 @@ def run_ours(args):
     if ws > 1:
         dist.barrier()
     name = args.workload
-    w, res = measure(name, args.steps, args.warmup, device, with_clocks=True, gpu_index=local)
+    # this rank's share of the global batch (N times the single-GPU workload)
+    case = dp.rank_case(name, rank, ws)
+    w, res = measure(name, args.steps, args.warmup, device, with_clocks=True, gpu_index=local,
+                     case=case)
     ms, value = aggregate_ranks(res["ms_per_step"], res["kv_bytes"], device)
     extra = {}
     if rank == 0 and not args.no_cpu_baseline:
@@ -674,13 +771,15 @@ def run_ours(args):
             torch.cuda.empty_cache()
             others[other] = {k: ores[k] for k in ("ms_per_step", "ms_per_step_eager",
                                                   "ms_per_step_graph", "kv_gbs", "attn_kernel_us",
+                                                  "attn_kernel_isolated_us",
                                                   "tokens_per_s_per_layer",
                                                   "decode_tokens_per_s_model", "batch",
                                                   "block_waste")}
             others[other]["roofline_frac"] = ores["roofline"]["frac"]
             others[other]["achieved_gbs"] = ores["roofline"]["achieved"]
-            if "unique_kv_gbs" in ores:
-                others[other]["unique_kv_gbs"] = ores["unique_kv_gbs"]
+            if "logical_kv_gbs" in ores:
+                others[other]["logical_kv_gbs"] = ores["logical_kv_gbs"]
+                others[other]["unique_kv_bytes"] = ores["unique_kv_bytes"]
     if rank == 0 and not args.only_primary:
         for mq_name, (base, q_len) in wl.MULTI_TOKEN.items():
             others[mq_name] = measure_multi_token(base, q_len, max(50, args.steps // 20), device)
@@ -700,18 +799,15 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": c.kv_dtype, "data": "synthetic (seeded N(0,1))",
-        "config": {"workload": wl.FULL[name]().name, "batch": c.batch,
-                   "seq_len": int(c.seq_lens.max()), "q_heads": c.num_q_heads,
-                   "kv_heads": c.num_kv_heads, "head_dim": c.head_dim,
-                   "block_size": c.block_size, "kv_dtype": c.kv_dtype,
-                   "parallelism": f"dp{ws} (independent sequences per GPU)",
-                   "l2": "inputs larger than L2 (KV read per step >> 129 MB), no flush"},
+        "config": bench_config(c, ws),
         "decode_tokens_per_s": res["decode_tokens_per_s_model"],
         "decode_tokens_per_s_per_layer": res["tokens_per_s_per_layer"],
         "roofline": res["roofline"],
         "attn_kernel_us": res["attn_kernel_us"],
-        "attn_kernel_median_us": res["attn_kernel_median_us"],
-        "attn_kernel_p10_p90_us": res["attn_kernel_p10_p90_us"],
+        "attn_kernel_timing": res["attn_kernel_timing"],
+        "attn_kernel_isolated_us": res["attn_kernel_isolated_us"],
+        "attn_kernel_isolated_median_us": res["attn_kernel_isolated_median_us"],
+        "attn_kernel_isolated_p10_p90_us": res["attn_kernel_isolated_p10_p90_us"],
         "ms_per_step_eager": res["ms_per_step_eager"],
         "ms_per_step_graph": res["ms_per_step_graph"],
         "timing": res["timing"],
@@ -725,6 +821,17 @@ def run_ours(args):
     if others:
         line["workloads"] = others
     print(json.dumps(line), flush=True)
+
+
+def bench_config(c, world):
+    """The line's config: the workload of one GPU, the global batch of the job."""
+    return {"workload": c.name, "batch": c.batch, "global_batch": c.batch * world,
+            "seq_len": int(c.seq_lens.max()), "q_heads": c.num_q_heads,
+            "kv_heads": c.num_kv_heads, "head_dim": c.head_dim, "block_size": c.block_size,
+            "kv_dtype": c.kv_dtype,
+            "parallelism": f"dp{world} (the global batch split by sequence across GPUs, "
+                           "no exchange)",
+            "l2": "inputs larger than L2 (KV read per step >> 129 MB), no flush"}
 
 
 # ---------------------------------------------------------------------------- reference arm
@@ -792,9 +899,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1))",
-        "config": {"workload": c.name, "batch": c.batch, "seq_len": int(c.seq_lens.max()),
-                   "q_heads": c.num_q_heads, "kv_heads": c.num_kv_heads,
-                   "head_dim": c.head_dim, "block_size": c.block_size, "kv_dtype": c.kv_dtype},
+        "config": bench_config(c, ws),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -340,7 +340,11 @@ PKV_API size_t paged_decode_workspace_bytes_mq(const pkv_geometry* geom, int bat
  * they save, so such a call runs steps 2-3 as paged_decode_attention over the
  * sequences' own tables, after the same check of step 1.  opts->kernel (opts
  * may be NULL): 0 that automatic choice, 2 always the plain decode, 3 always the
- * prefix pass; other values PKV_EINVAL; the other fields are ignored.
+ * prefix pass; other values PKV_EINVAL.  opts->phase splits the call so that a
+ * caller can time its parts: 0 everything, 1 steps 1-2 (the suffix tables and
+ * the prefix pass), 2 step 3 (the suffix decode and the merge; needs a phase-1
+ * call with the same arguments and workspace before it on the stream); other
+ * values PKV_EINVAL.  The other fields are ignored.
  * Measured on one GB300: 32 sequences sharing 64K tokens (268 MB of K/V), 7x
  * faster than paged_decode_attention; 64 sequences sharing 4K tokens (17 MB),
  * the prefix pass 2% slower than the plain decode. */

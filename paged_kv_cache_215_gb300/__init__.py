@@ -7,7 +7,7 @@ machine without the library; using the binding without the library raises.
 """
 import importlib
 
-__all__ = ["pkv", "workloads", "build"]
+__all__ = ["pkv", "workloads", "build", "dp"]
 
 
 def __getattr__(name):

@@ -833,7 +833,9 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
       !mma_supported(g.kv_dtype, g.block_size, g.head_dim, G, 1) || batch > 65535)
     return PKV_EUNSUPPORTED;
   const int kernel = opts ? opts->kernel : 0;
+  const int phase = opts ? opts->phase : 0;
   if (kernel != 0 && kernel != 2 && kernel != 3) return PKV_EINVAL;
+  if (phase < 0 || phase > 2) return PKV_EINVAL;
   DeviceInfo dev;
   if (!device_info(&dev)) return PKV_ECUDA;
   const size_t dec = paged_decode_workspace_bytes(&g, batch, max_seq_len, 0);
@@ -857,7 +859,7 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
 
   // 1. suffix tables and lengths (and the check that each prefix is the shared
   //    one; the plain route runs the check alone)
-  if (launch_suffix_tables(d_block_tables, max_blocks_per_seq, d_seq_lens,
+  if (phase != 2 && launch_suffix_tables(d_block_tables, max_blocks_per_seq, d_seq_lens,
                            prefix_len_max > 0 ? d_prefix_table : d_block_tables,
                            prefix_len_max > 0 ? prefix_blocks : 0, d_prefix_lens, prefix_len_max,
                            batch, g.block_size, plain ? nullptr : suf_tab,
@@ -865,12 +867,14 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
                            stream) != cudaSuccess)
     return PKV_ECUDA;
   if (plain)
-    return decode_common(d_out, out_dtype, d_q, q_dtype, 1, nullptr, nullptr, 0, pool, layer,
-                         d_block_tables, max_blocks_per_seq, d_seq_lens, batch, max_seq_len, scale,
-                         k_scale, v_scale, 0, ws + w.dec_off, ws_bytes - w.dec_off, nullptr, stream);
+    return phase == 1 ? PKV_OK
+                      : decode_common(d_out, out_dtype, d_q, q_dtype, 1, nullptr, nullptr, 0, pool,
+                                      layer, d_block_tables, max_blocks_per_seq, d_seq_lens, batch,
+                                      max_seq_len, scale, k_scale, v_scale, 0, ws + w.dec_off,
+                                      ws_bytes - w.dec_off, nullptr, stream);
   // 2. the shared prefix once for every sequence: tcgen05 tiles of 128 query rows
   //    (sequences x heads of a KV head), key range cut into w.S splits
-  if (prefix_len_max > 0) {
+  if (prefix_len_max > 0 && phase != 2) {
     const CUtensorMap* map = p->tmap(1);
     if (!map) return PKV_ECUDA;
     DecodeArgs t{};
@@ -905,6 +909,7 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
     if (launch_prefill_tc(map, t, stream) != cudaSuccess) return PKV_ECUDA;
   }
   // 3. the private suffixes, merged with the prefix partials
+  if (phase == 1) return PKV_OK;
   const ExtPartials ext{ext_o, ext_lse, prefix_len_max > 0 ? w.S : 0};
   return decode_common(d_out, out_dtype, d_q, q_dtype, 1, nullptr, nullptr, 0, pool, layer, suf_tab,
                        max_blocks_per_seq, suf_lens, batch, max_seq_len, scale, k_scale, v_scale, 0,

@@ -1,0 +1,60 @@
+"""Data-parallel decode over sequences: which GPU owns which sequences.
+
+Decode attention of one sequence reads only that sequence's blocks, so a batch
+splits across GPUs by sequence with no exchange between them: each GPU holds
+its sequences' blocks in its own pool, runs the whole step (append, attention,
+merge) on them, and returns their outputs.  The only host-side decision is the
+split; this module makes it: contiguous ranges of the global batch, cut at the
+token-count quantiles so that every GPU reads about the same KV bytes (the
+quantity the step's time follows), every sequence owned by exactly one rank.
+"""
+from __future__ import annotations
+
+from typing import List, Tuple
+
+import numpy as np
+
+from . import workloads as wl
+
+
+def partition(seq_lens, world: int) -> List[Tuple[int, int]]:
+    """Contiguous [lo, hi) ranges of sequences, one per rank, covering the batch
+    once.  Rank r takes the sequences whose first token lies in the r-th
+    1/world of all tokens (a sequence straddling a cut goes to the rank its
+    start falls in); with no tokens at all, equal sequence counts."""
+    lens = np.asarray(seq_lens, dtype=np.int64)
+    B = int(lens.shape[0])
+    if world < 1:
+        raise ValueError("world must be >= 1")
+    total = int(lens.sum())
+    if total == 0:
+        cuts = [B * r // world for r in range(world + 1)]
+    else:
+        starts = np.concatenate([[0], np.cumsum(lens)[:-1]])
+        # first sequence whose start reaches r * total / world (exact integer test)
+        cuts = [int(np.searchsorted(starts * world, r * total, side="left"))
+                for r in range(world)] + [B]
+        cuts[0] = 0
+    return [(cuts[r], cuts[r + 1]) for r in range(world)]
+
+
+def shard(case: "wl.Case", lo: int, hi: int) -> "wl.Case":
+    """The sub-batch [lo, hi) of a case as a case of its own, for one rank: the
+    sequences keep their lengths (and their shared prefix, if any), and get a
+    pool and tables of the rank's own.  The whole batch is returned as is."""
+    if lo == 0 and hi == case.batch:
+        return case
+    return wl.make_case(f"{case.name}_seqs{lo}-{hi}", case.seq_lens[lo:hi], case.num_q_heads,
+                        case.num_kv_heads, case.head_dim, case.block_size, case.kv_dtype,
+                        case.q_dtype, case.out_dtype, seed=case.seed + 7919 * (lo + 1),
+                        spike_frac=case.spike_frac,
+                        shared_prefix_tokens=case.shared_prefix_tokens,
+                        num_layers=case.num_layers, layer=case.layer)
+
+
+def rank_case(name: str, rank: int, world: int) -> "wl.Case":
+    """Rank `rank`'s share of the global batch of workload `name` at `world` GPUs
+    (weak scaling: the global batch is `world` times the single-GPU one)."""
+    glob = wl.FULL[name](world)
+    lo, hi = partition(glob.seq_lens, world)[rank]
+    return shard(glob, lo, hi)

@@ -146,10 +146,11 @@ def llama8b_batch(batch=32, lo=4096, hi=12288, seed=1001, block_size=16) -> Case
                      block_size, "bf16", "bf16", "bf16", seed=seed)
 
 
-def long_context(tokens=131072, seed=1002) -> Case:
-    """Batch 1, 32 query / 8 KV heads, head_dim 128, bf16, 1% of K rows x4."""
-    return make_case(f"long_context_b1_{tokens}", [tokens], 32, 8, 128, 16, "bf16", "bf16",
-                     "bf16", seed=seed, spike_frac=0.01)
+def long_context(tokens=131072, seed=1002, batch=1) -> Case:
+    """Batch 1 (or `batch` such requests), 32 query / 8 KV heads, head_dim 128, bf16,
+    1% of K rows x4."""
+    return make_case(f"long_context_b{batch}_{tokens}", [tokens] * batch, 32, 8, 128, 16, "bf16",
+                     "bf16", "bf16", seed=seed, spike_frac=0.01)
 
 
 def fp8_batch(batch=8, tokens=32768, heads=(32, 8, 128), seed=1003) -> Case:
@@ -179,10 +180,10 @@ def llama8b_layers(num_layers=4, layer=2, batch=32, lo=4096, hi=12288, seed=1005
                      layer=layer)
 
 
-def long_context_bs64(tokens=131072, seed=1006) -> Case:
+def long_context_bs64(tokens=131072, seed=1006, batch=1) -> Case:
     """The 128K request in 64-token blocks."""
-    return make_case(f"long_context_b1_{tokens}_bs64", [tokens], 32, 8, 128, 64, "bf16", "bf16",
-                     "bf16", seed=seed, spike_frac=0.01)
+    return make_case(f"long_context_b{batch}_{tokens}_bs64", [tokens] * batch, 32, 8, 128, 64,
+                     "bf16", "bf16", "bf16", seed=seed, spike_frac=0.01)
 
 
 def shared_prefix_long(batch=32, prefix=65536, lo=64, hi=2048, seed=1010) -> Case:
@@ -207,17 +208,21 @@ def prefix_args(case: Case, used: Optional[int] = None):
     return table, used, lens
 
 
+# Each full-size workload, drawn for `mult` times its batch (a data-parallel job
+# over several GPUs draws one global batch of that many sequences and gives
+# each GPU a share; mult = 1 is the single-GPU workload).
 FULL = {
-    "tiny": tiny_gqa2_d64_f32,
-    "llama8b_b32_8k": lambda: llama8b_batch(),
-    "long_128k": lambda: long_context(131072),
-    "long_1m": lambda: long_context(1048576),
-    "fp8_b8_32k": lambda: fp8_batch(),
-    "llama70b_prefix_bs16": lambda: llama70b_prefix(block_size=16),
-    "llama70b_prefix_bs32": lambda: llama70b_prefix(block_size=32),
-    "long_128k_bs64": lambda: long_context_bs64(),
-    "llama8b_b32_8k_layers4": lambda: llama8b_layers(),
-    "shared_prefix_64k_b32": lambda: shared_prefix_long(),
+    "tiny": lambda mult=1: tiny_gqa2_d64_f32() if mult == 1 else make_case(
+        f"tiny_x{mult}", [38, 101] * mult, 4, 2, 64, 16, "f32", "f32", "f32", seed=1000),
+    "llama8b_b32_8k": lambda mult=1: llama8b_batch(batch=32 * mult),
+    "long_128k": lambda mult=1: long_context(131072, batch=mult),
+    "long_1m": lambda mult=1: long_context(1048576, batch=mult),
+    "fp8_b8_32k": lambda mult=1: fp8_batch(batch=8 * mult),
+    "llama70b_prefix_bs16": lambda mult=1: llama70b_prefix(batch=64 * mult, block_size=16),
+    "llama70b_prefix_bs32": lambda mult=1: llama70b_prefix(batch=64 * mult, block_size=32),
+    "long_128k_bs64": lambda mult=1: long_context_bs64(batch=mult),
+    "llama8b_b32_8k_layers4": lambda mult=1: llama8b_layers(batch=32 * mult),
+    "shared_prefix_64k_b32": lambda mult=1: shared_prefix_long(batch=32 * mult),
 }
 
 # query tokens per sequence of the multi-token (speculative verification) measurements

@@ -27,6 +27,10 @@ def test_reference_arm_prints_one_contract_line():
     assert d["impl"] == "reference" and d["steps"] == 3 and d["warmup"] == 3 and d["n_gpus"] == 1
     assert d["value"] > 0 and d["higher_is_better"] is True
     assert d["config"]["workload"] == "tiny_gqa2_d64_f32"
+    # the same config keys as the GPU arm prints (bench_config), so the two lines compare
+    import bench
+    assert d["config"] == json.loads(json.dumps(bench.bench_config(
+        __import__("paged_kv_cache_215_gb300.workloads", fromlist=["x"]).FULL["tiny"](), 1)))
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,

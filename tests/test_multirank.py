@@ -1,11 +1,17 @@
-"""The benchmark's multi-rank path on CPU: two gloo ranks, each with its own
-(independent) batch, report the slowest rank's time and the sum of bytes."""
+"""The multi-rank path on CPU (gloo): the data-parallel split of one global batch
+by sequence (every sequence owned by exactly one rank, ranks balanced by token
+count) and the benchmark's aggregation (the slowest rank's time, the sum of all
+ranks' bytes)."""
 import os
 import socket
 
+import numpy as np
 import pytest
 import torch.distributed as dist
 import torch.multiprocessing as mp
+
+from paged_kv_cache_215_gb300 import dp
+from paged_kv_cache_215_gb300 import workloads as wl
 
 
 def _free_port():
@@ -48,3 +54,86 @@ def test_single_rank_aggregation_is_identity():
     import bench
     ms, gbs = bench.aggregate_ranks(2.0, 4_000_000)
     assert ms == 2.0 and gbs == pytest.approx(4_000_000 / 2e-3 / 1e9)
+
+
+def _check_partition(lens, world):
+    parts = dp.partition(lens, world)
+    assert len(parts) == world
+    assert parts[0][0] == 0 and parts[-1][1] == len(lens)
+    for (a0, a1), (b0, b1) in zip(parts, parts[1:]):
+        assert a0 <= a1 == b0 <= b1                       # contiguous, disjoint
+    lens = np.asarray(lens, dtype=np.int64)
+    total, mx = int(lens.sum()), int(lens.max()) if len(lens) else 0
+    for lo, hi in parts:                                  # within one sequence of the mean
+        assert abs(int(lens[lo:hi].sum()) - total / world) <= mx + 1e-9
+    return parts
+
+
+def test_partition_covers_every_sequence_once():
+    rng = np.random.default_rng(0)
+    for world in (1, 2, 3, 4, 8):
+        for B in (1, 2, 7, 64, 200):
+            for kind in ("uniform", "loguniform", "one_long", "zeros"):
+                if kind == "uniform":
+                    lens = rng.integers(4096, 12289, B)
+                elif kind == "loguniform":
+                    lens = np.round(np.exp(rng.uniform(np.log(512), np.log(131072), B)))
+                elif kind == "one_long":
+                    lens = np.full(B, 100)
+                    lens[B // 2] = 1 << 20
+                else:
+                    lens = np.zeros(B, dtype=np.int64)
+                _check_partition(lens.astype(np.int64), world)
+    # a world larger than the batch leaves some ranks empty, never a sequence twice
+    parts = _check_partition([5, 6], 4)
+    assert sum(hi - lo for lo, hi in parts) == 2
+
+
+def test_weak_scaling_global_batch_is_world_times_the_workload():
+    for name in ("llama8b_b32_8k", "long_128k", "fp8_b8_32k", "llama70b_prefix_bs16"):
+        one = wl.FULL[name]()
+        for world in (2, 4):
+            glob = wl.FULL[name](world)
+            assert glob.batch == world * one.batch
+            got = sorted(int(n) for r in range(world)
+                         for n in dp.rank_case(name, r, world).seq_lens)
+            assert got == sorted(int(n) for n in glob.seq_lens)
+    assert dp.rank_case("long_128k", 0, 1).name == wl.FULL["long_128k"]().name
+
+
+def _shard_worker(rank, world, port, results):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    case = dp.rank_case("llama8b_b32_8k", rank, world)
+    lo, hi = dp.partition(wl.FULL["llama8b_b32_8k"](world).seq_lens, world)[rank]
+    mine = (lo, hi, [int(n) for n in case.seq_lens], int(case.num_blocks))
+    gathered = [None] * world
+    dist.all_gather_object(gathered, mine)
+    results[rank] = gathered
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_ranks_own_disjoint_shards_of_one_global_batch():
+    """Each gloo rank builds its own share of the 8K x 32 workload's two-GPU global
+    batch (64 sequences); gathered, the shares are disjoint, contiguous, cover the
+    global batch once with its lengths, and each rank's pool holds its own blocks."""
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    results = mgr.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_shard_worker, args=(r, 2, port, results)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=180)
+        assert p.exitcode == 0
+    glob = wl.FULL["llama8b_b32_8k"](2)
+    for r in range(2):
+        g = results[r]
+        assert g[0][0] == 0 and g[0][1] == g[1][0] and g[1][1] == glob.batch
+        lens = g[0][2] + g[1][2]
+        assert lens == [int(n) for n in glob.seq_lens]
+        for lo, hi, ls, nb in g:
+            need = sum((n + 15) // 16 for n in ls)
+            assert nb >= need                              # its own pool covers its blocks
