@@ -119,6 +119,30 @@ PKV_API int kv_pool_num_free(const pkv_pool* pool);
  * PKV_ENOMEM if no block is free. */
 PKV_API int kv_pool_cow(pkv_pool* pool, int32_t id, int32_t* out_id, cudaStream_t stream);
 
+/* Room for the next tokens of every sequence, before they are appended ([ENG26]
+ * 2.2: append_token calls allocate_block when a token starts a new block;
+ * [UNLOCK] 3.1: on-demand allocation, and copy-on-write of a block shared with
+ * another sequence before it is written).  For s in [0, batch), sequence s holds
+ * n = h_seq_lens[s] tokens and will append k = h_new_tokens[s] (NULL: 1 each):
+ *   - table entries [ceil(n / bs), ceil((n + k) / bs)) get freshly taken blocks;
+ *   - if k > 0 and n % bs != 0, the block at entry n / bs (the partly filled one
+ *     the first new token lands in) is copied into a fresh block when its
+ *     reference count is above 1, on `stream` (all layers, K and V), the entry
+ *     is replaced and the shared block loses one reference.  Sequences sharing
+ *     one tail are resolved in order: the last of them keeps the original.
+ * h_block_tables: host int32 [batch, max_blocks_per_seq], updated in place (the
+ * caller uploads the rows that changed before the append).  h_first_changed:
+ * host int32 [batch] or NULL; receives the first changed entry of each row, or
+ * -1.  All or nothing: PKV_ENOMEM if the free blocks do not cover every
+ * sequence's need, PKV_EINVAL if a count is negative, a sequence would outgrow
+ * max_blocks_per_seq or its tail entry is not a live block, PKV_ECUDA if a copy
+ * cannot be issued; in each case pool and tables are unchanged.  Host-side and
+ * not thread-safe with the other allocator calls. */
+PKV_API int kv_pool_prepare_append(pkv_pool* pool, int batch, const int32_t* h_seq_lens,
+                                   const int32_t* h_new_tokens, int32_t* h_block_tables,
+                                   int max_blocks_per_seq, int32_t* h_first_changed,
+                                   cudaStream_t stream);
+
 /* ---------------------------------------------------------------- append (reshape_and_cache) */
 
 /* [ENG26] 2.2 append_token, one token per sequence: for s in [0, batch),

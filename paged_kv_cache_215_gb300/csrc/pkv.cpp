@@ -375,6 +375,86 @@ int kv_pool_cow(pkv_pool* p, int32_t id, int32_t* out_id, cudaStream_t stream) {
   return PKV_OK;
 }
 
+int kv_pool_prepare_append(pkv_pool* p, int batch, const int32_t* h_seq_lens,
+                           const int32_t* h_new_tokens, int32_t* h_block_tables,
+                           int max_blocks_per_seq, int32_t* h_first_changed,
+                           cudaStream_t stream) {
+  if (!p || batch < 0 || max_blocks_per_seq < 1) return PKV_EINVAL;
+  if (batch == 0) return PKV_OK;
+  if (!h_seq_lens || !h_block_tables) return PKV_EINVAL;
+  const int bs = p->g.block_size;
+  std::lock_guard<std::mutex> lk(p->mu);
+  // plan: per sequence the table entries to fill and whether its tail block
+  // (the partly filled block the first new token lands in) must be copied;
+  // shared tails are resolved in sequence order, as the copies will be
+  struct Plan { int s, first_new, end, cow; };
+  std::vector<Plan> plan;
+  std::map<int32_t, int> refs;   // simulated counts of the tail blocks touched
+  long long need = 0;
+  for (int s = 0; s < batch; ++s) {
+    const long long n = h_seq_lens[s];
+    const long long k = h_new_tokens ? h_new_tokens[s] : 1;
+    if (n < 0 || k < 0) return PKV_EINVAL;
+    if (k == 0) continue;
+    const long long have = (n + bs - 1) / bs, want = (n + k + bs - 1) / bs;
+    if (want > max_blocks_per_seq) return PKV_EINVAL;
+    int cow = 0;
+    if (n % bs != 0) {
+      const int32_t id = h_block_tables[(size_t)s * max_blocks_per_seq + n / bs];
+      if (id < 0 || id >= p->g.num_blocks || p->ref[id] <= 0) return PKV_EINVAL;
+      auto it = refs.emplace(id, p->ref[id]).first;
+      if (it->second > 1) {
+        cow = 1;
+        --it->second;
+      }
+    }
+    need += (want - have) + cow;
+    if (want > have || cow) plan.push_back({s, (int)have, (int)want, cow});
+  }
+  if (need > (long long)p->free_ids.size()) return PKV_ENOMEM;   // nothing changed
+  // the blocks to take, from the top of the free stack (taken only below)
+  std::vector<int32_t> ids(p->free_ids.end() - need, p->free_ids.end());
+  std::reverse(ids.begin(), ids.end());
+  // copies first: a failed copy leaves the host state as it was
+  size_t next = 0;
+  const size_t bb = p->block_bytes();
+  char* base = static_cast<char*>(p->d_pool);
+  for (const Plan& pl : plan) {
+    if (!pl.cow) continue;
+    const int32_t src = h_block_tables[(size_t)pl.s * max_blocks_per_seq + h_seq_lens[pl.s] / bs];
+    if (cudaMemcpyAsync(base + (size_t)ids[next] * bb, base + (size_t)src * bb, bb,
+                        cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+      return PKV_ECUDA;
+    ++next;
+  }
+  // commit: take the blocks, move the references, write the tables
+  if (h_first_changed)
+    for (int s = 0; s < batch; ++s) h_first_changed[s] = -1;
+  next = 0;
+  size_t fresh = 0;
+  for (const int32_t id : ids) {
+    p->take(id);
+    p->ref[id] = 1;
+  }
+  // copies took ids[0 .. copies); fresh blocks follow
+  size_t copies = 0;
+  for (const Plan& pl : plan) copies += pl.cow;
+  fresh = copies;
+  for (const Plan& pl : plan) {
+    int32_t* row = h_block_tables + (size_t)pl.s * max_blocks_per_seq;
+    int first = pl.first_new;
+    if (pl.cow) {
+      const int j = h_seq_lens[pl.s] / bs;
+      --p->ref[row[j]];
+      row[j] = ids[next++];
+      first = j;
+    }
+    for (int j = pl.first_new; j < pl.end; ++j) row[j] = ids[fresh++];
+    if (h_first_changed) h_first_changed[pl.s] = first;
+  }
+  return PKV_OK;
+}
+
 static int append_common(pkv_pool* p, int layer, const void* k, const void* v, pkv_dtype in_dtype,
                          const int32_t* tables, int max_blocks, int batch, const int32_t* seq_ids,
                          const int32_t* positions, int64_t num_tokens, float k_scale,

@@ -67,6 +67,7 @@ def _load() -> ctypes.CDLL:
         "kv_pool_refcount": (I, [P, ctypes.c_int32]),
         "kv_pool_num_free": (I, [P]),
         "kv_pool_cow": (I, [P, ctypes.c_int32, P, P]),
+        "kv_pool_prepare_append": (I, [P, I, P, P, P, I, P, P]),
         "kv_append": (I, [P, I, P, P, I, P, I, P, I, F, F, P]),
         "kv_append_tokens": (I, [P, I, P, P, I, P, I, I, P, P, I64, F, F, P]),
         "kv_absmax": (I, [P, I, I64, P, P]),
@@ -102,7 +103,8 @@ def _load() -> ctypes.CDLL:
 _lib = _load()
 EXPORTS = ("kv_pool_bytes", "kv_pool_create", "kv_pool_destroy", "kv_pool_geometry",
            "kv_pool_alloc", "kv_pool_reserve", "kv_pool_free", "kv_pool_share",
-           "kv_pool_refcount", "kv_pool_num_free", "kv_pool_cow", "kv_append",
+           "kv_pool_refcount", "kv_pool_num_free", "kv_pool_cow", "kv_pool_prepare_append",
+           "kv_append",
            "kv_append_tokens", "kv_absmax", "kv_fp8_scale", "paged_decode_workspace_bytes",
            "kv_pool_set_block_scales", "kv_block_scales",
            "paged_decode_attention", "paged_decode_attention_ex", "merge_partials",
@@ -230,6 +232,23 @@ class KVPool:
         _check(_lib.kv_pool_cow(self.handle, block_id, ctypes.byref(out), _stream(stream)),
                "kv_pool_cow")
         return out.value
+
+    def prepare_append(self, seq_lens, tables, new_tokens=None, stream=None):
+        """Extend the host tables (numpy int32 [B, max_blocks], updated in place) for
+        the next tokens of every sequence, copying shared tail blocks first; returns
+        each row's first changed entry (-1: unchanged)."""
+        import numpy as np
+        assert tables.dtype == np.int32 and tables.flags["C_CONTIGUOUS"]
+        B = tables.shape[0]
+        lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        newt = None if new_tokens is None else np.ascontiguousarray(new_tokens, dtype=np.int32)
+        first = np.empty(B, dtype=np.int32)
+        _check(_lib.kv_pool_prepare_append(self.handle, B, lens.ctypes.data,
+                                           None if newt is None else newt.ctypes.data,
+                                           tables.ctypes.data, tables.shape[1],
+                                           first.ctypes.data, _stream(stream)),
+               "kv_pool_prepare_append")
+        return first
 
     # ---- append (reshape_and_cache)
     def append(self, layer, k, v, tables, positions, k_scale=1.0, v_scale=1.0, stream=None):

@@ -219,3 +219,112 @@ def test_binding_argument_lists_match_the_header(pkv):
         kinds = [_c_kind(re.sub(r"\b\w+$", "", a).strip() or a) for a in args]
         got = [_ct_kind(t) for t in (getattr(lib, name).argtypes or [])]
         assert kinds == got, f"{name}: header {kinds} binding {got}"
+
+
+def _prep(pkv, p, lens, tables, new=None):
+    import numpy as np
+    lens = np.asarray(lens, np.int32)
+    first = np.full(len(lens), 77, np.int32)
+    newp = None
+    if new is not None:
+        new = np.asarray(new, np.int32)
+        newp = new.ctypes.data
+    rc = pkv.lib().kv_pool_prepare_append(p.h, len(lens), lens.ctypes.data, newp,
+                                          tables.ctypes.data, tables.shape[1],
+                                          first.ctypes.data, None)
+    return rc, first
+
+
+def test_prepare_append_takes_a_block_exactly_when_a_token_starts_one(pkv):
+    """The pages' append_token: a block is allocated when the new token's
+    position is a multiple of the block size (block size 16 here)."""
+    import numpy as np
+    p = FakePool(pkv, nb=20)
+    _, ids = p.alloc(2)
+    tables = np.full((4, 6), -1, np.int32)
+    tables[0, 0] = ids[0]                                 # 16 tokens: the next starts block 1
+    tables[1, 0] = ids[1]                                 # 5 tokens: room left in block 0
+    # sequences 2 and 3 hold no token yet: each needs its block 0
+    free0 = p.nfree()
+    rc, first = _prep(pkv, p, [16, 5, 0, 0], tables)
+    assert rc == 0
+    assert list(first) == [1, -1, 0, 0]
+    assert tables[1, 1] == -1 and tables[0, 0] == ids[0] and tables[1, 0] == ids[1]
+    new = [int(tables[0, 1]), int(tables[2, 0]), int(tables[3, 0])]
+    assert len(set(new) | set(ids)) == 5 and all(p.ref(i) == 1 for i in new)
+    assert p.nfree() == free0 - 3
+    p.close()
+
+
+def test_prepare_append_chunk_spans_several_blocks(pkv):
+    import numpy as np
+    p = FakePool(pkv, nb=20)
+    tables = np.full((2, 8), -1, np.int32)
+    _, ids = p.alloc(1)
+    tables[0, 0] = ids[0]
+    rc, first = _prep(pkv, p, [10, 0], tables, new=[40, 17])   # 10+40 -> 4 blocks; 17 -> 2
+    assert rc == 0 and list(first) == [1, 0]
+    assert (tables[0, :4] >= 0).all() and tables[0, 4] == -1
+    assert (tables[1, :2] >= 0).all() and tables[1, 2] == -1
+    assert p.nfree() == 20 - 1 - 3 - 2
+    # k = 0 changes nothing
+    before = tables.copy()
+    rc, first = _prep(pkv, p, [50, 17], tables, new=[0, 0])
+    assert rc == 0 and list(first) == [-1, -1] and np.array_equal(tables, before)
+    p.close()
+
+
+def test_prepare_append_is_all_or_nothing(pkv):
+    import numpy as np
+    p = FakePool(pkv, nb=5)
+    tables = np.full((3, 4), -1, np.int32)
+    rc, _ = _prep(pkv, p, [0, 0, 0], tables, new=[32, 32, 17])   # 2 + 2 + 2 > 5
+    assert rc == pkv.PKV_ENOMEM and p.nfree() == 5 and (tables == -1).all()
+    rc, _ = _prep(pkv, p, [0, 0, 0], tables, new=[65, 1, 1])     # 5 blocks > 4 entries
+    assert rc == pkv.PKV_EINVAL and p.nfree() == 5 and (tables == -1).all()
+    rc, _ = _prep(pkv, p, [-1, 0, 0], tables)
+    assert rc == pkv.PKV_EINVAL and p.nfree() == 5
+    rc, _ = _prep(pkv, p, [0, 0, 0], tables, new=[32, 32, 16])   # exactly 5
+    assert rc == 0 and p.nfree() == 0
+    p.close()
+
+
+def test_prepare_append_copy_of_a_shared_tail_is_planned_in_order(pkv):
+    """Two sequences share a partly filled tail block.  Without a device the
+    copy cannot be issued, so the call reports PKV_ECUDA and leaves pool and
+    tables exactly as they were (the copy itself is exercised on the GPU); a
+    shared *full* block needs no copy (the next token starts a new block)."""
+    import numpy as np
+    p = FakePool(pkv, nb=8)
+    _, ids = p.alloc(2)
+    p.call("kv_pool_share", ids)                          # both blocks shared by 2 tables
+    tables = np.full((2, 4), -1, np.int32)
+    tables[:, 0], tables[:, 1] = ids[0], ids[1]
+    before, free0 = tables.copy(), p.nfree()
+    rc, _ = _prep(pkv, p, [20, 20], tables)               # tail block ids[1] has room
+    assert rc == pkv.PKV_ECUDA
+    assert np.array_equal(tables, before) and p.nfree() == free0
+    assert p.ref(ids[1]) == 2
+    rc, first = _prep(pkv, p, [32, 32], tables)           # full: each starts a new block
+    assert rc == 0 and list(first) == [2, 2] and p.nfree() == free0 - 2
+    assert p.ref(ids[0]) == 2 and p.ref(ids[1]) == 2
+    # not enough blocks for the copy either: PKV_ENOMEM before any copy is tried
+    q = FakePool(pkv, nb=2)
+    _, qids = q.alloc(2)
+    q.call("kv_pool_share", qids[:1])
+    t2 = np.full((2, 2), -1, np.int32)
+    t2[:, 0] = qids[0]
+    rc, _ = _prep(pkv, q, [3, 3], t2)
+    assert rc == pkv.PKV_ENOMEM and q.ref(qids[0]) == 2
+    p.close()
+    q.close()
+
+
+def test_prepare_append_rejects_a_dead_tail_entry(pkv):
+    import numpy as np
+    p = FakePool(pkv, nb=4)
+    tables = np.full((1, 2), -1, np.int32)
+    tables[0, 0] = 3                                      # never taken: refcount 0
+    rc, _ = _prep(pkv, p, [5], tables)
+    assert rc == pkv.PKV_EINVAL and p.nfree() == 4 and tables[0, 0] == 3
+    p.close()
