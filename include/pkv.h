@@ -173,26 +173,36 @@ PKV_API int kv_append_tokens(pkv_pool* pool, int layer, const void* d_k, const v
                              const int32_t* d_positions, int64_t num_tokens, float k_scale,
                              float v_scale, cudaStream_t stream);
 
-/* Block-wise FP8 scaling ([UNLOCK] 3.2: one scale per 64-128 tokens), read as one
- * fp32 scale per pool block, K or V, layer and KV head.  d_scales is a
+/* Block-wise FP8 scaling ([UNLOCK] 3.2: one scale per 64-128 tokens).  Storage
+ * is one fp32 scale per pool block, K or V, layer and KV head: d_scales is a
  * caller-owned device array [num_blocks, 2, num_layers, num_kv_heads] of fp32
- * (16-byte aligned).  While it is attached to an E4M3 pool, kv_append,
- * kv_append_tokens, paged_decode_step and every decode call encode and
- * dequantise each tile with its own scale (x / scale stored, value x scale
- * read) and ignore their k_scale / v_scale arguments.  NULL detaches it.
+ * (16-byte aligned); a scale group spanning several blocks stores its scale in
+ * each of them (kv_block_scales).  While it is attached to an E4M3 pool,
+ * kv_append, kv_append_tokens, paged_decode_step and every decode call encode and
+ * dequantise each tile with its own slot's scale (x / scale stored, value x
+ * scale read) and ignore their k_scale / v_scale arguments.  NULL detaches it.
  * PKV_EINVAL for a pool that is not E4M3. */
 PKV_API int kv_pool_set_block_scales(pkv_pool* pool, float* d_scales);
-/* Set the attached block scales of every tile the given tokens land in (token
- * i: sequence d_seq_ids[i], or i when d_seq_ids is NULL, at d_positions[i]) to
- * amax / 448 over those tokens' elements of that tile (IEEE fp32 division;
- * amax = 0 gives 1); other tiles keep their scales.  Run it on the tokens that
- * fill a block before storing them (a prefill); a block's scale must not change
- * while it holds encoded tokens, so later appends into it reuse its scale and
- * values beyond 448 x scale saturate. */
+/* Compute the attached block scales of every scale group the given tokens land
+ * in (token i: sequence d_seq_ids[i], or i when d_seq_ids is NULL, at
+ * d_positions[i]).  A scale group is group_tokens consecutive positions of a
+ * sequence, [g x group_tokens, (g + 1) x group_tokens), a multiple of the block
+ * size (0: one block; the pages' reading is 64 or 128); groups of sequences that
+ * share their first block (a shared prefix) are one group.  Its scale is
+ * amax / 448 over those tokens' finite elements (IEEE fp32 division; amax = 0
+ * gives 1), written into the slot of every block of the group present in the
+ * table; other slots keep their scales.  Run it on the tokens that fill a group
+ * before storing them (a prefill): a group's scale must not change while it
+ * holds encoded tokens, so later appends into its blocks reuse the scale and
+ * values beyond 448 x scale saturate (a block taken later for a group's
+ * remaining positions needs its slot set to the group's scale, for example by
+ * this call over the group's tokens).  PKV_EINVAL for a group size that is not
+ * a positive multiple of the block size. */
 PKV_API int kv_block_scales(pkv_pool* pool, int layer, const void* d_k, const void* d_v,
                             pkv_dtype in_dtype, const int32_t* d_block_tables,
                             int max_blocks_per_seq, int batch, const int32_t* d_seq_ids,
-                            const int32_t* d_positions, int64_t num_tokens, cudaStream_t stream);
+                            const int32_t* d_positions, int64_t num_tokens, int group_tokens,
+                            cudaStream_t stream);
 
 /* Absolute maximum behind the per-tensor FP8 scale ([UNLOCK] 3.2): the largest
  * |x| over the finite elements of d_x (n elements of f32/f16/bf16; NaN and +-Inf

@@ -62,7 +62,7 @@ def lib() -> ctypes.CDLL:
             L.or_decode_mq.argtypes = [P, P, P, I, P, I, I, I, I, I, I, I, I, P, I, P, I, I,
                                        D, D, D, P]
             L.or_block_scales.restype = I
-            L.or_block_scales.argtypes = [P, I, I, I, I, I, I, P, P, I, P, I, I, P, P, LL]
+            L.or_block_scales.argtypes = [P, I, I, I, I, I, I, P, P, I, P, I, I, P, P, LL, I]
             L.or_append.restype = I
             L.or_append.argtypes = [P, I, I, I, I, I, I, I, P, P, I, P, I, P, I, F, F, P]
             L.or_append_tokens.restype = I
@@ -237,9 +237,12 @@ def append_tokens(pool, kv_dtype, geom, layer, k, v, in_dtype, tables, seq_ids, 
         raise ValueError(f"oracle append_tokens rejected its inputs (code {rc})")
 
 
-def block_scales(scales, geom, layer, k, v, in_dtype, tables, seq_ids, positions):
-    """[UNLOCK 3.2] per-block scales amax / 448 of the tiles these tokens land in,
-    written into `scales` ([NB, 2, L, Hkv] float32, modified in place)."""
+def block_scales(scales, geom, layer, k, v, in_dtype, tables, seq_ids, positions,
+                 group_tokens=0):
+    """[UNLOCK 3.2] block-wise scales amax / 448 of the scale groups (group_tokens
+    consecutive positions of a sequence; 0: one block) these tokens land in,
+    written into the slot of every block of each group (`scales`, [NB, 2, L, Hkv]
+    float32, modified in place)."""
     tables = _i32(tables)
     seq_ids = _i32(seq_ids)
     positions = _i32(positions)
@@ -248,7 +251,8 @@ def block_scales(scales, geom, layer, k, v, in_dtype, tables, seq_ids, positions
     rc = lib().or_block_scales(_f32(scales), geom["num_blocks"], geom["num_layers"],
                                geom["num_kv_heads"], geom["block_size"], geom["head_dim"], layer,
                                _ptr(k), _ptr(v), DT[in_dtype], _ptr(tables), tables.shape[1],
-                               tables.shape[0], _ptr(seq_ids), _ptr(positions), seq_ids.shape[0])
+                               tables.shape[0], _ptr(seq_ids), _ptr(positions), seq_ids.shape[0],
+                               int(group_tokens))
     if rc != 0:
         raise ValueError(f"oracle block_scales rejected its inputs (code {rc})")
 

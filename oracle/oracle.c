@@ -236,29 +236,42 @@ int or_append_tokens(void* pool, int kv_dtype, int NB, int L, int Hkv, int bs, i
 }
 
 /*
- * [UNLOCK 3.2] block-wise scaling, read as one fp32 scale per pool block (and per
- * K / V, layer and KV head): for every tile (blk, kv, layer, h) that the n tokens
- * land in, scale = fp32(amax over those tokens' elements) / 448 in IEEE single
- * precision (amax 0 -> 1).  Tiles no token lands in are left unchanged.
- * scales: [NB, 2, L, Hkv] fp32.  Returns 0 or -2 (a token out of range).
+ * [UNLOCK 3.2] block-wise scaling: one fp32 scale per group of group_tokens
+ * consecutive token positions of a sequence (the page: one scale per 64-128
+ * tokens), per K / V, layer and KV head.  group_tokens is a multiple of bs (0
+ * means bs: one scale per block).  A paged pool scatters a group's blocks, so
+ * the group's scale is stored in the scale slot of every one of its blocks
+ * ([NB, 2, L, Hkv] fp32, the same layout as per-block scales).
+ * For every group that the n tokens land in: scale = fp32(amax over those
+ * tokens' finite elements) / 448 in IEEE single precision (amax 0 -> 1),
+ * written to every block of the group present in the table.  A group is named
+ * by its first block (entry pos / group_tokens * group_tokens / bs of the
+ * table); groups of several sequences with the same first block (a shared
+ * prefix) are one group.  Slots of other blocks are left unchanged.
+ * Returns 0, -1 (group size) or -2 (a token, or its group's first block, out of range).
  */
 int or_block_scales(float* scales, int NB, int L, int Hkv, int bs, int D, int layer,
                     const void* k, const void* v, int in_dtype, const int32_t* tables,
                     int max_blocks, int B, const int32_t* seq_ids, const int32_t* positions,
-                    long long n) {
+                    long long n, int group_tokens) {
+  const int S = group_tokens == 0 ? bs : group_tokens;
+  if (S < bs || S % bs != 0) return -1;
+  const int per = S / bs;                            /* blocks per group */
   size_t tiles = (size_t)NB * 2 * L * Hkv;
   double* amax = (double*)calloc(tiles, sizeof(double));
   char* touched = (char*)calloc(tiles, 1);
   if (!amax || !touched) { free(amax); free(touched); return -3; }
+  /* amax per group, kept in the tile of the group's first block */
   for (long long i = 0; i < n; ++i) {
     int s = seq_ids[i], pos = positions[i];
     if (pos < 0) continue;
     if (s < 0 || s >= B || pos / bs >= max_blocks) { free(amax); free(touched); return -2; }
     int blk = tables[(size_t)s * max_blocks + pos / bs];
-    if (blk < 0 || blk >= NB) { free(amax); free(touched); return -2; }
+    int lead = tables[(size_t)s * max_blocks + (pos / S) * per];
+    if (blk < 0 || blk >= NB || lead < 0 || lead >= NB) { free(amax); free(touched); return -2; }
     for (int kv = 0; kv < 2; ++kv)
       for (int h = 0; h < Hkv; ++h) {
-        size_t tile = (((size_t)blk * 2 + kv) * L + layer) * Hkv + h;
+        size_t tile = (((size_t)lead * 2 + kv) * L + layer) * Hkv + h;
         touched[tile] = 1;
         for (int d = 0; d < D; ++d) {
           double x = fabs(or_load(kv ? v : k, ((size_t)i * Hkv + h) * D + d, in_dtype));
@@ -266,8 +279,22 @@ int or_block_scales(float* scales, int NB, int L, int Hkv, int bs, int D, int la
         }
       }
   }
-  for (size_t t = 0; t < tiles; ++t)
-    if (touched[t]) scales[t] = or_fp8_scale(amax[t]);
+  /* the group's scale into the slot of every block of the group */
+  for (long long i = 0; i < n; ++i) {
+    int s = seq_ids[i], pos = positions[i];
+    if (pos < 0) continue;
+    int e0 = (pos / S) * per;
+    int lead = tables[(size_t)s * max_blocks + e0];
+    for (int e = e0; e < e0 + per && e < max_blocks; ++e) {
+      int blk = tables[(size_t)s * max_blocks + e];
+      if (blk < 0 || blk >= NB) continue;
+      for (int kv = 0; kv < 2; ++kv)
+        for (int h = 0; h < Hkv; ++h) {
+          size_t lt = (((size_t)lead * 2 + kv) * L + layer) * Hkv + h;
+          scales[(((size_t)blk * 2 + kv) * L + layer) * Hkv + h] = or_fp8_scale(amax[lt]);
+        }
+    }
+  }
   free(amax);
   free(touched);
   return 0;

@@ -60,17 +60,23 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
   }
 }
 
-// Tile of token `tok` for (kv, h), or -1 when the token is skipped / out of range.
+// Scale group of token `tok`: a.group_tokens consecutive positions of its
+// sequence (a multiple of the block size), named by its first block.  Returns
+// the tile of that first block for (kv, h), or -1 when the token is skipped or
+// out of range.
 __device__ __forceinline__ long long tile_of(const AppendArgs& a, long long tok, int kv, int h) {
   const int s = a.seq_ids ? __ldg(a.seq_ids + tok) : (int)tok;
   const int pos = __ldg(a.positions + tok);
   if (pos < 0 || s < 0 || s >= a.B || pos / a.BS >= a.max_blocks) return -1;
   const int blk = __ldg(a.tables + (size_t)s * a.max_blocks + pos / a.BS);
-  if (blk < 0 || blk >= a.num_blocks) return -1;
-  return (((long long)blk * 2 + kv) * a.L + a.layer) * a.Hkv + h;
+  const int lead = __ldg(a.tables + (size_t)s * a.max_blocks +
+                         (pos / a.group_tokens) * (a.group_tokens / a.BS));
+  if (blk < 0 || blk >= a.num_blocks || lead < 0 || lead >= a.num_blocks) return -1;
+  return (((long long)lead * 2 + kv) * a.L + a.layer) * a.Hkv + h;
 }
 
-// Block-wise scales, pass 1: mark every tile the tokens land in with -0.0.
+// Block-wise scales, pass 1: mark the tile of every group the tokens land in
+// (its first block's) with -0.0.
 __global__ void __launch_bounds__(256) scales_mark_kernel(const AppendArgs a, float* scales) {
   const long long total = a.num_tokens * 2 * a.Hkv;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
@@ -103,7 +109,8 @@ __global__ void __launch_bounds__(256) scales_amax_kernel(const AppendArgs a, fl
   }
 }
 
-// Pass 3: every tile holding -amax becomes amax / 448 (IEEE fp32 division; amax 0 -> 1).
+// Pass 3: every tile holding -amax becomes amax / 448 (IEEE fp32 division;
+// amax 0 -> 1); pass 4 copies it to the group's other blocks.
 __global__ void __launch_bounds__(256) scales_finish_kernel(float* scales, long long tiles) {
   for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < tiles;
        t += (long long)gridDim.x * blockDim.x) {
@@ -112,6 +119,30 @@ __global__ void __launch_bounds__(256) scales_finish_kernel(float* scales, long 
       const float amax = __uint_as_float(u & 0x7fffffffu);
       scales[t] = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
     }
+  }
+}
+
+// Pass 4 (groups of several blocks): every block of a token's group takes the
+// scale of the group's first block.  Tokens of one group write the same value.
+__global__ void __launch_bounds__(256) scales_spread_kernel(const AppendArgs a, float* scales) {
+  const int per = a.group_tokens / a.BS;
+  const long long total = a.num_tokens * 2 * a.Hkv * (per - 1);
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int m = 1 + (int)(i % (per - 1));             // member of the group after the first
+    long long r = i / (per - 1);
+    const int h = (int)(r % a.Hkv);
+    r /= a.Hkv;
+    const int kv = (int)(r % 2);
+    const long long tok = r / 2;
+    const long long lt = tile_of(a, tok, kv, h);
+    if (lt < 0) continue;
+    const int s = a.seq_ids ? __ldg(a.seq_ids + tok) : (int)tok;
+    const int e = (__ldg(a.positions + tok) / a.group_tokens) * per + m;
+    if (e >= a.max_blocks) continue;
+    const int blk = __ldg(a.tables + (size_t)s * a.max_blocks + e);
+    if (blk < 0 || blk >= a.num_blocks) continue;        // not allocated yet
+    scales[(((long long)blk * 2 + kv) * a.L + a.layer) * a.Hkv + h] = scales[lt];
   }
 }
 
@@ -189,9 +220,16 @@ cudaError_t launch_block_scales(const AppendArgs& a, float* scales, cudaStream_t
   }
   scales_finish_kernel<<<(int)std::min<long long>((tiles + 255) / 256, 1LL << 16), 256, 0,
                          stream>>>(scales, tiles);
+  const int per = a.group_tokens / a.BS;
+  const bool spread = a.num_tokens > 0 && per > 1;
+  if (spread) {
+    const long long t4 = a.num_tokens * 2 * a.Hkv * (per - 1);
+    scales_spread_kernel<<<(int)std::min<long long>((t4 + 255) / 256, 1LL << 16), 256, 0,
+                           stream>>>(a, scales);
+  }
   const cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess)
-    for (int i = 0; i < (a.num_tokens > 0 ? 3 : 1); ++i) count_launch();
+    for (int i = 0; i < (a.num_tokens > 0 ? 3 : 1) + (spread ? 1 : 0); ++i) count_launch();
   return e;
 }
 

@@ -105,9 +105,11 @@ struct AppendArgs {
   int in_dtype, kv_dtype;
   float k_scale, v_scale;
   const float* block_scales;  // E4M3 per-tile scales [NB, 2, L, Hkv], or nullptr (per-tensor)
+  int group_tokens;           // block-wise scales: positions per scale group (a multiple of BS)
 };
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
-// Per-tile E4M3 scales amax / 448 of the tiles the tokens land in (three launches).
+// E4M3 block-wise scales amax / 448 of the scale groups the tokens land in, stored
+// in every block of each group (three launches, four for groups of several blocks).
 cudaError_t launch_block_scales(const AppendArgs& a, float* scales, cudaStream_t stream);
 cudaError_t launch_absmax(const void* x, int dtype, int64_t n, float* amax, cudaStream_t stream);
 // scale = max(amax[0..n)) / 448 (1 when that is 0), one thread block.

@@ -525,10 +525,12 @@ int kv_pool_set_block_scales(pkv_pool* p, float* d_scales) {
 int kv_block_scales(pkv_pool* p, int layer, const void* d_k, const void* d_v, pkv_dtype in_dtype,
                     const int32_t* d_block_tables, int max_blocks_per_seq, int batch,
                     const int32_t* d_seq_ids, const int32_t* d_positions, int64_t num_tokens,
-                    cudaStream_t stream) {
+                    int group_tokens, cudaStream_t stream) {
   if (!p || !p->d_block_scales || layer < 0 || layer >= p->g.num_layers || num_tokens < 0 ||
       batch < 0 || !act_dtype(in_dtype))
     return PKV_EINVAL;
+  if (group_tokens == 0) group_tokens = p->g.block_size;
+  if (group_tokens < p->g.block_size || group_tokens % p->g.block_size != 0) return PKV_EINVAL;
   if (num_tokens > 0 &&
       (!d_k || !d_v || !d_block_tables || !d_positions || max_blocks_per_seq < 1 || batch < 1))
     return PKV_EINVAL;
@@ -549,6 +551,7 @@ int kv_block_scales(pkv_pool* p, int layer, const void* d_k, const void* d_v, pk
   a.num_blocks = p->g.num_blocks;
   a.in_dtype = in_dtype;
   a.kv_dtype = p->g.kv_dtype;
+  a.group_tokens = group_tokens;
   return launch_block_scales(a, p->d_block_scales, stream) == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 

@@ -73,7 +73,7 @@ def _load() -> ctypes.CDLL:
         "kv_absmax": (I, [P, I, I64, P, P]),
         "kv_fp8_scale": (I, [P, I, P, P]),
         "kv_pool_set_block_scales": (I, [P, P]),
-        "kv_block_scales": (I, [P, I, P, P, I, P, I, I, P, P, I64, P]),
+        "kv_block_scales": (I, [P, I, P, P, I, P, I, I, P, P, I64, I, P]),
         "paged_decode_workspace_bytes": (Z, [G, I, I, I]),
         "paged_decode_workspace_bytes_mq": (Z, [G, I, I, I, I]),
         "paged_decode_attention_mq": (I, [P, I, P, I, I, P, I, P, I, P, I, I, F, F, F, I, P, Z,
@@ -268,11 +268,14 @@ class KVPool:
         self.block_scales = scales
         _check(_lib.kv_pool_set_block_scales(self.handle, _ptr(scales)), "kv_pool_set_block_scales")
 
-    def compute_block_scales(self, layer, k, v, tables, seq_ids, positions, stream=None):
+    def compute_block_scales(self, layer, k, v, tables, seq_ids, positions, group_tokens=0,
+                             stream=None):
+        """Block-wise scales of the scale groups (group_tokens positions; 0: one
+        block) the tokens land in, into the attached scale array."""
         _check(_lib.kv_block_scales(self.handle, layer, _ptr(k), _ptr(v), TORCH_CODE[k.dtype],
                                     _ptr(tables), tables.shape[1], tables.shape[0],
                                     _ptr(seq_ids), _ptr(positions), positions.shape[0],
-                                    _stream(stream)), "kv_block_scales")
+                                    group_tokens, _stream(stream)), "kv_block_scales")
 
     def check_status(self, stream=None) -> int:
         return int(_lib.pkv_check_status(self.handle, _stream(stream)))

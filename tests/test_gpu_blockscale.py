@@ -1,5 +1,7 @@
-"""Block-wise E4M3 scales (needs a GPU): one fp32 scale per pool block, K/V,
-layer and KV head.  Scales and pool bytes are bit-exact with the oracle; decode
+"""Block-wise E4M3 scales (needs a GPU): one fp32 scale per scale group of a
+sequence's positions, K/V, layer and KV head, stored in each of the group's
+blocks -- one block, or the pages' 64 and 128 tokens ("Unlocking long context"
+section 3.2).  Scales and pool bytes are bit-exact with the oracle; decode
 results match the oracle (dequantising the same bytes with the same scales)
 within 5e-3 x max|V|."""
 import numpy as np
@@ -14,7 +16,7 @@ from tests.helpers import np_raw
 pytestmark = pytest.mark.gpu
 
 
-def _setup(case):
+def _setup(case, group=0):
     from paged_kv_cache_215_gb300 import pkv
     tens = wl.make_tensors(case)
     dev = "cuda"
@@ -36,13 +38,13 @@ def _setup(case):
     pos = torch.cat([tens.tok_pos, tens.new_pos]).to(dev)
     k_all = torch.cat([tens.k_tokens, tens.k_new]).to(dev)
     v_all = torch.cat([tens.v_tokens, tens.v_new]).to(dev)
-    pool.compute_block_scales(case.layer, k_all, v_all, tables, seq, pos)
+    pool.compute_block_scales(case.layer, k_all, v_all, tables, seq, pos, group_tokens=group)
     pool.append_tokens(case.layer, tens.k_tokens.to(dev), tens.v_tokens.to(dev), tables,
                        tens.tok_seq.to(dev), tens.tok_pos.to(dev))
     # oracle side
     osc = np.full(tuple(scales.shape), 7.0, np.float32)
     oracle.block_scales(osc, case.geometry, case.layer, np_raw(k_all), np_raw(v_all), "bf16",
-                        case.tables, np_raw(seq), np_raw(pos))
+                        case.tables, np_raw(seq), np_raw(pos), group)
     opool = np.zeros(pool.nbytes, np.uint8)
     oracle.append_tokens(opool, "e4m3", case.geometry, case.layer, np_raw(k_all), np_raw(v_all),
                          "bf16", case.tables, np_raw(seq), np_raw(pos), block_scales=osc)
@@ -59,9 +61,13 @@ CASES = [
 ]
 
 
+GROUPS = [0, 64, 128]
+
+
+@pytest.mark.parametrize("group", GROUPS, ids=lambda g: f"group{g}")
 @pytest.mark.parametrize("case", CASES, ids=lambda c: c.name)
-def test_block_scales_and_pool_bit_exact(case):
-    tens, pool, scales, tables, lens, osc, opool = _setup(case)
+def test_block_scales_and_pool_bit_exact(case, group):
+    tens, pool, scales, tables, lens, osc, opool = _setup(case, group)
     pool.append(case.layer, tens.k_new.cuda(), tens.v_new.cuda(), tables, tens.new_pos.cuda())
     torch.cuda.synchronize()
     assert np.array_equal(scales.cpu().numpy(), osc)
@@ -69,11 +75,12 @@ def test_block_scales_and_pool_bit_exact(case):
     assert pool.check_status() == 0
 
 
+@pytest.mark.parametrize("group", GROUPS, ids=lambda g: f"group{g}")
 @pytest.mark.parametrize("mode", ["auto", "simt", "split3", "fused", "mq2", "mq40", "cascade"])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: c.name)
-def test_block_scaled_decode_parity(case, mode):
+def test_block_scaled_decode_parity(case, mode, group):
     from paged_kv_cache_215_gb300 import pkv
-    tens, pool, scales, tables, lens, osc, opool = _setup(case)
+    tens, pool, scales, tables, lens, osc, opool = _setup(case, group)
     q = tens.q.cuda()
     maxlen = int(case.seq_lens.max())
     if mode in ("mq2", "mq40"):
@@ -132,3 +139,18 @@ def test_block_scaled_decode_parity(case, mode):
         vmax = np.abs(dec[blocks, 1, case.layer]).max()
         err = np.abs(got[s] - ref[s]).max()
         assert err <= TOL["e4m3"] * vmax, f"{case.name} {mode} seq {s}: {err}"
+
+
+@pytest.mark.parametrize("group", [64, 128])
+def test_every_block_of_a_group_holds_its_scale(group):
+    """A 64- or 128-token group at block size 16 spans 4 or 8 scattered blocks:
+    every one of them holds the group's scale (read back from the device)."""
+    case = CASES[1]                                          # block size 16
+    tens, pool, scales, tables, lens, osc, opool = _setup(case, group)
+    got = scales.cpu().numpy()
+    per = group // case.block_size
+    for s in range(case.batch):
+        nb = (int(case.seq_lens[s]) + case.block_size - 1) // case.block_size
+        for e0 in range(0, nb, per):
+            blocks = case.tables[s, e0:min(e0 + per, nb)]
+            assert np.all(got[blocks] == got[blocks[0]]), (s, e0)

@@ -447,7 +447,7 @@ def test_multi_token_decode_with_one_token_is_single_query_decode():
 
 
 # --------------------------------------------------------------------------- block-wise FP8 scales
-def _bs_setup(case, tens):
+def _bs_setup(case, tens, group_tokens=0):
     geom = case.geometry
     nb = case.num_blocks
     scales = np.zeros((nb, 2, case.num_layers, case.num_kv_heads), np.float32)
@@ -455,7 +455,8 @@ def _bs_setup(case, tens):
     pos = np.concatenate([np_raw(tens.tok_pos), np_raw(tens.new_pos)])
     k = np.concatenate([np_raw(tens.k_tokens), np_raw(tens.k_new)])
     v = np.concatenate([np_raw(tens.v_tokens), np_raw(tens.v_new)])
-    oracle.block_scales(scales, geom, case.layer, k, v, "bf16", case.tables, seq, pos)
+    oracle.block_scales(scales, geom, case.layer, k, v, "bf16", case.tables, seq, pos,
+                        group_tokens)
     pool = np.zeros(oracle.kv_bytes(case.num_layers, case.num_kv_heads, case.head_dim,
                                     nb * case.block_size, 1), np.uint8)
     oracle.append_tokens(pool, "e4m3", geom, case.layer, k, v, "bf16", case.tables, seq, pos,
@@ -530,3 +531,66 @@ def test_block_scales_are_more_accurate_than_one_scale_on_spiky_keys():
     blockwise, _, _ = oracle.decode(np_raw(tens.q), "bf16", pool, "e4m3", case.geometry, 0,
                                     case.tables, case.seq_lens, case.scale, block_scales=scales)
     assert np.abs(blockwise - exact).max() < np.abs(per_tensor - exact).max()
+
+
+# --------------------------------------------------------------------------- scale groups
+def _groups(case, S):
+    """(sequence, first entry, entries) of every scale group of S tokens."""
+    bs = case.block_size
+    out = []
+    for sq in range(case.batch):
+        n = int(case.seq_lens[sq])
+        for e0 in range(0, (n + bs - 1) // bs, S // bs):
+            out.append((sq, e0, case.tables[sq, e0:min(e0 + S // bs, (n + bs - 1) // bs)]))
+    return out
+
+
+@pytest.mark.parametrize("S", [64, 128])
+def test_scale_groups_share_one_scale_and_store_their_max_at_448(S):
+    """One scale per S tokens ("Unlocking long context" section 3.2, 64-128
+    tokens): every block of a group holds the same scale, and the group's
+    largest element encodes to the largest E4M3 code, in K and in V."""
+    case = wl.make_case(f"grp{S}", [700, 333, 64, 1], 8, 2, 32, 16, "e4m3", "bf16", "bf16",
+                        seed=140, spike_frac=0.01)
+    tens = wl.make_tensors(case)
+    scales, pool = _bs_setup(case, tens, S)
+    codes = pool.reshape(case.num_blocks, 2, 1, 2, 16, 32)
+    for sq, e0, blocks in _groups(case, S):
+        for kv in range(2):
+            for h in range(2):
+                sc = scales[blocks, kv, 0, h]
+                assert np.all(sc == sc[0]) and sc[0] > 0, (sq, e0, kv, h)
+                n = int(case.seq_lens[sq])
+                toks = codes[blocks, kv, 0, h].reshape(-1, 32)[:n - e0 * 16]
+                assert np.any((toks == 0x7E) | (toks == 0xFE)), (sq, e0, kv, h)
+
+
+def test_scale_groups_nest_and_reduce_to_per_block_scales():
+    """Scale groups of 128 tokens are the larger of their two 64-token halves'
+    scales (the maximum commutes with the correctly rounded division), and
+    groups of one block (S = block size, or 0) are the per-block scales."""
+    case = wl.make_case("grp_nest", [1000, 129, 300], 8, 2, 32, 16, "e4m3", "bf16", "bf16",
+                        seed=141, spike_frac=0.01)
+    tens = wl.make_tensors(case)
+    s64, _ = _bs_setup(case, tens, 64)
+    s128, _ = _bs_setup(case, tens, 128)
+    for sq, e0, blocks in _groups(case, 128):
+        lo, hi = blocks[:4], blocks[4:]
+        want = s64[lo[0]] if hi.size == 0 else np.maximum(s64[lo[0]], s64[hi[0]])
+        for b in blocks:
+            assert np.array_equal(s128[b], want), (sq, e0)
+    s16, _ = _bs_setup(case, tens, 16)
+    s0, _ = _bs_setup(case, tens, 0)
+    assert np.array_equal(s16, s0)
+    # one block per group is the per-block result: each block's largest value at 448
+    used = sorted({int(b) for b in case.tables[case.tables >= 0]})
+    assert np.array_equal(s16[used], s0[used])
+
+
+def test_scale_group_size_must_be_a_multiple_of_the_block_size():
+    case = wl.make_case("grp_bad", [40], 8, 2, 32, 16, "e4m3", "bf16", "bf16", seed=142)
+    tens = wl.make_tensors(case)
+    with pytest.raises(ValueError):
+        _bs_setup(case, tens, 24)
+    with pytest.raises(ValueError):
+        _bs_setup(case, tens, 8)
