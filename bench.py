@@ -47,7 +47,8 @@ SECONDARY = ["llama8b_b32_8k", "long_1m", "fp8_b8_32k", "llama70b_prefix_bs16",
              "llama70b_prefix_bs32", "long_128k_bs64", "llama8b_b32_8k_layers4"]
 MODEL_LAYERS = {"long_128k": 32, "long_1m": 32, "llama8b_b32_8k": 32, "fp8_b8_32k": 32,
                 "llama70b_prefix_bs16": 80, "llama70b_prefix_bs32": 80, "long_128k_bs64": 32,
-                "llama8b_b32_8k_layers4": 32}
+                "llama8b_b32_8k_layers4": 32, "llama70b_prefix_small": 80,
+                "shared_prefix_64k_b32": 32, "tiny": 1}
 KERNEL_SOURCES = ["paged_kv_cache_215_gb300/csrc/decode_mma.cu",
                   "paged_kv_cache_215_gb300/csrc/decode_mma.cuh",
                   "paged_kv_cache_215_gb300/csrc/decode_mma_bf16.cu",
@@ -918,6 +919,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the chunked-prefill (tcgen05) case and print its JSON")
+    ap.add_argument("--cascade-only", action="store_true",
+                    help="time only the shared-prefix decode workloads and print their JSON")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -928,6 +931,13 @@ def main():
         build.build()
         for kv in ("bf16", "e4m3"):
             print(json.dumps(measure_chunked_prefill("cuda", steps=args.steps, kv=kv)), flush=True)
+    elif args.cascade_only:
+        from paged_kv_cache_215_gb300 import build
+        build.build()
+        names = CASCADE if args.workload == PRIMARY else [args.workload]
+        for cname in names:
+            r = measure_cascade(cname, "cuda", steps=args.steps)
+            print(json.dumps({"workload": f"{cname}_shared_prefix_decode", **r}), flush=True)
     else:
         run_ours(args)
 

@@ -59,6 +59,9 @@ struct DecodeArgs {
   // row (split * q_len + i) * Hq + head.
   const int32_t* key_limit;
   float* out_lse;
+  // with key_limit and a single query tile: the CTA's two tile slots take
+  // alternate key tiles of the split and write partials 2 x split + slot
+  int kv_interleave;
 };
 
 // Shared memory the tensor-core kernel needs for one CTA.

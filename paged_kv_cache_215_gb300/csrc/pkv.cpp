@@ -847,7 +847,8 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
 // decode's own workspace.
 struct CascadeWs {
   size_t n_off, lens_off, tab_off, o_off, lse_off, dec_off, bytes;
-  int S;
+  int S;          // key splits of the prefix pass
+  int parts;      // prefix partials per row: S, or 2S when one query tile's two slots split keys
 };
 static CascadeWs cascade_ws(const pkv_geometry& g, int batch, int max_blocks, int prefix_len_max,
                             int sms, size_t decode_bytes) {
@@ -856,16 +857,23 @@ static CascadeWs cascade_ws(const pkv_geometry& g, int batch, int max_blocks, in
   const int qtiles = (batch * G + 127) / 128;           // 128-row query tiles of the prefix pass
   const int ctas = ((qtiles + 1) / 2) * g.num_kv_heads;  // CTAs per key split
   const int ktiles = (prefix_len_max + 63) / 64;
-  int S = ctas > 0 ? (sms + ctas - 1) / ctas : 1;        // about one wave of CTAs
+  // as many key splits as keep every CTA in the first wave (one CTA per SM: the
+  // kernel takes the SM's shared and tensor memory); a second, partial wave
+  // would double the pass's time
+  int S = ctas > 0 ? std::max(1, sms / ctas) : 1;
   S = std::max(1, std::min(S, std::min(std::max(ktiles, 1), 64)));
   w.S = S;
+  // (a single query tile could let both tile slots take alternate key tiles,
+  // writing 2S partials; measured slower on the 64K shared document -- the pass is
+  // bound by the TMA box rate, not by the softmax -- so one partial per split)
+  w.parts = S;
   const size_t rows = (size_t)batch * g.num_q_heads;
   w.n_off = 0;
   w.lens_off = 256;
   w.tab_off = w.lens_off + align256((size_t)batch * 4);
   w.o_off = w.tab_off + align256((size_t)batch * max_blocks * 4);
-  w.lse_off = w.o_off + align256((size_t)S * rows * g.head_dim * 4);
-  w.dec_off = w.lse_off + align256((size_t)S * rows * 4);
+  w.lse_off = w.o_off + align256((size_t)w.parts * rows * g.head_dim * 4);
+  w.dec_off = w.lse_off + align256((size_t)w.parts * rows * 4);
   w.bytes = w.dec_off + decode_bytes;
   return w;
 }
@@ -984,6 +992,7 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
     t.q_len = batch;
     t.R = G * batch;
     t.S = w.S;
+    t.kv_interleave = w.parts == 2 * w.S ? 1 : 0;
     // E4M3: per-tensor scales on the softmax scale and the partial O (as the
     // decode kernel's partials carry them), per-block ones in the tile conversion
     t.qk_scale_log2 = (float)((double)scale * 1.4426950408889634 * (double)k_scale);
@@ -993,7 +1002,7 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
   }
   // 3. the private suffixes, merged with the prefix partials
   if (phase == 1) return PKV_OK;
-  const ExtPartials ext{ext_o, ext_lse, prefix_len_max > 0 ? w.S : 0};
+  const ExtPartials ext{ext_o, ext_lse, prefix_len_max > 0 ? w.parts : 0};
   return decode_common(d_out, out_dtype, d_q, q_dtype, 1, nullptr, nullptr, 0, pool, layer, suf_tab,
                        max_blocks_per_seq, suf_lens, batch, max_seq_len, scale, k_scale, v_scale, 0,
                        ws + w.dec_off, ws_bytes - w.dec_off, nullptr, stream, &ext);

@@ -164,6 +164,12 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
   // blockIdx.z cuts the key range into a.S splits
   const bool casc = a.key_limit != nullptr;
   const int hkv = blockIdx.y, s = casc ? 0 : blockIdx.z, split = casc ? blockIdx.z : 0;
+  // Shared-prefix mode with a single query tile: both tile slots hold the same
+  // query rows and take alternate key tiles (slot t: local tiles j = t mod 2),
+  // each with its own O, running max and sum; each writes its own partial
+  // (partial index 2 x split + t) for the merge.  This keeps both softmax
+  // warpgroups and both issuer pairs busy on one query tile.
+  const bool ilv = casc && a.kv_interleave != 0;
   const int G = a.G, QT = kM / G;                 // query tokens per query tile
 
   int n = __ldg(a.seq_lens + s);
@@ -173,20 +179,32 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
     n = n < 0 ? 0 : cap;
   }
   // key tiles jt0 .. jt0 + T - 1 of the sequence; local tile j is global tile jt0 + j
-  int tiles[kQT], jt0 = 0;
+  int tiles[kQT], jt0 = 0;                        // key tiles each slot computes
+  int T = 0;                                      // key tiles the CTA loads
   if (casc) {
     const int nt = (n + kN - 1) / kN;
     jt0 = (int)((long long)split * nt / a.S);
     const int jt1 = (int)((long long)(split + 1) * nt / a.S);
+    if (ilv) {
+      T = jt1 - jt0;
+      tiles[0] = (T + 1) / 2;
+      tiles[1] = T / 2;
+    } else {
 #pragma unroll
-    for (int t = 0; t < kQT; ++t) tiles[t] = (blockIdx.x * kQT + t) * QT < a.q_len ? jt1 - jt0 : 0;
+      for (int t = 0; t < kQT; ++t)
+        tiles[t] = (blockIdx.x * kQT + t) * QT < a.q_len ? jt1 - jt0 : 0;
+    }
   } else {
 #pragma unroll
     for (int t = 0; t < kQT; ++t) tiles[t] = key_tiles(a, n, blockIdx.x * kQT + t);
   }
-  int T = 0;                                      // key tiles the CTA loads
+  if (!ilv) {
 #pragma unroll
-  for (int t = 0; t < kQT; ++t) T = max(T, tiles[t]);
+    for (int t = 0; t < kQT; ++t) T = max(T, tiles[t]);
+  }
+  // does slot t compute loaded tile j, and as which of its own tiles
+  auto owns = [&](int t, int j) { return ilv ? (j & 1) == t : j < tiles[t]; };
+  auto local = [&](int j) { return ilv ? j >> 1 : j; };
   // the sequence's last key tile, if it is ragged and this CTA reads it (local index)
   const int jg_tail = (n % kN != 0) ? (n - 1) / kN : -1;
   const int j_tail = (jg_tail >= jt0 && jg_tail < jt0 + T) ? jg_tail - jt0 : -1;
@@ -223,7 +241,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
   int q_e = 0;
   if (warp < kSoftmaxWarps) {
     const int t = warp / 4, r = tid - 128 * t, i = r / G, g = r % G;
-    const int tok = (blockIdx.x * kQT + t) * QT + i;
+    const int tok = (blockIdx.x * kQT + (ilv ? 0 : t)) * QT + i;
     const bool live = tok < a.q_len;
     const size_t qrow = ((size_t)s * a.q_len + tok) * a.Hq + (size_t)hkv * G + g;
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) +
@@ -535,19 +553,22 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
         const uint64_t qb = d_k + ((kSmemQ + t * 2 * kHalf) >> 4);
         for (int j = 0; j < T && ok; ++j) {
           ok = wait(&bars->kv_full[j % kStages], (j / kStages) & 1);
-          // S_tj overwrites the TMEM buffer of P_t,j-2: its P V must have read it
-          if (ok && j < tiles[t] && j >= 2) ok = wait(&bars->p_free[t][j & 1], ((j - 2) >> 1) & 1);
+          const bool mine = owns(t, j);
+          const int jl = local(j);
+          // S_tj overwrites the TMEM buffer of the slot's P two tiles back: its P V
+          // must have read it
+          if (ok && mine && jl >= 2) ok = wait(&bars->p_free[t][jl & 1], ((jl - 2) >> 1) & 1);
           if (!ok) break;
           tc_fence_after();
-          if (j < tiles[t] && leader) {
+          if (mine && leader) {
             const uint64_t kb = d_k + ((kSmemKV + (j % kStages) * kStageBytes) >> 4);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               const uint32_t off = ((k >> 2) * kHalf + (k & 3) * 32) >> 4;
               const uint32_t offk = ((k >> 2) * kKVHalf + (k & 3) * 32) >> 4;
-              tc_mma_f16(tmem + t * 256 + (j & 1) * kN, qb + off, kb + offk, id_s, k > 0);
+              tc_mma_f16(tmem + t * 256 + (jl & 1) * kN, qb + off, kb + offk, id_s, k > 0);
             }
-            tc_commit(&bars->s_full[t][j & 1]);
+            tc_commit(&bars->s_full[t][jl & 1]);
           }
           if (leader) tc_commit(&bars->kv_empty[j % kStages]);  // S_tj has read K_j
           __syncwarp();
@@ -558,9 +579,10 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
           // paces this warp's releases: its arrival for the stage's next tile can
           // only follow that tile's load, which follows this tile's release
           ok = wait(&bars->kv_full[j % kStages], (j / kStages) & 1);
-          if (ok && j < tiles[t]) {
-            const int b = j & 1;
-            ok = wait(&bars->p_full[t][b], (j >> 1) & 1);
+          const int jl = local(j);
+          if (ok && owns(t, j)) {
+            const int b = jl & 1;
+            ok = wait(&bars->p_full[t][b], (jl >> 1) & 1);
             if (!kFp8 && ok && j == j_tail) ok = wait(&bars->v_zeroed, 0);
             if (!ok) break;
             tc_fence_after();
@@ -570,12 +592,12 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
 #pragma unroll
               for (int k = 0; k < 4; ++k) {                     // 16 keys (8 columns of P) per MMA
                 tc_mma_f16_ts(tmem + t * 256 + 128, pa + k * 8, vb + k * 128, id_o,
-                              (j > 0 || k > 0) ? 1u : 0u);
+                              (jl > 0 || k > 0) ? 1u : 0u);
                 if (kSplitP) tc_mma_f16_ts(tmem + t * 256 + 128, pa + 32 + k * 8, vb + k * 128, id_o, 1u);
               }
               tc_commit(&bars->o_done[t]);
               tc_commit(&bars->p_free[t][b]);
-              if (j == tiles[t] - 1) tc_commit(&bars->o_final[t]);
+              if (jl == tiles[t] - 1) tc_commit(&bars->o_final[t]);
             }
           }
           if (!ok) break;
@@ -592,7 +614,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
   } else {
     // ------------------------------------------------------------ softmax, one row per thread
     const int t = warp / 4, r = tid - 128 * t, i = r / G, g = r % G;
-    const int tok = (blockIdx.x * kQT + t) * QT + i;
+    const int tok = (blockIdx.x * kQT + (ilv ? 0 : t)) * QT + i;
     const bool live = tok < a.q_len;
     // this query's last visible key: causal within the chunk, or its prefix length
     const int pos = casc ? (live ? __ldg(a.key_limit + tok) : 0) - 1 : n - a.q_len + tok;
@@ -620,8 +642,9 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
     }
     const int32_t* trow = a.tables + (size_t)s * a.max_blocks;
     const int nblk = (n + a.BS - 1) / a.BS;
-    for (int j = 0; j < my_tiles && ok; ++j) {
-      const int b = j & 1;
+    for (int jl = 0; jl < my_tiles && ok; ++jl) {
+      const int b = jl & 1;
+      const int j = ilv ? 2 * jl + t : jl;            // the loaded tile
       const int kpos0 = (jt0 + j) * kN;
       float qsb[4] = {qs, qs, qs, qs};
       if (bscaled) {
@@ -633,7 +656,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
           qsb[g4] = qs * __ldg(a.block_scales + ((size_t)blk * 2 * a.L + a.layer) * a.Hkv + hkv);
         }
       }
-      if (!wait(&bars->s_full[t][b], (j >> 1) & 1)) {
+      if (!wait(&bars->s_full[t][b], (jl >> 1) & 1)) {
         ok = false;
         break;
       }
@@ -669,7 +692,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
       if (mx > mref + 8.f) {            // also the first visible key (mref = -inf)
         alpha = exp2f(mref - mx);       // 0 when mref = -inf
         mref = mx;
-        rescale = j > 0;
+        rescale = jl > 0;
       }
       const float ref = mref == -INFINITY ? 0.f : mref;
       uint64_t pp[4];                   // partial row sums, two lanes each
@@ -678,8 +701,8 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
       // a rescale needs O stable: P_{t,j-1} V_{j-1} done (its phase is the only
       // one pending here: P_tj is not yet written, and S_tj came after P_t,j-2 V)
       if (__any_sync(0xffffffffu, rescale)) {
-        if (j > 0) {
-          if (!wait(&bars->o_done[t], (j - 1) & 1)) {
+        if (jl > 0) {
+          if (!wait(&bars->o_done[t], (jl - 1) & 1)) {
             ok = false;
             break;
           }
@@ -745,7 +768,8 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
     // softmax waits for P V only before a rescale, so the last P V may be up to
     // two phases of o_done away: a one-shot barrier marks the end instead.
     // (shared-prefix mode: fp32 partial O and its natural log-sum-exp per split)
-    const size_t hrow = ((size_t)(casc ? split : s) * a.q_len + tok) * a.Hq + (size_t)hkv * G + g;
+    const int pidx = ilv ? 2 * split + t : split;     // this slot's partial set
+    const size_t hrow = ((size_t)(casc ? pidx : s) * a.q_len + tok) * a.Hq + (size_t)hkv * G + g;
     const size_t orow = hrow * kD;
     const int odt = casc ? PKV_F32 : a.out_dtype;
     if (ok && my_tiles > 0 && wait(&bars->o_final[t], 0)) {

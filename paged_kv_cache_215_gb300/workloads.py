@@ -223,6 +223,11 @@ FULL = {
     "long_128k_bs64": lambda mult=1: long_context_bs64(batch=mult),
     "llama8b_b32_8k_layers4": lambda mult=1: llama8b_layers(batch=32 * mult),
     "shared_prefix_64k_b32": lambda mult=1: shared_prefix_long(batch=32 * mult),
+    # the 70B-shaped prefix batch with lengths 4K-8K (a 1.5 GB pool): the same
+    # prefix pass (64 sequences x 8 query heads per KV head, a 4096-token prefix)
+    # on a case small enough to profile
+    "llama70b_prefix_small": lambda mult=1: llama70b_prefix(batch=64 * mult, lo=4096, hi=8192,
+                                                           seed=1011),
 }
 
 # query tokens per sequence of the multi-token (speculative verification) measurements
