@@ -372,6 +372,73 @@ __global__ void __launch_bounds__(128) merge_units_ext_kernel(const DecodeArgs a
   }
 }
 
+// Many rows (head_dim 128): one warp per row, 8 rows per CTA.  Lane l holds
+// columns 4l .. 4l+3; the partials' weights are computed 32 at a time, one per
+// lane, and broadcast by shuffle while eight partial rows are in flight.
+__global__ void __launch_bounds__(256) merge_units_ext_warp_kernel(const DecodeArgs a) {
+  const int HGR = a.HG * a.R;
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= (long long)a.B * a.NHG * HGR) return;
+  const int lane = threadIdx.x & 31;
+  const int u = (int)(row / HGR), hl = (int)(row % HGR);
+  int2 info = a.unit_info[u];
+  if (!info_ok(a, info)) {
+    if (hl == 0 && lane == 0) record_error(a.status, PKV_EBOUNDS);
+    info = make_int2(0, 0);                                   // the prefix partials alone
+  }
+  const int s = u / a.NHG, hg = u % a.NHG;
+  const int w = hl / a.R, r = hl % a.R;
+  const int i = r / a.G, g = r % a.G;
+  const size_t q_row = ((size_t)s * a.q_len + i) * a.Hq + (size_t)(hg * a.HG + w) * a.G + g;
+  const size_t rows = (size_t)a.B * a.q_len * a.Hq;           // rows of one ext partial set
+  const size_t row0 = (size_t)info.x * HGR + hl;
+  const int total = info.y + a.ext_count;
+  auto lse_of = [&](int p) {
+    return p < info.y ? a.part_lse[row0 + (size_t)p * HGR]
+                      : a.ext_lse[(size_t)(p - info.y) * rows + q_row];
+  };
+  auto o_of = [&](int p) {
+    return p < info.y ? a.part_o + (row0 + (size_t)p * HGR) * a.D
+                      : a.ext_o + ((size_t)(p - info.y) * rows + q_row) * a.D;
+  };
+  float M = -INFINITY;
+  for (int p = lane; p < total; p += 32) M = fmaxf(M, lse_of(p));
+  M = warp_max(M);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float W = 0.f;
+  if (M != -INFINITY) {
+    for (int base = 0; base < total; base += 32) {
+      const int cnt = min(32, total - base);
+      const float wl = lane < cnt ? exp2f((lse_of(base + lane) - M) * kLog2e) : 0.f;
+      for (int k = 0; k < cnt; k += 8) {
+        float4 v[8];
+        float wt[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          wt[e] = __shfl_sync(0xffffffffu, wl, (k + e) & 31);
+          v[e] = k + e < cnt ? reinterpret_cast<const float4*>(o_of(base + k + e))[lane]
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (k + e >= cnt) break;
+          W += wt[e];
+          acc.x = fmaf(wt[e], v[e].x, acc.x);
+          acc.y = fmaf(wt[e], v[e].y, acc.y);
+          acc.z = fmaf(wt[e], v[e].z, acc.z);
+          acc.w = fmaf(wt[e], v[e].w, acc.w);
+        }
+      }
+    }
+  }
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+  const size_t o = q_row * a.D + 4 * lane;
+  store_from_float(a.out, o + 0, a.out_dtype, acc.x * inv);
+  store_from_float(a.out, o + 1, a.out_dtype, acc.y * inv);
+  store_from_float(a.out, o + 2, a.out_dtype, acc.z * inv);
+  store_from_float(a.out, o + 3, a.out_dtype, acc.w * inv);
+}
+
 // Suffix tables: one thread per (sequence, entry).
 __global__ void suffix_tables_kernel(const int32_t* tables, int max_blocks, const int32_t* seq_lens,
                                      const int32_t* prefix_table, int prefix_blocks,
@@ -406,6 +473,12 @@ cudaError_t launch_merge_units_ext(const DecodeArgs& a, cudaStream_t stream) {
   const long long rows = (long long)a.B * a.NHG * a.HG * a.R;
   if (rows == 0) return cudaSuccess;
   if (rows > 0x7fffffffLL || a.D > 256) return cudaErrorInvalidValue;
+  if (a.D == 128) {
+    merge_units_ext_warp_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) count_launch();
+    return e;
+  }
   merge_units_ext_kernel<<<(unsigned)rows, 128, 0, stream>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
