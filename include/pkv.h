@@ -260,6 +260,29 @@ PKV_API int paged_decode_attention(void* d_out, pkv_dtype out_dtype, const void*
                                    float scale, float k_scale, float v_scale, int num_splits,
                                    void* d_workspace, size_t ws_bytes, cudaStream_t stream);
 
+/* Partial decode attention over the tokens this pool holds, for a key range of
+ * each sequence split across GPUs ([SEQPAR] "numerically stable incremental
+ * softmax": every device attends over its own range and the partial results are
+ * combined by log-sum-exp; [ENG26] 3.1).  Same computation as
+ * paged_decode_attention over the d_seq_lens[s] tokens of each sequence's table,
+ * but it returns, per row (s, h) of batch x num_q_heads, the normalised fp32
+ * output d_out [batch, num_q_heads, head_dim] and the natural log-sum-exp of the
+ * row's scaled scores d_lse [batch, num_q_heads] (-inf and out = 0 for a
+ * sequence with no tokens here).  Partials of the ranges of one sequence, stacked
+ * as [batch, num_q_heads, ranges, head_dim] and [batch, num_q_heads, ranges],
+ * give its whole attention through merge_partials.  Runs on the tensor-core
+ * kernel (bf16 / f16 pools with q in the pool's dtype, E4M3 pools with bf16 / f16
+ * q; head_dim 128), else PKV_EUNSUPPORTED.  The workspace is
+ * paged_decode_workspace_bytes(geom, batch, max_seq_len, 0); other arguments and
+ * errors as in paged_decode_attention. */
+PKV_API int paged_decode_attention_partial(float* d_out, float* d_lse, const void* d_q,
+                                           pkv_dtype q_dtype, const pkv_pool* pool, int layer,
+                                           const int32_t* d_block_tables, int max_blocks_per_seq,
+                                           const int32_t* d_seq_lens, int batch, int max_seq_len,
+                                           float scale, float k_scale, float v_scale,
+                                           void* d_workspace, size_t ws_bytes,
+                                           cudaStream_t stream);
+
 /* Launch choices a caller may force (tests, ablations, benchmarks).  Zero-filled
  * means "automatic" for every field. */
 typedef struct {

@@ -1032,8 +1032,9 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
     return;
   }
 
-  // a shared-prefix decode merges every row with its prefix partials
-  const bool whole_ok = a.ext_lse == nullptr;
+  // a shared-prefix decode merges every row with its prefix partials, and a call
+  // that returns each row's log-sum-exp has the merge write every row
+  const bool whole_ok = a.ext_lse == nullptr && a.out_lse == nullptr;
   int stage = 0;
   uint32_t round = 0;
   while (cur.remaining > 0) {

@@ -32,7 +32,7 @@ constexpr int kUnroll = 4;     // partial rows in flight per warp
 // (and 4(g+32)..) of one partial row per load, so a warp reads a whole row.
 __device__ void merge_row(const float* __restrict__ lse, size_t lse_stride,
                           const float* __restrict__ o, size_t o_stride, int count, int D,
-                          void* out, size_t out_off, int out_dtype) {
+                          void* out, size_t out_off, int out_dtype, float* out_lse = nullptr) {
   __shared__ float wts[kChunk];
   __shared__ float red[kWarps][kMaxD];
   __shared__ float redw[kWarps];
@@ -132,6 +132,8 @@ __device__ void merge_row(const float* __restrict__ lse, size_t lse_stride,
       v += red[w][d];
     }
     store_from_float(out, out_off + d, out_dtype, W > 0.f ? v / W : 0.f);
+    // the row's natural log-sum-exp: M + ln(sum of exp(lse_p - M))
+    if (out_lse && d == 0) *out_lse = W > 0.f ? M + __logf(W) : -INFINITY;
   }
 }
 
@@ -152,7 +154,7 @@ __global__ void __launch_bounds__(kThreads) merge_units_kernel(const DecodeArgs 
   grid_launch_dependents();
   const int u = blockIdx.x, hl = blockIdx.y;
   const int2 info = a.unit_info[u];
-  if (info.y == 1) return;
+  if (info.y == 1 && !a.out_lse) return;       // the attention kernel wrote this row
   if (!info_ok(a, info)) {
     if (hl == 0 && threadIdx.x == 0) record_error(a.status, PKV_EBOUNDS);
     return;
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(kThreads) merge_units_kernel(const DecodeArgs 
   const size_t q_row = ((size_t)s * a.q_len + i) * a.Hq + (size_t)(hg * a.HG + w) * a.G + g;
   const size_t row0 = (size_t)info.x * HGR + hl;
   merge_row(a.part_lse + row0, HGR, a.part_o + row0 * a.D, (size_t)HGR * a.D, info.y, a.D, a.out,
-            q_row * a.D, a.out_dtype);
+            q_row * a.D, a.out_dtype, a.out_lse ? a.out_lse + q_row : nullptr);
 }
 
 // Many rows, few partials each (multi-token decode, large batches): one warp per
@@ -181,7 +183,7 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) merge_units_warp_kernel(cons
   const int lane = threadIdx.x & 31;
   const int u = (int)(row / HGR), hl = (int)(row % HGR);
   const int2 info = a.unit_info[u];
-  if (info.y == 1) return;                      // the attention kernel wrote this row
+  if (info.y == 1 && !a.out_lse) return;        // the attention kernel wrote this row
   if (!info_ok(a, info)) {
     if (hl == 0 && lane == 0) record_error(a.status, PKV_EBOUNDS);
     return;
@@ -214,6 +216,7 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) merge_units_warp_kernel(cons
     store_from_float(a.out, q_row * a.D + d0 + 1, a.out_dtype, acc.y * inv);
     store_from_float(a.out, q_row * a.D + d0 + 2, a.out_dtype, acc.z * inv);
     store_from_float(a.out, q_row * a.D + d0 + 3, a.out_dtype, acc.w * inv);
+    if (a.out_lse && d0 == 0) a.out_lse[q_row] = W > 0.f ? M + __logf(W) : -INFINITY;
   }
 }
 

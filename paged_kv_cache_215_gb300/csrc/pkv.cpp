@@ -610,7 +610,7 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
                          int max_seq_len, float scale, float k_scale, float v_scale,
                          int num_splits, void* d_workspace, size_t ws_bytes,
                          const pkv_launch_opts* opts, cudaStream_t stream,
-                         const ExtPartials* ext = nullptr) {
+                         const ExtPartials* ext = nullptr, float* out_lse = nullptr) {
   pkv_pool* p = const_cast<pkv_pool*>(pool);
   if (!p || batch < 0 || max_seq_len < 0 || num_splits < 0 || layer < 0 ||
       layer >= p->g.num_layers || q_len < 1)
@@ -691,7 +691,7 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
     return launch_prefill_tc(map, t, stream) == cudaSuccess ? PKV_OK : PKV_ECUDA;
   }
   bool use_mma;
-  if (ext) {
+  if (ext || out_lse) {
     if (!mma_ok || num_splits != 0 || q_len != 1 || kernel == 1) return PKV_EUNSUPPORTED;
     use_mma = true;
   } else if (kernel == 2) {
@@ -788,6 +788,7 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
       a.part_lse = reinterpret_cast<float*>(ws + w.lse_off);
       a.unit_info = reinterpret_cast<int2*>(ws + w.info_off);
       a.slots = plan.grid + batch * plan.NHG;
+      a.out_lse = out_lse;
       if (ext) {
         a.ext_o = ext->o;
         a.ext_lse = ext->lse;
@@ -1017,6 +1018,18 @@ int paged_decode_attention_ex(void* d_out, pkv_dtype out_dtype, const void* d_q,
   return decode_common(d_out, out_dtype, d_q, q_dtype, 1, nullptr, nullptr, 0, pool, layer,
                        d_block_tables, max_blocks_per_seq, d_seq_lens, batch, max_seq_len, scale,
                        k_scale, v_scale, num_splits, d_workspace, ws_bytes, opts, stream);
+}
+
+int paged_decode_attention_partial(float* d_out, float* d_lse, const void* d_q,
+                                   pkv_dtype q_dtype, const pkv_pool* pool, int layer,
+                                   const int32_t* d_block_tables, int max_blocks_per_seq,
+                                   const int32_t* d_seq_lens, int batch, int max_seq_len,
+                                   float scale, float k_scale, float v_scale, void* d_workspace,
+                                   size_t ws_bytes, cudaStream_t stream) {
+  if (batch > 0 && !d_lse) return PKV_EINVAL;
+  return decode_common(d_out, PKV_F32, d_q, q_dtype, 1, nullptr, nullptr, 0, pool, layer,
+                       d_block_tables, max_blocks_per_seq, d_seq_lens, batch, max_seq_len, scale,
+                       k_scale, v_scale, 0, d_workspace, ws_bytes, nullptr, stream, nullptr, d_lse);
 }
 
 int paged_decode_attention_mq(void* d_out, pkv_dtype out_dtype, const void* d_q,

@@ -58,3 +58,36 @@ def rank_case(name: str, rank: int, world: int) -> "wl.Case":
     glob = wl.FULL[name](world)
     lo, hi = partition(glob.seq_lens, world)[rank]
     return shard(glob, lo, hi)
+
+
+# ---------------------------------------------------------------------------
+# One long sequence across GPUs: every rank holds a contiguous key range of it
+# and attends over that range alone; the partial results meet once.
+
+def key_ranges(n: int, world: int, block_size: int) -> List[Tuple[int, int]]:
+    """Block-aligned contiguous [lo, hi) ranges of a sequence's n keys, one per
+    rank (rank r: blocks [r * nb / world, (r + 1) * nb / world)), covering every
+    key once; a rank may get an empty range."""
+    nb = (int(n) + block_size - 1) // block_size
+    cuts = [min(int(n), (r * nb // world) * block_size) for r in range(world)] + [int(n)]
+    return [(cuts[r], cuts[r + 1]) for r in range(world)]
+
+
+def gather_and_merge(o_local, lse_local, merge, out, group=None):
+    """The exchange of a key-range split ("Sequence-parallel engineering for
+    long-context LLM inference", numerically stable incremental softmax, and its
+    communication-cost section: one gather of every rank's partial output and
+    log-sum-exp): all-gather this rank's fp32 partial o_local [B, H, D] and
+    lse_local [B, H], stack them as [B, H, ranks, D] and [B, H, ranks], and let
+    `merge(out, part_o, part_lse)` combine them (the library's merge_partials on
+    GPUs).  Every rank ends with the whole result in `out`."""
+    import torch
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    os_ = [torch.empty_like(o_local) for _ in range(world)]
+    ls_ = [torch.empty_like(lse_local) for _ in range(world)]
+    dist.all_gather(os_, o_local.contiguous(), group=group)
+    dist.all_gather(ls_, lse_local.contiguous(), group=group)
+    part_o = torch.stack(os_, dim=2).contiguous()
+    part_lse = torch.stack(ls_, dim=2).contiguous()
+    return merge(out, part_o, part_lse)

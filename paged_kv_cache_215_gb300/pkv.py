@@ -82,6 +82,7 @@ def _load() -> ctypes.CDLL:
         "paged_decode_attention_ex": (I, [P, I, P, I, P, I, P, I, P, I, I, F, F, F, I, P, Z,
                                           ctypes.POINTER(LaunchOpts), P]),
         "merge_partials": (I, [P, I, P, P, I, I, I, I, P]),
+        "paged_decode_attention_partial": (I, [P, P, P, I, P, I, P, I, P, I, I, F, F, F, P, Z, P]),
         "paged_decode_step": (I, [P, I, P, I, P, P, I, P, I, P, I, P, I, I, F, F, F, I, P, Z,
                                   ctypes.POINTER(LaunchOpts), P]),
         "paged_decode_attention_static": (I, [P, I, P, I, P, I, P, I, P, I, I, F, F, F, I, P]),
@@ -108,6 +109,7 @@ EXPORTS = ("kv_pool_bytes", "kv_pool_create", "kv_pool_destroy", "kv_pool_geomet
            "kv_append_tokens", "kv_absmax", "kv_fp8_scale", "paged_decode_workspace_bytes",
            "kv_pool_set_block_scales", "kv_block_scales",
            "paged_decode_attention", "paged_decode_attention_ex", "merge_partials",
+           "paged_decode_attention_partial",
            "paged_decode_attention_static", "paged_decode_step",
            "paged_decode_attention_mq", "paged_decode_workspace_bytes_mq",
            "paged_decode_attention_cascade", "paged_decode_workspace_bytes_cascade",
@@ -334,6 +336,22 @@ def paged_decode_attention(out, q, pool: KVPool, layer, tables, seq_lens, max_se
         rc = _lib.paged_decode_attention_ex(*args, ctypes.byref(opts), _stream(stream))
     _check(rc, "paged_decode_attention")
     return out
+
+
+def paged_decode_attention_partial(out, lse, q, pool: KVPool, layer, tables, seq_lens,
+                                   max_seq_len, scale, k_scale=1.0, v_scale=1.0, workspace=None,
+                                   stream=None):
+    """Partial attention over the tokens this pool holds: fp32 out [B, Hq, D] and
+    the natural log-sum-exp lse [B, Hq] of every row (for merging key ranges)."""
+    if workspace is None:
+        nb = workspace_bytes(pool.geom, q.shape[0], max_seq_len, 0)
+        workspace = torch.empty(max(nb, 16), dtype=torch.uint8, device=q.device)
+    assert out.dtype == torch.float32 and lse.dtype == torch.float32
+    _check(_lib.paged_decode_attention_partial(
+        _ptr(out), _ptr(lse), _ptr(q), TORCH_CODE[q.dtype], pool.handle, layer, _ptr(tables),
+        tables.shape[1], _ptr(seq_lens), q.shape[0], max_seq_len, scale, k_scale, v_scale,
+        _ptr(workspace), workspace.numel(), _stream(stream)), "paged_decode_attention_partial")
+    return out, lse
 
 
 def paged_decode_attention_static(out, q, pool: KVPool, layer, tables, seq_lens, max_seq_len,

@@ -137,3 +137,61 @@ def test_two_ranks_own_disjoint_shards_of_one_global_batch():
         for lo, hi, ls, nb in g:
             need = sum((n + 15) // 16 for n in ls)
             assert nb >= need                              # its own pool covers its blocks
+
+
+def test_key_ranges_cover_a_sequence_once_on_block_boundaries():
+    for n in (0, 1, 15, 16, 17, 1000, 131072):
+        for world in (1, 2, 3, 8):
+            rs = dp.key_ranges(n, world, 16)
+            assert rs[0][0] == 0 and rs[-1][1] == n and len(rs) == world
+            for (a0, a1), (b0, b1) in zip(rs, rs[1:]):
+                assert a1 == b0 and a0 <= a1 and b0 <= b1
+            assert all(lo % 16 == 0 for lo, _ in rs)
+
+
+def _seqpar_worker(rank, world, port, results):
+    """Rank r attends over its key range of every sequence (the oracle stands in
+    for the GPU kernel here), then the gather-and-merge exchange over gloo."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import torch
+    import oracle
+    from tests.helpers import np_raw, oracle_pool
+    case = wl.make_case("seqpar", [300, 77, 5], 8, 2, 32, 16, "f32", "f32", "f32", seed=61)
+    tens = wl.make_tensors(case)
+    pool = oracle_pool(case, tens, include_new=True)
+    ranges = [dp.key_ranges(int(n), world, 16)[rank] for n in case.seq_lens]
+    lo = np.array([r[0] for r in ranges], np.int32)
+    hi = np.array([r[1] for r in ranges], np.int32)
+    o, lse, _ = oracle.decode(np_raw(tens.q), "f32", pool, "f32", case.geometry, 0, case.tables,
+                              case.seq_lens, case.scale, tok_begin=lo, tok_end=hi)
+
+    def merge(out, part_o, part_lse):
+        B, H, S, D = part_o.shape
+        m, _ = oracle.merge(part_o.numpy().reshape(B * H, S, D), part_lse.numpy().reshape(B * H, S))
+        out.copy_(torch.from_numpy(m.reshape(B, H, D)))
+        return out
+    out = torch.empty(case.batch, 8, 32, dtype=torch.float64)
+    dp.gather_and_merge(torch.from_numpy(o), torch.from_numpy(lse), merge, out)
+    full, _, _ = oracle.decode(np_raw(tens.q), "f32", pool, "f32", case.geometry, 0, case.tables,
+                               case.seq_lens, case.scale)
+    results[rank] = float(np.abs(out.numpy() - full).max())
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_key_range_split_gathers_and_merges_to_the_whole_attention(world):
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    results = mgr.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_seqpar_worker, args=(r, world, port, results))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=180)
+        assert p.exitcode == 0
+    for r in range(world):
+        assert results[r] < 1e-12
