@@ -244,6 +244,36 @@ struct pkv_pool {
     if (r != CUDA_SUCCESS) return nullptr;
     return &tmaps.emplace(hg, m).first->second;
   }
+  // TMA descriptor for the tcgen05 kernel's K/V tiles (2-byte pools, D = 128): one
+  // box holds a whole block of one KV head, both 64-column halves, laid out in
+  // shared memory as 8-token groups, each group's half 0 then half 1 (1 KB
+  // swizzle atoms: [group][half][8 rows][128 B]).  The dimensions, innermost
+  // first: column within a half (64), token within a group (stride one row),
+  // half (stride 128 B), group of 8 rows over heads and tokens (stride 8 rows),
+  // block plane (blk * 2 + kv) * L + layer.  E4M3 pools use tmap(1).
+  const CUtensorMap* tmap_tiles() {
+    if (g.kv_dtype == PKV_FP8_E4M3) return tmap(1);
+    if (g.head_dim != 128 || g.block_size % 8 != 0 || g.block_size > 64) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = tmaps.find(0);
+    if (it != tmaps.end()) return &it->second;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return nullptr;
+    const cuuint64_t row = (cuuint64_t)g.head_dim * 2;
+    CUtensorMapDataType dt = g.kv_dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    cuuint64_t dims[5] = {64, 8, 2, (cuuint64_t)g.num_kv_heads * g.block_size / 8,
+                          (cuuint64_t)g.num_blocks * 2 * g.num_layers};
+    cuuint64_t strides[4] = {row, 128, 8 * row, (cuuint64_t)g.num_kv_heads * g.block_size * row};
+    cuuint32_t box[5] = {64, 8, 2, (cuuint32_t)g.block_size / 8, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUtensorMap m;
+    CUresult r = enc(&m, dt, 5, d_pool, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return nullptr;
+    return &tmaps.emplace(0, m).first->second;
+  }
 };
 
 extern "C" {
@@ -659,7 +689,7 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
     if (!tc_ok) return PKV_EUNSUPPORTED;
     if (num_splits != 0 || phase == 2) return phase == 2 ? PKV_OK : PKV_EUNSUPPORTED;
     if (batch > 65535 || g.num_kv_heads > 65535) return PKV_EUNSUPPORTED;
-    const CUtensorMap* map = p->tmap(1);
+    const CUtensorMap* map = p->tmap_tiles();
     if (!map) return PKV_ECUDA;
     DecodeArgs t{};
     t.q = d_q;
@@ -967,7 +997,7 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
   // 2. the shared prefix once for every sequence: tcgen05 tiles of 128 query rows
   //    (sequences x heads of a KV head), key range cut into w.S splits
   if (prefix_len_max > 0 && phase != 2) {
-    const CUtensorMap* map = p->tmap(1);
+    const CUtensorMap* map = p->tmap_tiles();
     if (!map) return PKV_ECUDA;
     DecodeArgs t{};
     t.q = d_q;

@@ -14,8 +14,8 @@
 //   M = 128 rows = 128/G query tokens x G heads, staged once in shared memory
 //   (128-byte swizzled).  Both tiles of the pair consume every K/V tile, so
 //   each 64-token K/V tile loaded from L2 feeds 256 query rows.  K/V tiles
-//   arrive by TMA from the pool (one box per block, K/V and 64-column half)
-//   into a 4-stage ring.  Per query tile t and key tile j:
+//   arrive by TMA from the pool (one box per block and K/V, both 64-column
+//   halves: bs x 256 bytes) into a 5-stage ring.  Per query tile t and key tile j:
 //     S_tj = Q_t K_j^T      tcgen05.mma M128 N64 K128 -> TMEM (two buffers per
 //                           query tile, so S_t,j+1 runs while the softmax of S_tj does)
 //     softmax               one warpgroup per query tile, one thread per row:
@@ -34,7 +34,7 @@
 // Issuers, one thread each: warp 8 + t issues query tile t's S MMAs, warp 10 + t
 // its P V MMAs (a single thread issues a UMMA about every 70 cycles, short of
 // what these tiles take on the tensor core; issuers in different warps multiply
-// the rate), warp 12 the K/V loads (16 boxes per tile at block size 16, from 16
+// the rate), warp 12 the K/V loads (8 boxes per tile at block size 16, from 8
 // lanes).  mbarriers (all waits bounded) pass the tiles between the roles; a
 // stage is refilled once every issuer's MMAs reading it have completed.
 #include "device.cuh"
@@ -55,7 +55,7 @@ constexpr int kWarpConv = kWarpTMA + 1;      // E4M3 pools: warps converting K/V
 constexpr int kIssuers = 2 * kQT;            // MMA issuers committing each stage's release
 constexpr uint32_t kHalf = 16384;            // 128 rows x 128 B: one 64-column half of Q
 constexpr uint32_t kKVHalf = kN * 128;       // 64 rows x 128 B
-constexpr uint32_t kStageBytes = 4 * kKVHalf;        // K halves 0, 1 then V halves 0, 1
+constexpr uint32_t kStageBytes = 4 * kKVHalf;        // K tile (16 KB) then V tile (16 KB)
 constexpr uint32_t kStage8Bytes = 2 * kKVHalf;       // an E4M3 tile: K then V, 128 B a key
 constexpr uint32_t kSmemQ = 0;                        // [query tile][half]
 constexpr uint32_t kSmemKV = kSmemQ + kQT * 2 * kHalf;
@@ -310,8 +310,14 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
       // Descriptors of the shared-memory base; a tile's descriptor adds its byte
       // offset / 16 to the start-address field (shared addresses stay below 256 KB,
       // so the 14-bit field never carries).
-      const uint64_t d_k = smem_desc_sw128(base, 16, 1024);      // K-major operands
-      const uint64_t d_v = smem_desc_sw128(base, kKVHalf, 1024); // V: MN-major
+      // Q: K-major, 8-row groups 1 KB apart.  16-bit K/V tiles: 8-key groups of
+      // [half 0 | half 1] atoms, so K (K-major) has its groups 2 KB apart and V
+      // (MN-major) its halves 1 KB and its groups 2 KB apart.  E4M3 tiles are
+      // converted into 64-row halves: K groups 1 KB apart, V halves 8 KB apart.
+      const uint64_t d_k = smem_desc_sw128(base, 16, 1024);
+      const uint64_t d_kt = smem_desc_sw128(base, 16, kFp8 ? 1024 : 2048);
+      const uint64_t d_v = kFp8 ? smem_desc_sw128(base, kKVHalf, 1024)
+                                : smem_desc_sw128(base, 1024, 2048);
       bool ok = true;
       if (warp == kWarpTMA) {
         const int bpt = kN / a.BS;                             // blocks per key tile
@@ -331,24 +337,24 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
             id_base = first;
             ids = id_base + lane < nblk ? __ldg(trow + id_base + lane) : 0;
           }
-          // lane l < 4 * bpt loads one box: block l / 4 of the tile, K or V
-          // ((l / 2) & 1), 64-column half l & 1.  Blocks past the sequence's last
-          // one are replaced by its last block: their keys are masked and their
-          // V rows zeroed before use.
-          const int jb = min(first + (lane >> 2), nblk - 1);
+          // lane l < 2 * bpt loads one box: block l / 2 of the tile, K or V (l & 1),
+          // both 64-column halves (bs x 256 bytes).  Blocks past the sequence's
+          // last one are replaced by its last block: their keys are masked and
+          // their V rows zeroed before use.
+          const int jb = min(first + (lane >> 1), nblk - 1);
           int blk = __shfl_sync(0xffffffffu, ids, jb - id_base);
           if (leader) mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
           __syncwarp();
-          if (lane < 4 * bpt) {
+          if (lane < 2 * bpt) {
             if (blk < 0 || blk >= a.num_blocks) {
               record_error(a.status, PKV_EBOUNDS);
               blk = 0;
             }
-            const int kv = (lane >> 1) & 1, h = lane & 1;
+            const int kv = lane & 1;
             const int z = (blk * 2 + kv) * a.L + a.layer;
-            tma_load_3d(sm + kSmemKV + st * kStageBytes + (kv * 2 + h) * kKVHalf +
-                            (lane >> 2) * a.BS * 128,
-                        &tmap, &bars->kv_full[st], h * 64, hkv * a.BS, z);
+            tma_load_5d(sm + kSmemKV + st * kStageBytes + kv * 2 * kKVHalf +
+                            (lane >> 1) * a.BS * 256,
+                        &tmap, &bars->kv_full[st], 0, 0, 0, hkv * a.BS / 8, z);
           }
         };
         if constexpr (kFp8) {
@@ -407,8 +413,8 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
             uint8_t* vbuf = sm + kSmemKV + (j_tail % kStages) * kStageBytes + 2 * kKVHalf;
             for (int e = lane; e < (kN - valid) * 16; e += 32) {
               const int row = valid + e / 16, c16 = e % 16;
-              *reinterpret_cast<uint4*>(vbuf + (c16 >> 3) * kKVHalf + sw128(row, c16 & 7)) =
-                  make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(vbuf + ((row >> 3) * 2 + (c16 >> 3)) * 1024 +
+                                        sw128(row & 7, c16 & 7)) = make_uint4(0, 0, 0, 0);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -561,11 +567,11 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           if (mine && leader) {
-            const uint64_t kb = d_k + ((kSmemKV + (j % kStages) * kStageBytes) >> 4);
+            const uint64_t kb = d_kt + ((kSmemKV + (j % kStages) * kStageBytes) >> 4);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               const uint32_t off = ((k >> 2) * kHalf + (k & 3) * 32) >> 4;
-              const uint32_t offk = ((k >> 2) * kKVHalf + (k & 3) * 32) >> 4;
+              const uint32_t offk = ((k >> 2) * (kFp8 ? kKVHalf : 1024u) + (k & 3) * 32) >> 4;
               tc_mma_f16(tmem + t * 256 + (jl & 1) * kN, qb + off, kb + offk, id_s, k > 0);
             }
             tc_commit(&bars->s_full[t][jl & 1]);
@@ -591,9 +597,10 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
               const uint32_t pa = tmem + t * 256 + b * kN;       // P hi: 32 columns, lo: the next 32
 #pragma unroll
               for (int k = 0; k < 4; ++k) {                     // 16 keys (8 columns of P) per MMA
-                tc_mma_f16_ts(tmem + t * 256 + 128, pa + k * 8, vb + k * 128, id_o,
+                const uint32_t vk = k * (kFp8 ? 128u : 256u);   // 16 keys: 2 KB / 4 KB on
+                tc_mma_f16_ts(tmem + t * 256 + 128, pa + k * 8, vb + vk, id_o,
                               (jl > 0 || k > 0) ? 1u : 0u);
-                if (kSplitP) tc_mma_f16_ts(tmem + t * 256 + 128, pa + 32 + k * 8, vb + k * 128, id_o, 1u);
+                if (kSplitP) tc_mma_f16_ts(tmem + t * 256 + 128, pa + 32 + k * 8, vb + vk, id_o, 1u);
               }
               tc_commit(&bars->o_done[t]);
               tc_commit(&bars->p_free[t][b]);
