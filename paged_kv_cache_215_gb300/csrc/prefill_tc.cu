@@ -61,7 +61,7 @@ constexpr uint32_t kSmemQ = 0;                        // [query tile][half]
 constexpr uint32_t kSmemKV = kSmemQ + kQT * 2 * kHalf;
 constexpr uint32_t kTmemCols = 512;          // query tile t: S/P0 [256t, +64) S/P1 [+64, +128) O [+128, +256)
 constexpr uint32_t kAlignSlack = 1024;       // the tiles start on a 1024-byte boundary
-constexpr int kMaxStages = 5;
+constexpr int kMaxStages = 6;
 
 // Per pool dtype.  bf16 / f16: TMA fills kStages tiles the MMAs read directly.
 // E4M3: TMA lands the E4M3 tile (one 128-byte line per key: half the boxes) in
@@ -205,17 +205,25 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
   // does slot t compute loaded tile j, and as which of its own tiles
   auto owns = [&](int t, int j) { return ilv ? (j & 1) == t : j < tiles[t]; };
   auto local = [&](int j) { return ilv ? j >> 1 : j; };
+  // The K/V ring: kStages stages after the Q tiles; a CTA whose second query
+  // tile is empty (a single 128-row tile: the shared-prefix pass, or the last
+  // CTA of an odd tile count) also puts one in that tile's Q space, so one more
+  // K/V tile is in flight while the memory system answers.
+  const int nst = (T > 0 && tiles[kQT - 1] == 0 && !ilv) ? kStages + 1 : kStages;
+  auto stage_off = [&](int st) -> uint32_t {
+    return st < kStages ? kSmemKV + (uint32_t)st * kStageBytes : kSmemQ + (kQT - 1) * 2 * kHalf;
+  };
   // the sequence's last key tile, if it is ragged and this CTA reads it (local index)
   const int jg_tail = (n % kN != 0) ? (n - 1) / kN : -1;
   const int j_tail = (jg_tail >= jt0 && jg_tail < jt0 + T) ? jg_tail - jt0 : -1;
 
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kMaxStages; ++i) {
       mbar_init(&bars->kv_full[i], kFp8 ? C::kConvWarps : 1);   // the converters, or TMA
       mbar_init(&bars->kv_empty[i], kIssuers);   // one commit from each MMA issuer
     }
     if (kFp8)
-      for (int i = 0; i < kStages; ++i) mbar_init(&bars->s8_full[i], 1);
+      for (int i = 0; i < kMaxStages; ++i) mbar_init(&bars->s8_full[i], 1);
     for (int t = 0; t < kQT; ++t) {
       for (int b = 0; b < 2; ++b) {
         mbar_init(&bars->s_full[t][b], 1);
@@ -323,14 +331,14 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
         const int bpt = kN / a.BS;                             // blocks per key tile
         const int nblk = (n + a.BS - 1) / a.BS;
         const int32_t* trow = a.tables + (size_t)s * a.max_blocks;
-        int last_load[kStages];                                // last key tile requested per stage
+        int last_load[kMaxStages];                             // last key tile requested per stage
 #pragma unroll
-        for (int i = 0; i < kStages; ++i) last_load[i] = -1;
+        for (int i = 0; i < kMaxStages; ++i) last_load[i] = -1;
         // block ids of the sequence, 32 at a time: lane i holds entry id_base + i
         // (one table read per 32 blocks instead of a dependent read per box)
         int ids = 0, id_base = -1;
         auto load_tile = [&](int j) {
-          const int st = j % kStages;
+          const int st = j % nst;
           last_load[st] = j;
           const int first = (jt0 + j) * bpt;                    // < nblk for every tile loaded
           if (id_base < 0 || first + bpt > id_base + 32) {
@@ -352,7 +360,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
             }
             const int kv = lane & 1;
             const int z = (blk * 2 + kv) * a.L + a.layer;
-            tma_load_5d(sm + kSmemKV + st * kStageBytes + kv * 2 * kKVHalf +
+            tma_load_5d(sm + stage_off(st) + kv * 2 * kKVHalf +
                             (lane >> 1) * a.BS * 256,
                         &tmap, &bars->kv_full[st], 0, 0, 0, hkv * a.BS / 8, z);
           }
@@ -362,7 +370,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
           // into the V half of the stage: E4M3 K where f16 V half 0 goes, E4M3 V
           // where half 1 goes; the converters then fill the stage in place
           auto load8 = [&](int j) {
-            const int st = j % kStages;
+            const int st = j % nst;
             last_load[st] = j;
             const int first = (jt0 + j) * bpt;
             if (id_base < 0 || first + bpt > id_base + 32) {
@@ -380,37 +388,37 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
               }
               const int kv = lane & 1;
               const int z = (blk * 2 + kv) * a.L + a.layer;
-              tma_load_3d(sm + kSmemKV + st * kStageBytes + (2 + kv) * kKVHalf +
+              tma_load_3d(sm + stage_off(st) + (2 + kv) * kKVHalf +
                               (lane >> 1) * a.BS * 128,
                           &tmap, &bars->s8_full[st], 0, hkv * a.BS, z);
             }
           };
-          for (int j = 0; j < T && j < kStages; ++j) load8(j);
-          for (int k = kStages; k < T && ok; ++k) {
-            ok = wait(&bars->kv_empty[(k - kStages) % kStages], ((k - kStages) / kStages) & 1);
+          for (int j = 0; j < T && j < nst; ++j) load8(j);
+          for (int k = nst; k < T && ok; ++k) {
+            ok = wait(&bars->kv_empty[(k - nst) % nst], ((k - nst) / nst) & 1);
             if (!ok) break;
             load8(k);
           }
           if (leader)
-            for (int st = 0; st < kStages; ++st)
+            for (int st = 0; st < nst; ++st)
               if (last_load[st] >= 0)
-                mbar_wait_bounded(&bars->s8_full[st], (last_load[st] / kStages) & 1);
+                mbar_wait_bounded(&bars->s8_full[st], (last_load[st] / nst) & 1);
         } else {
-        for (int j = 0; j < T && j < kStages; ++j) load_tile(j);
-        // key tile k goes into the stage of tile k - kStages once every issuer's
+        for (int j = 0; j < T && j < nst; ++j) load_tile(j);
+        // key tile k goes into the stage of tile k - nst once every issuer's
         // MMAs reading that tile have completed
-        for (int k = kStages; k < T && ok; ++k) {
-          ok = wait(&bars->kv_empty[(k - kStages) % kStages], ((k - kStages) / kStages) & 1);
+        for (int k = nst; k < T && ok; ++k) {
+          ok = wait(&bars->kv_empty[(k - nst) % nst], ((k - nst) / nst) & 1);
           if (!ok) break;
           load_tile(k);
         }
         // keys past the sequence end in its last tile: zero their V rows once the
         // tile has landed, so that P = 0 never meets an unwritten (possibly NaN) slot
         if (ok && j_tail >= 0) {
-          ok = wait(&bars->kv_full[j_tail % kStages], (j_tail / kStages) & 1);
+          ok = wait(&bars->kv_full[j_tail % nst], (j_tail / nst) & 1);
           if (ok) {
             const int valid = n - (jt0 + j_tail) * kN;
-            uint8_t* vbuf = sm + kSmemKV + (j_tail % kStages) * kStageBytes + 2 * kKVHalf;
+            uint8_t* vbuf = sm + stage_off(j_tail % nst) + 2 * kKVHalf;
             for (int e = lane; e < (kN - valid) * 16; e += 32) {
               const int row = valid + e / 16, c16 = e % 16;
               *reinterpret_cast<uint4*>(vbuf + ((row >> 3) * 2 + (c16 >> 3)) * 1024 +
@@ -422,12 +430,12 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
           }
         }
         // every TMA load issued must land before the CTA may exit.  A stage's key
-        // tile k is requested only after tile k - kStages landed and was read, so
+        // tile k is requested only after tile k - nst landed and was read, so
         // waiting for the phase of the last tile requested into it covers all.
         if (leader)
-          for (int st = 0; st < kStages; ++st)
+          for (int st = 0; st < nst; ++st)
             if (last_load[st] >= 0)
-              mbar_wait_bounded(&bars->kv_full[st], (last_load[st] / kStages) & 1);
+              mbar_wait_bounded(&bars->kv_full[st], (last_load[st] / nst) & 1);
         }
       } else if (warp >= kWarpConv) {
         if constexpr (kFp8) {
@@ -495,10 +503,10 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
           ev_ref = ev == -100000 ? 0 : ev;
         }
         for (int j = 0; j < T && ok; ++j) {
-          const int st = j % kStages;
-          ok = wait(&bars->s8_full[st], (j / kStages) & 1);
+          const int st = j % nst;
+          ok = wait(&bars->s8_full[st], (j / nst) & 1);
           if (!ok) break;
-          uint8_t* dst = sm + kSmemKV + st * kStageBytes;
+          uint8_t* dst = sm + stage_off(st);
           const uint8_t* src = dst + 2 * kKVHalf;              // E4M3 K rows, then V rows
           const int valid = n - (jt0 + j) * kN;                // keys of the tile in the sequence
           // two groups a step (eight loads in flight a lane before the warp syncs)
@@ -558,7 +566,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
         const int t = warp - kWarpS;                           // this warp's query tile
         const uint64_t qb = d_k + ((kSmemQ + t * 2 * kHalf) >> 4);
         for (int j = 0; j < T && ok; ++j) {
-          ok = wait(&bars->kv_full[j % kStages], (j / kStages) & 1);
+          ok = wait(&bars->kv_full[j % nst], (j / nst) & 1);
           const bool mine = owns(t, j);
           const int jl = local(j);
           // S_tj overwrites the TMEM buffer of the slot's P two tiles back: its P V
@@ -567,7 +575,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           if (mine && leader) {
-            const uint64_t kb = d_kt + ((kSmemKV + (j % kStages) * kStageBytes) >> 4);
+            const uint64_t kb = d_kt + (stage_off(j % nst) >> 4);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               const uint32_t off = ((k >> 2) * kHalf + (k & 3) * 32) >> 4;
@@ -576,7 +584,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
             }
             tc_commit(&bars->s_full[t][jl & 1]);
           }
-          if (leader) tc_commit(&bars->kv_empty[j % kStages]);  // S_tj has read K_j
+          if (leader) tc_commit(&bars->kv_empty[j % nst]);  // S_tj has read K_j
           __syncwarp();
         }
       } else {
@@ -584,7 +592,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
         for (int j = 0; j < T && ok; ++j) {
           // paces this warp's releases: its arrival for the stage's next tile can
           // only follow that tile's load, which follows this tile's release
-          ok = wait(&bars->kv_full[j % kStages], (j / kStages) & 1);
+          ok = wait(&bars->kv_full[j % nst], (j / nst) & 1);
           const int jl = local(j);
           if (ok && owns(t, j)) {
             const int b = jl & 1;
@@ -593,7 +601,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             if (leader) {
-              const uint64_t vb = d_v + ((kSmemKV + (j % kStages) * kStageBytes + 2 * kKVHalf) >> 4);
+              const uint64_t vb = d_v + ((stage_off(j % nst) + 2 * kKVHalf) >> 4);
               const uint32_t pa = tmem + t * 256 + b * kN;       // P hi: 32 columns, lo: the next 32
 #pragma unroll
               for (int k = 0; k < 4; ++k) {                     // 16 keys (8 columns of P) per MMA
@@ -608,7 +616,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
             }
           }
           if (!ok) break;
-          if (leader) tc_commit(&bars->kv_empty[j % kStages]);  // P_tj V_j has read V_j
+          if (leader) tc_commit(&bars->kv_empty[j % nst]);  // P_tj V_j has read V_j
           __syncwarp();
         }
       }
