@@ -86,6 +86,7 @@ struct Bars {
   uint64_t s_full[kQT][2], p_full[kQT][2], p_free[kQT][2], o_done[kQT];
   uint64_t o_final[kQT];                      // query tile t's last P V has completed
   uint64_t v_zeroed;                          // the tail tile's V rows past the end are zero
+  uint64_t q_ready;                           // the Q tiles are staged
   uint64_t eref_ready;                        // E4M3 per-block scales: the reference exponent is in
   int eref[4];                                // per converter warp: largest exponent of the V scales
   uint32_t tmem;
@@ -163,7 +164,12 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
   // shared-prefix mode: query token i is sequence i, one key table (the prefix),
   // blockIdx.z cuts the key range into a.S splits
   const bool casc = a.key_limit != nullptr;
-  const int hkv = blockIdx.y, s = casc ? 0 : blockIdx.z, split = casc ? blockIdx.z : 0;
+  // blockIdx.x = KV head; y = sequence (shared-prefix mode: key split); z = pair of
+  // query tiles, counted from the chunk's end in chunked prefill: the pairs nearest
+  // the end see the most keys and are launched first, so the last, partial wave of
+  // CTAs holds the shortest ones
+  const int hkv = blockIdx.x, s = casc ? 0 : blockIdx.y, split = casc ? blockIdx.y : 0;
+  const int pair = casc ? (int)blockIdx.z : (int)(gridDim.z - 1 - blockIdx.z);
   // Shared-prefix mode with a single query tile: both tile slots hold the same
   // query rows and take alternate key tiles (slot t: local tiles j = t mod 2),
   // each with its own O, running max and sum; each writes its own partial
@@ -192,11 +198,11 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
     } else {
 #pragma unroll
       for (int t = 0; t < kQT; ++t)
-        tiles[t] = (blockIdx.x * kQT + t) * QT < a.q_len ? jt1 - jt0 : 0;
+        tiles[t] = (pair * kQT + t) * QT < a.q_len ? jt1 - jt0 : 0;
     }
   } else {
 #pragma unroll
-    for (int t = 0; t < kQT; ++t) tiles[t] = key_tiles(a, n, blockIdx.x * kQT + t);
+    for (int t = 0; t < kQT; ++t) tiles[t] = key_tiles(a, n, pair * kQT + t);
   }
   if (!ilv) {
 #pragma unroll
@@ -234,6 +240,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
       mbar_init(&bars->o_final[t], 1);
     }
     mbar_init(&bars->v_zeroed, 1);
+    mbar_init(&bars->q_ready, 32 * kSoftmaxWarps);
     mbar_init(&bars->eref_ready, kFp8 ? C::kConvWarps : 1);
     bars->abort_flag = 0;
     fence_mbar_init();
@@ -242,15 +249,23 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
     tmem_alloc(&bars->tmem, kTmemCols);
     tmem_relinquish();
   }
-  // Q tiles: thread (t, r) stages row r = (token t0 + r / G, head hkv*G + r % G), swizzled.
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;
+  // Q tiles, staged while the first K/V tiles are in flight (the S issuers wait
+  // for q_ready): thread (t, r) stages row r = (token t0 + r / G, head hkv*G + r % G), swizzled.
   // E4M3 pools run f16 MMAs: a bf16 q row is scaled by 2^q_e (f16_fit_exponent of
   // its largest |q|) before the f16 rounding, exactly, and the same thread's
   // softmax takes 2^-q_e onto the scale.
   int q_e = 0;
   if (warp < kSoftmaxWarps) {
     const int t = warp / 4, r = tid - 128 * t, i = r / G, g = r % G;
-    const int tok = (blockIdx.x * kQT + (ilv ? 0 : t)) * QT + i;
+    // an empty tile is not staged: its S MMAs never run, and its Q space may
+    // hold the ring's extra stage
+    const int tok = (pair * kQT + (ilv ? 0 : t)) * QT + i;
     const bool live = tok < a.q_len;
+    const bool staged = tiles[t] > 0;
     const size_t qrow = ((size_t)s * a.q_len + tok) * a.Hq + (size_t)hkv * G + g;
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) +
                                                       (live ? qrow : 0) * kD);
@@ -276,7 +291,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
       qscale = pow2i(q_e);
     }
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
+    for (int c = 0; c < 16 && staged; ++c) {
       uint4 v = live ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
       if (to_f16) {
         // the MMAs of an E4M3 pool run on f16 operands: q bf16 x 2^q_e -> f16
@@ -294,11 +309,8 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
       *reinterpret_cast<uint4*>(qdst + (c >> 3) * kHalf + sw128(r, c & 7)) = v;
     }
     fence_proxy_async_smem();
+    mbar_arrive(&bars->q_ready);
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = bars->tmem;
 
   if (warp >= kSoftmaxWarps) {
     // ------------------------------------------------------------ issuers
@@ -565,6 +577,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
       } else if (warp < kWarpPV) {
         const int t = warp - kWarpS;                           // this warp's query tile
         const uint64_t qb = d_k + ((kSmemQ + t * 2 * kHalf) >> 4);
+        ok = wait(&bars->q_ready, 0);
         for (int j = 0; j < T && ok; ++j) {
           ok = wait(&bars->kv_full[j % nst], (j / nst) & 1);
           const bool mine = owns(t, j);
@@ -629,7 +642,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
   } else {
     // ------------------------------------------------------------ softmax, one row per thread
     const int t = warp / 4, r = tid - 128 * t, i = r / G, g = r % G;
-    const int tok = (blockIdx.x * kQT + (ilv ? 0 : t)) * QT + i;
+    const int tok = (pair * kQT + (ilv ? 0 : t)) * QT + i;
     const bool live = tok < a.q_len;
     // this query's last visible key: causal within the chunk, or its prefix length
     const int pos = casc ? (live ? __ldg(a.key_limit + tok) : 0) - 1 : n - a.q_len + tok;
@@ -865,7 +878,9 @@ cudaError_t launch_prefill_tc(const CUtensorMap* map, const DecodeArgs& a, cudaS
   const int qtiles = (a.q_len + QT - 1) / QT;
   if (qtiles == 0 || a.B == 0) return cudaSuccess;
   if (a.key_limit && (a.S < 1 || a.S > 65535 || a.B != 1 || !a.out_lse)) return cudaErrorInvalidValue;
-  dim3 grid((qtiles + kQT - 1) / kQT, a.Hkv, a.key_limit ? a.S : a.B);
+  const int pairs = (qtiles + kQT - 1) / kQT;
+  if (pairs > 65535 || a.B > 65535) return cudaErrorInvalidValue;
+  dim3 grid(a.Hkv, a.key_limit ? a.S : a.B, pairs);
   cudaError_t e;
   switch (a.kv_dtype) {
     case PKV_BF16: e = launch_t<PKV_BF16>(map, a, grid, stream); break;
