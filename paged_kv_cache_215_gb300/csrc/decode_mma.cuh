@@ -871,6 +871,12 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
     }
   }
   __syncthreads();
+  // Balanced mode runs one resident wave, so the next launch (the merge, or the
+  // next step's attention) may be scheduled now: it takes SMs as this grid's CTAs
+  // retire, and waits (griddepcontrol.wait) before it reads or overwrites
+  // anything this grid writes.  (E4M3 pools keep the trigger at the end: there
+  // the next attention grid, started early, ran 0.5% slower.)
+  if (a.mode == 0 && !T::kFp8) grid_launch_dependents();
 
   // ---- this CTA's cursor (identical in every warp)
   Cursor cur;

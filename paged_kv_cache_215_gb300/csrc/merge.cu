@@ -149,9 +149,10 @@ __device__ __forceinline__ bool info_ok(const DecodeArgs& a, int2 info) {
 // first .. first+count-1, each with HG*R rows (R = q_len * G); count 1 means the
 // attention kernel already wrote the output.
 __global__ void __launch_bounds__(kThreads) merge_units_kernel(const DecodeArgs a) {
-  grid_dependency_wait();
-  // the next launch may begin now: this grid's inputs are complete
+  // the next launch may be scheduled now (it waits for this grid before it
+  // writes anything this grid reads); this grid's own inputs come first
   grid_launch_dependents();
+  grid_dependency_wait();
   const int u = blockIdx.x, hl = blockIdx.y;
   const int2 info = a.unit_info[u];
   if (info.y == 1 && !a.out_lse) return;       // the attention kernel wrote this row
@@ -175,8 +176,8 @@ __global__ void __launch_bounds__(kThreads) merge_units_kernel(const DecodeArgs 
 // reads each partial's lse (a broadcast) and computes its weight.
 constexpr int kRowsPerCta = 8;
 __global__ void __launch_bounds__(32 * kRowsPerCta) merge_units_warp_kernel(const DecodeArgs a) {
-  grid_dependency_wait();
   grid_launch_dependents();
+  grid_dependency_wait();
   const int HGR = a.HG * a.R;
   const long long row = (long long)blockIdx.x * kRowsPerCta + (threadIdx.x >> 5);
   if (row >= (long long)a.B * a.NHG * HGR) return;
@@ -224,8 +225,8 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) merge_units_warp_kernel(cons
 __global__ void __launch_bounds__(kThreads)
     merge_rows_kernel(void* out, int out_dtype, const float* part_o, const float* part_lse, int S,
                       int D) {
-  grid_dependency_wait();
   grid_launch_dependents();
+  grid_dependency_wait();
   const size_t r = blockIdx.x;
   merge_row(part_lse + r * S, 1, part_o + r * S * D, D, S, D, out, r * D, out_dtype);
 }
