@@ -295,11 +295,14 @@ typedef struct {
   int32_t stages;          /* 0 auto; shared-memory pipeline depth */
   int32_t phase;           /* 0 attention then merge, 1 attention only, 2 merge only */
   int32_t pdl;             /* 1: launch the attention kernel with programmatic dependent
-                              launch, so its start-up overlaps the kernel before it in the
-                              stream.  Only valid when that kernel writes none of q, the
-                              block tables, seq_lens, the pool or k/v_new (for example the
-                              previous decode step's merge); every write to out, the
-                              workspace and the pool still waits for it. */
+                              launch, so that it starts while the launches before it in
+                              the stream (for example the previous decode step's attention
+                              and merge, chained the same way) finish.  Only valid when
+                              those launches write none of q, the block tables, seq_lens or
+                              k/v_new, and write the pool only within the last two blocks
+                              of each sequence (a previous decode step's new token): the
+                              kernel waits for them before it loads those two blocks and
+                              before any write to out, the workspace and the pool. */
   int32_t reserved[2];
 } pkv_launch_opts;
 

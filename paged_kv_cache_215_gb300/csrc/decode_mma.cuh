@@ -871,12 +871,14 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
     }
   }
   __syncthreads();
-  // Balanced mode runs one resident wave, so the next launch (the merge, or the
-  // next step's attention) may be scheduled now: it takes SMs as this grid's CTAs
-  // retire, and waits (griddepcontrol.wait) before it reads or overwrites
-  // anything this grid writes.  (E4M3 pools keep the trigger at the end: there
-  // the next attention grid, started early, ran 0.5% slower.)
-  if (a.mode == 0 && !T::kFp8) grid_launch_dependents();
+  // Balanced mode runs one resident wave.  When the next launch in the stream is
+  // this call's own merge (a.early_trigger), it may be scheduled now: it takes
+  // SMs as this grid's CTAs retire and waits (griddepcontrol.wait) for the whole
+  // grid before it reads a partial.  The merge in turn lets the next step's
+  // attention start early; that kernel waits for this chain before it loads the
+  // last two blocks of a sequence (the blocks this step's new token went to) and
+  // before it writes anything.
+  if (a.mode == 0 && a.early_trigger) grid_launch_dependents();
 
   // ---- this CTA's cursor (identical in every warp)
   Cursor cur;
@@ -924,6 +926,12 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
       if (!blk_ok) {
         if (lane == 0) record_error(a.status, PKV_EBOUNDS);
         blk = 0;
+      }
+      // with programmatic dependent launch the kernels ahead in the stream may still
+      // run: the last two blocks of a sequence may hold tokens they store
+      if (a.pdl && !waited && cur.j >= cur.nb - 2) {
+        grid_dependency_wait();
+        waited = true;
       }
       if (a.k_new && cur.j == cur.nb - 1 && blk_ok) {
         // decode step: store the sequence's new token (position n - 1) for this

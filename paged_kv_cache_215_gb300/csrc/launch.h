@@ -47,6 +47,7 @@ struct DecodeArgs {
   // 1: launched with programmatic dependent launch; every write to out, the
   // workspace or the pool waits for the preceding kernel (griddepcontrol.wait).
   int pdl;
+  int early_trigger;  // balanced mode, this call's merge next: let it be scheduled at the start
   // Shared-prefix decode (cascade).  Decode kernel + merge: ext_count partials per
   // output row computed elsewhere (over the shared prefix), [ext_count][B*Hq][D] and
   // [ext_count][B*Hq]; every unit then leaves partials and the merge adds these.

@@ -819,6 +819,9 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
       a.unit_info = reinterpret_cast<int2*>(ws + w.info_off);
       a.slots = plan.grid + batch * plan.NHG;
       a.out_lse = out_lse;
+      // the merge may be scheduled at the attention grid's start (E4M3 pools: at its
+      // end, measured 0.4% faster there)
+      a.early_trigger = phase == 0 && !fp8 ? 1 : 0;
       if (ext) {
         a.ext_o = ext->o;
         a.ext_lse = ext->lse;
