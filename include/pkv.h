@@ -15,7 +15,11 @@
  * Conventions shared by every call:
  *   - Every device buffer is owned by the caller (for example a torch tensor);
  *     the library never allocates device memory.  `d_` marks a device pointer,
- *     `h_` or no prefix a host pointer.
+ *     `h_` or no prefix a host pointer.  On a host whose pinned memory the GPU
+ *     maps (a Grace host), the decode calls also take q, the new token's k and
+ *     v, the lengths, the tables and out in pinned host memory (the kernels read
+ *     and write them over the CPU-GPU link); the workspace is device memory,
+ *     and every buffer must stay allocated until the launches that use it end.
  *   - Shapes are row-major: q and out [batch, num_q_heads, head_dim];
  *     k and v of new tokens [tokens, num_kv_heads, head_dim]; block tables
  *     int32 [batch, max_blocks_per_seq] (entries past ceil(seq_len/block_size)

@@ -326,7 +326,7 @@ def paged_decode_attention(out, q, pool: KVPool, layer, tables, seq_lens, max_se
                            stream=None):
     if workspace is None:
         nb = workspace_bytes(pool.geom, q.shape[0], max_seq_len, num_splits)
-        workspace = torch.empty(max(nb, 16), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(max(nb, 16), dtype=torch.uint8, device=pool.storage.device)
     args = (_ptr(out), TORCH_CODE[out.dtype], _ptr(q), TORCH_CODE[q.dtype], pool.handle, layer,
             _ptr(tables), tables.shape[1], _ptr(seq_lens), q.shape[0], max_seq_len, scale,
             k_scale, v_scale, num_splits, _ptr(workspace), workspace.numel())
@@ -345,7 +345,7 @@ def paged_decode_attention_partial(out, lse, q, pool: KVPool, layer, tables, seq
     the natural log-sum-exp lse [B, Hq] of every row (for merging key ranges)."""
     if workspace is None:
         nb = workspace_bytes(pool.geom, q.shape[0], max_seq_len, 0)
-        workspace = torch.empty(max(nb, 16), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(max(nb, 16), dtype=torch.uint8, device=pool.storage.device)
     assert out.dtype == torch.float32 and lse.dtype == torch.float32
     _check(_lib.paged_decode_attention_partial(
         _ptr(out), _ptr(lse), _ptr(q), TORCH_CODE[q.dtype], pool.handle, layer, _ptr(tables),
@@ -372,7 +372,7 @@ def paged_decode_step(out, q, k_new, v_new, pool: KVPool, layer, tables, seq_len
     (fused into one attention launch on the tensor-core kernel)."""
     if workspace is None:
         nb = workspace_bytes(pool.geom, q.shape[0], max_seq_len, num_splits)
-        workspace = torch.empty(max(nb, 16), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(max(nb, 16), dtype=torch.uint8, device=pool.storage.device)
     _check(_lib.paged_decode_step(
         _ptr(out), TORCH_CODE[out.dtype], _ptr(q), TORCH_CODE[q.dtype], _ptr(k_new), _ptr(v_new),
         TORCH_CODE[k_new.dtype], pool.handle, layer, _ptr(tables), tables.shape[1],
@@ -391,7 +391,7 @@ def paged_decode_attention_mq(out, q, pool: KVPool, layer, tables, seq_lens, max
     if workspace is None:
         nb = int(_lib.paged_decode_workspace_bytes_mq(ctypes.byref(pool.geom), B, q_len,
                                                       max_seq_len, num_splits))
-        workspace = torch.empty(max(nb, 16), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(max(nb, 16), dtype=torch.uint8, device=pool.storage.device)
     _check(_lib.paged_decode_attention_mq(
         _ptr(out), TORCH_CODE[out.dtype], _ptr(q), TORCH_CODE[q.dtype], q_len, pool.handle, layer,
         _ptr(tables), tables.shape[1], _ptr(seq_lens), B, max_seq_len, scale, k_scale, v_scale,
@@ -419,7 +419,7 @@ def paged_decode_attention_cascade(out, q, pool: KVPool, layer, prefix_table, pr
     B = q.shape[0]
     if workspace is None:
         nb = cascade_workspace_bytes(pool.geom, B, tables.shape[1], max_seq_len, prefix_len_max)
-        workspace = torch.empty(max(nb, 16), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(max(nb, 16), dtype=torch.uint8, device=pool.storage.device)
     _check(_lib.paged_decode_attention_cascade(
         _ptr(out), TORCH_CODE[out.dtype], _ptr(q), TORCH_CODE[q.dtype], pool.handle, layer,
         _ptr(prefix_table), int(prefix_table.numel()) if prefix_table is not None else 0,
