@@ -1,4 +1,4 @@
-"""Data-parallel decode over sequences: which GPU owns which sequences.
+"""Decode across GPUs: which GPU owns which sequences, key ranges or heads.
 
 Decode attention of one sequence reads only that sequence's blocks, so a batch
 splits across GPUs by sequence with no exchange between them: each GPU holds
@@ -7,6 +7,10 @@ merge) on them, and returns their outputs.  The only host-side decision is the
 split; this module makes it: contiguous ranges of the global batch, cut at the
 token-count quantiles so that every GPU reads about the same KV bytes (the
 quantity the step's time follows), every sequence owned by exactly one rank.
+Two splits with one exchange each are here too: a long sequence's keys cut
+into block-aligned ranges (an all-gather of the partial outputs and their
+log-sum-exp, then the merge), and the KV heads cut into ranges (an all-gather
+of the outputs, concatenated along the heads).
 """
 from __future__ import annotations
 
@@ -91,3 +95,31 @@ def gather_and_merge(o_local, lse_local, merge, out, group=None):
     part_o = torch.stack(os_, dim=2).contiguous()
     part_lse = torch.stack(ls_, dim=2).contiguous()
     return merge(out, part_o, part_lse)
+
+
+# ---------------------------------------------------------------------------
+# KV heads across GPUs: every rank holds all sequences' blocks for a contiguous
+# range of KV heads (and attends with the query heads that read them); the
+# outputs of the ranks are concatenated along the head dimension.
+
+def head_ranges(num_kv_heads: int, world: int) -> List[Tuple[int, int]]:
+    """Contiguous [lo, hi) KV-head ranges of equal size, one per rank; rank r
+    serves query heads [lo * G, hi * G) (query head h reads KV head h // G).
+    num_kv_heads must be a multiple of world."""
+    if world < 1 or num_kv_heads % world:
+        raise ValueError("num_kv_heads must be a positive multiple of world")
+    per = num_kv_heads // world
+    return [(r * per, (r + 1) * per) for r in range(world)]
+
+
+def gather_heads(o_local, out, group=None):
+    """The exchange of the head split: all-gather every rank's output for its
+    query heads, o_local [B, Hq / world, D], and concatenate them in rank order
+    into out [B, Hq, D].  Every rank ends with the whole result."""
+    import torch
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    parts = [torch.empty_like(o_local) for _ in range(world)]
+    dist.all_gather(parts, o_local.contiguous(), group=group)
+    out.copy_(torch.cat(parts, dim=1))
+    return out

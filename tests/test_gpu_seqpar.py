@@ -1,4 +1,4 @@
-"""A key-range split of sequences across GPUs, emulated on one GPU (needs a GPU).
+"""Key-range and head splits of decode across GPUs, emulated on one GPU (needs a GPU).
 
 "Sequence-parallel engineering for long-context LLM inference" splits a long
 sequence's keys across devices; each attends over its own range and the
@@ -10,7 +10,9 @@ the N ranks, stacked, go through merge_partials.  The ranks run one after the
 other on the one GPU (no kernel waits for another).  Checked against the fp64
 oracle: each rank's partial output and log-sum-exp against the oracle over the
 same key range, and the merged output against the whole attention, within
-2e-3 x max|V| (bf16) or 5e-3 x max|V| (E4M3).
+2e-3 x max|V| (bf16) or 5e-3 x max|V| (E4M3).  The head split gives each rank
+the blocks of a range of KV heads (dp.head_ranges) and concatenates the ranks'
+outputs along the heads.
 """
 import numpy as np
 import pytest
@@ -116,3 +118,49 @@ def test_key_range_split_partials_merge_to_the_whole_attention(kv, world):
     got = out.double().cpu().numpy()
     for s in seqs:
         assert np.abs(got[s] - ref[s]).max() <= tol * vm[s], s
+
+
+@pytest.mark.parametrize("world", [2, 4, 8])
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_head_split_outputs_concatenate_to_the_whole_attention(kv, world):
+    """Rank r of N holds every sequence's blocks for KV heads dp.head_ranges(8, N)[r]
+    only, in a pool of its own, and attends with their query heads; the ranks'
+    outputs, concatenated along the heads, must match the oracle's whole
+    attention (E4M3: the per-tensor scales of the whole tensors, as one pool would
+    use)."""
+    from paged_kv_cache_215_gb300 import build, pkv
+    build.build()
+    case = wl.make_case(f"heads_{kv}", [3000, 40, 1], 32, 8, 128, 16, kv, "bf16", "bf16",
+                        seed=71, spike_frac=0.01)
+    tens = wl.make_tensors(case)
+    ks_, vs_ = (1.0, 1.0) if kv != "e4m3" else fp8_scales(tens)
+    pool_o, ref, seqs = oracle_side(case, tens, None, ks_, vs_)
+    vm = vmax_per_seq(case, pool_o, seqs, vs_)
+    kall, vall = _full_kv(case, tens)
+    G, bs = 4, 16
+    lens = [int(n) for n in case.seq_lens]
+    outs = []
+    for lo, hi in dp.head_ranges(8, world):
+        nbs = [(n + bs - 1) // bs for n in lens]
+        geom = pkv.geometry(1, (hi - lo) * G, hi - lo, 128, bs, sum(nbs) + 3, kv)
+        pool = pkv.KVPool(geom)
+        pool.storage.fill_(0xFF)
+        tables = np.full((case.batch, max(nbs)), -1, np.int32)
+        pool.prepare_append(np.zeros(case.batch, np.int32), tables, new_tokens=lens)
+        k = torch.cat([kall[s][:, lo:hi] for s in range(case.batch)]).contiguous()
+        v = torch.cat([vall[s][:, lo:hi] for s in range(case.batch)]).contiguous()
+        seq = torch.cat([torch.full((n,), s, dtype=torch.int32) for s, n in enumerate(lens)])
+        pos = torch.cat([torch.arange(n, dtype=torch.int32) for n in lens])
+        td = torch.from_numpy(tables).cuda()
+        pool.append_tokens(0, k.cuda(), v.cuda(), td, seq.cuda(), pos.cuda(), ks_, vs_)
+        q = tens.q[:, lo * G:hi * G].contiguous().cuda()
+        out = torch.full((case.batch, (hi - lo) * G, 128), float("nan"), device="cuda")
+        pkv.paged_decode_attention(out, q, pool, 0, td,
+                                   torch.tensor(lens, dtype=torch.int32, device="cuda"),
+                                   max(lens), case.scale, ks_, vs_)
+        torch.cuda.synchronize()
+        assert pool.check_status() == 0
+        outs.append(out)
+    got = torch.cat(outs, dim=1).double().cpu().numpy()
+    for s in seqs:
+        assert np.abs(got[s] - ref[s]).max() <= TOL[kv] * vm[s], s

@@ -1,7 +1,8 @@
 """The multi-rank path on CPU (gloo): the data-parallel split of one global batch
 by sequence (every sequence owned by exactly one rank, ranks balanced by token
-count) and the benchmark's aggregation (the slowest rank's time, the sum of all
-ranks' bytes)."""
+count), the benchmark's aggregation (the slowest rank's time, the sum of all
+ranks' bytes), and the key-range and head splits with their one exchange each
+(the oracle standing in for each rank's GPU work)."""
 import os
 import socket
 
@@ -195,3 +196,55 @@ def test_key_range_split_gathers_and_merges_to_the_whole_attention(world):
         assert p.exitcode == 0
     for r in range(world):
         assert results[r] < 1e-12
+
+
+def test_head_ranges_split_kv_heads_evenly():
+    assert dp.head_ranges(8, 1) == [(0, 8)]
+    assert dp.head_ranges(8, 4) == [(0, 2), (2, 4), (4, 6), (6, 8)]
+    with pytest.raises(ValueError):
+        dp.head_ranges(8, 3)
+
+
+def _heads_worker(rank, world, port, results):
+    """Rank r attends with the query heads of its KV heads only (the oracle's rows
+    of those heads stand in for the GPU kernel on a pool of those heads), then the
+    all-gather that concatenates the heads."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import torch
+    import oracle
+    from tests.helpers import np_raw, oracle_pool
+    case = wl.make_case("heads", [300, 77, 5], 8, 4, 32, 16, "f32", "f32", "f32", seed=62)
+    tens = wl.make_tensors(case)
+    pool = oracle_pool(case, tens, include_new=True)
+    G = case.num_q_heads // case.num_kv_heads
+    lo, hi = dp.head_ranges(case.num_kv_heads, world)[rank]
+    rows = np.array([s * case.num_q_heads + h for s in range(case.batch)
+                     for h in range(lo * G, hi * G)], np.int32)
+    o, _, _ = oracle.decode(np_raw(tens.q), "f32", pool, "f32", case.geometry, 0, case.tables,
+                            case.seq_lens, case.scale, rows=rows)
+    mine = torch.from_numpy(np.ascontiguousarray(o[:, lo * G:hi * G]))
+    out = torch.empty(case.batch, case.num_q_heads, 32, dtype=torch.float64)
+    dp.gather_heads(mine, out)
+    full, _, _ = oracle.decode(np_raw(tens.q), "f32", pool, "f32", case.geometry, 0, case.tables,
+                               case.seq_lens, case.scale)
+    results[rank] = float(np.abs(out.numpy() - full).max())
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 4])
+def test_head_split_gathers_to_the_whole_attention(world):
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    results = mgr.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_heads_worker, args=(r, world, port, results))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=180)
+        assert p.exitcode == 0
+    for r in range(world):
+        assert results[r] == 0.0
