@@ -967,13 +967,21 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
   const CascadeWs w = cascade_ws(g, batch, max_blocks_per_seq, prefix_len_max, dev.sms, dec);
   // A prefix whose K/V fill at most a quarter of L2 is already read from HBM
   // about once by the plain decode: every sequence reaches its first blocks at
-  // the start of the launch and the repeats hit in L2.  There the prefix pass,
-  // its partials and the wider merge cost more than they save, so such a call
-  // (or kernel = 2) runs the plain decode over the sequences' own tables, after
-  // the same prefix check; kernel = 3 always takes the prefix pass.
+  // the start of the launch and the repeats hit in L2.  The repeats still cost
+  // the decode L2 traffic (measured on the 70B-shaped batch, 64 sequences
+  // sharing 17 MB: about 23 TB/s of repeats saved by the prefix pass), while the
+  // prefix pass costs about 30 us plus its K/V streamed once per pair of
+  // 128-row query tiles at about 5 TB/s.  So such a call runs the prefix pass
+  // only when the saving is larger, else (or with kernel = 2) the plain decode
+  // over the sequences' own tables, after the same prefix check; kernel = 3
+  // always takes the prefix pass.
   const size_t prefix_bytes = (size_t)prefix_len_max * 2 * g.num_kv_heads * g.head_dim *
                               elem_bytes(g.kv_dtype);
-  const bool plain = kernel == 2 || (kernel == 0 && prefix_bytes * 4 <= (size_t)dev.l2_bytes);
+  const int pairs = ((batch * G + 127) / 128 + 1) / 2;
+  const double saved_us = (batch - 1) * (double)prefix_bytes / 23e12 * 1e6;
+  const double cost_us = 30.0 + pairs * (double)prefix_bytes / 5e12 * 1e6;
+  const bool plain = kernel == 2 || (kernel == 0 && prefix_bytes * 4 <= (size_t)dev.l2_bytes &&
+                                     saved_us <= cost_us);
   if (ws_bytes < w.bytes) return PKV_ENOMEM;
   char* ws = static_cast<char*>(d_workspace);
   int32_t* n_prefix = reinterpret_cast<int32_t*>(ws + w.n_off);
