@@ -71,7 +71,10 @@ def rank_case(name: str, rank: int, world: int) -> "wl.Case":
 def key_ranges(n: int, world: int, block_size: int) -> List[Tuple[int, int]]:
     """Block-aligned contiguous [lo, hi) ranges of a sequence's n keys, one per
     rank (rank r: blocks [r * nb / world, (r + 1) * nb / world)), covering every
-    key once; a rank may get an empty range."""
+    key once; a rank may get an empty range.  Rank r holds its keys at local
+    positions 0 .. hi - lo of its own tables."""
+    if world < 1 or block_size < 1 or n < 0:
+        raise ValueError("need world >= 1, block_size >= 1 and n >= 0")
     nb = (int(n) + block_size - 1) // block_size
     cuts = [min(int(n), (r * nb // world) * block_size) for r in range(world)] + [int(n)]
     return [(cuts[r], cuts[r + 1]) for r in range(world)]

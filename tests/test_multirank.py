@@ -148,6 +148,8 @@ def test_key_ranges_cover_a_sequence_once_on_block_boundaries():
             for (a0, a1), (b0, b1) in zip(rs, rs[1:]):
                 assert a1 == b0 and a0 <= a1 and b0 <= b1
             assert all(lo % 16 == 0 for lo, _ in rs)
+    with pytest.raises(ValueError):
+        dp.key_ranges(10, 0, 16)
 
 
 def _seqpar_worker(rank, world, port, results):
