@@ -1108,6 +1108,9 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
       cons.load_q(a, cur.s, cur.n, hkv, lane);
     }
   }
+  // a chained launch ends only after the launches ahead of it (a CTA that wrote
+  // nothing has not waited yet)
+  if (a.pdl && !waited) grid_dependency_wait();
   grid_launch_dependents();
 }
 

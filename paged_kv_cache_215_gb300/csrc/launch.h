@@ -48,6 +48,7 @@ struct DecodeArgs {
   // workspace or the pool waits for the preceding kernel (griddepcontrol.wait).
   int pdl;
   int early_trigger;  // balanced mode, this call's merge next: let it be scheduled at the start
+  int casc_len;       // tcgen05 kernel, shared-prefix mode: the prefix length in tokens
   // Shared-prefix decode (cascade).  Decode kernel + merge: ext_count partials per
   // output row computed elsewhere (over the shared prefix), [ext_count][B*Hq][D] and
   // [ext_count][B*Hq]; every unit then leaves partials and the merge adds these.

@@ -826,7 +826,6 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
         a.ext_o = ext->o;
         a.ext_lse = ext->lse;
         a.ext_count = ext->count;
-        a.pdl = 0;
       }
       if (phase != 2 && launch_decode_mma(map, a, plan.grid, 1, stream) != cudaSuccess)
         return PKV_ECUDA;
@@ -1035,6 +1034,10 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
     t.R = G * batch;
     t.S = w.S;
     t.kv_interleave = w.parts == 2 * w.S ? 1 : 0;
+    // chained behind the suffix-table kernel: the pass reads only the caller's
+    // inputs (the prefix length comes with the launch)
+    t.casc_len = prefix_len_max;
+    t.pdl = 1;
     // E4M3: per-tensor scales on the softmax scale and the partial O (as the
     // decode kernel's partials carry them), per-block ones in the tile conversion
     t.qk_scale_log2 = (float)((double)scale * 1.4426950408889634 * (double)k_scale);
@@ -1042,12 +1045,18 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
     t.block_scales = bscales;
     if (launch_prefill_tc(map, t, stream) != cudaSuccess) return PKV_ECUDA;
   }
-  // 3. the private suffixes, merged with the prefix partials
+  // 3. the private suffixes, merged with the prefix partials; chained behind the
+  //    prefix pass when this call launched it (the decode takes SMs as the pass's
+  //    CTAs retire and waits for the pass before it writes)
   if (phase == 1) return PKV_OK;
   const ExtPartials ext{ext_o, ext_lse, prefix_len_max > 0 ? w.parts : 0};
+  pkv_launch_opts chained{};
+  chained.pdl = 1;
+  const bool chain = prefix_len_max > 0 && phase == 0;
   return decode_common(d_out, out_dtype, d_q, q_dtype, 1, nullptr, nullptr, 0, pool, layer, suf_tab,
                        max_blocks_per_seq, suf_lens, batch, max_seq_len, scale, k_scale, v_scale, 0,
-                       ws + w.dec_off, ws_bytes - w.dec_off, nullptr, stream, &ext);
+                       ws + w.dec_off, ws_bytes - w.dec_off, chain ? &chained : nullptr, stream,
+                       &ext);
 }
 
 int paged_decode_attention_ex(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_dtype q_dtype,

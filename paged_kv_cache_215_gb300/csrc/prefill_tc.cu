@@ -178,7 +178,9 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
   const bool ilv = casc && a.kv_interleave != 0;
   const int G = a.G, QT = kM / G;                 // query tokens per query tile
 
-  int n = __ldg(a.seq_lens + s);
+  // shared-prefix mode: the prefix length comes with the launch (nothing launched
+  // before it in the stream needs to have finished)
+  int n = casc ? a.casc_len : __ldg(a.seq_lens + s);
   const int cap = a.max_blocks * a.BS;
   if (n < 0 || n > cap) {
     if (tid == 0) record_error(a.status, PKV_EBOUNDS);
@@ -253,6 +255,10 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem;
+  // shared-prefix mode runs one wave: once every CTA is resident, the suffix
+  // decode launched behind it may be scheduled (it reads nothing this kernel
+  // writes, and waits for it before it writes); it takes SMs as CTAs retire
+  if (casc) grid_launch_dependents();
   // Q tiles, staged while the first K/V tiles are in flight (the S issuers wait
   // for q_ready): thread (t, r) stages row r = (token t0 + r / G, head hkv*G + r % G), swizzled.
   // E4M3 pools run f16 MMAs: a bf16 q row is scaled by 2^q_e (f16_fit_exponent of
@@ -860,9 +866,18 @@ cudaError_t launch_t(const CUtensorMap* map, const DecodeArgs& a, dim3 grid, cud
   const size_t smem = smem_bytes_t<KVT>();
   cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<KVT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e == cudaSuccess)
-    prefill_tc_kernel<KVT><<<grid, PfCfg<KVT>::kThreads, smem, stream>>>(*map, a);
-  return e;
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(PfCfg<KVT>::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<KVT>, *map, a);
 }
 
 bool prefill_tc_supported(int kv_dtype, int q_dtype, int BS, int D, int G) {
