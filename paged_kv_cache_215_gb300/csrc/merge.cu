@@ -306,6 +306,10 @@ __global__ void __launch_bounds__(128) merge_units_ext_kernel(const DecodeArgs a
   __shared__ float wts[kExtChunk];
   __shared__ const float* rowp[kExtChunk];
   __shared__ float red[4];
+  // chained behind the attention kernel: it and the prefix pass have finished
+  // (and their partials are visible) once past this wait
+  grid_launch_dependents();
+  grid_dependency_wait();
   const int HGR = a.HG * a.R;
   const long long row = blockIdx.x;
   const int u = (int)(row / HGR), hl = (int)(row % HGR);
@@ -380,6 +384,8 @@ __global__ void __launch_bounds__(128) merge_units_ext_kernel(const DecodeArgs a
 // columns 4l .. 4l+3; the partials' weights are computed 32 at a time, one per
 // lane, and broadcast by shuffle while eight partial rows are in flight.
 __global__ void __launch_bounds__(256) merge_units_ext_warp_kernel(const DecodeArgs a) {
+  grid_launch_dependents();
+  grid_dependency_wait();
   const int HGR = a.HG * a.R;
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (row >= (long long)a.B * a.NHG * HGR) return;
@@ -477,14 +483,21 @@ cudaError_t launch_merge_units_ext(const DecodeArgs& a, cudaStream_t stream) {
   const long long rows = (long long)a.B * a.NHG * a.HG * a.R;
   if (rows == 0) return cudaSuccess;
   if (rows > 0x7fffffffLL || a.D > 256) return cudaErrorInvalidValue;
-  if (a.D == 128) {
-    merge_units_ext_warp_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e == cudaSuccess) count_launch();
-    return e;
-  }
-  merge_units_ext_kernel<<<(unsigned)rows, 128, 0, stream>>>(a);
-  cudaError_t e = cudaGetLastError();
+  const bool warp = a.D == 128;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(warp ? (rows + 7) / 8 : rows));
+  cfg.blockDim = dim3(warp ? 256 : 128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.pdl ? 1 : 0;              // chained behind a chained attention launch
+  DecodeArgs copy = a;
+  void* args[] = {&copy};
+  const cudaError_t e = cudaLaunchKernelExC(
+      &cfg, warp ? reinterpret_cast<const void*>(merge_units_ext_warp_kernel)
+                 : reinterpret_cast<const void*>(merge_units_ext_kernel), args);
   if (e == cudaSuccess) count_launch();
   return e;
 }
