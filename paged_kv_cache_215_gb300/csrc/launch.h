@@ -57,13 +57,10 @@ struct DecodeArgs {
   int ext_count;
   // Prefill kernel over a shared prefix: query token i is sequence i, it sees keys
   // [0, key_limit[i]) (no causal mask); the key range is cut into S splits
-  // (blockIdx.z), each writing fp32 normalised O to out and its lse to out_lse at
+  // (blockIdx.y), each writing fp32 normalised O to out and its lse to out_lse at
   // row (split * q_len + i) * Hq + head.
   const int32_t* key_limit;
   float* out_lse;
-  // with key_limit and a single query tile: the CTA's two tile slots take
-  // alternate key tiles of the split and write partials 2 x split + slot
-  int kv_interleave;
 };
 
 // Shared memory the tensor-core kernel needs for one CTA.

@@ -881,7 +881,6 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
 struct CascadeWs {
   size_t n_off, lens_off, tab_off, o_off, lse_off, dec_off, bytes;
   int S;          // key splits of the prefix pass
-  int parts;      // prefix partials per row: S, or 2S when one query tile's two slots split keys
 };
 static CascadeWs cascade_ws(const pkv_geometry& g, int batch, int max_blocks, int prefix_len_max,
                             int sms, size_t decode_bytes) {
@@ -896,17 +895,13 @@ static CascadeWs cascade_ws(const pkv_geometry& g, int batch, int max_blocks, in
   int S = ctas > 0 ? std::max(1, sms / ctas) : 1;
   S = std::max(1, std::min(S, std::min(std::max(ktiles, 1), 64)));
   w.S = S;
-  // (a single query tile could let both tile slots take alternate key tiles,
-  // writing 2S partials; measured slower on the 64K shared document -- the pass is
-  // bound by the TMA box rate, not by the softmax -- so one partial per split)
-  w.parts = S;
   const size_t rows = (size_t)batch * g.num_q_heads;
   w.n_off = 0;
   w.lens_off = 256;
   w.tab_off = w.lens_off + align256((size_t)batch * 4);
   w.o_off = w.tab_off + align256((size_t)batch * max_blocks * 4);
-  w.lse_off = w.o_off + align256((size_t)w.parts * rows * g.head_dim * 4);
-  w.dec_off = w.lse_off + align256((size_t)w.parts * rows * 4);
+  w.lse_off = w.o_off + align256((size_t)w.S * rows * g.head_dim * 4);
+  w.dec_off = w.lse_off + align256((size_t)w.S * rows * 4);
   w.bytes = w.dec_off + decode_bytes;
   return w;
 }
@@ -1033,7 +1028,6 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
     t.q_len = batch;
     t.R = G * batch;
     t.S = w.S;
-    t.kv_interleave = w.parts == 2 * w.S ? 1 : 0;
     // chained behind the suffix-table kernel: the pass reads only the caller's
     // inputs (the prefix length comes with the launch)
     t.casc_len = prefix_len_max;
@@ -1049,7 +1043,7 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
   //    prefix pass when this call launched it (the decode takes SMs as the pass's
   //    CTAs retire and waits for the pass before it writes)
   if (phase == 1) return PKV_OK;
-  const ExtPartials ext{ext_o, ext_lse, prefix_len_max > 0 ? w.parts : 0};
+  const ExtPartials ext{ext_o, ext_lse, prefix_len_max > 0 ? w.S : 0};
   pkv_launch_opts chained{};
   chained.pdl = 1;
   const bool chain = prefix_len_max > 0 && phase == 0;

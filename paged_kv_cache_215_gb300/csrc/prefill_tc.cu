@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
   const uint32_t base = smem_u32(sm);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // shared-prefix mode: query token i is sequence i, one key table (the prefix),
-  // blockIdx.z cuts the key range into a.S splits
+  // blockIdx.y cuts the key range into a.S splits
   const bool casc = a.key_limit != nullptr;
   // blockIdx.x = KV head; y = sequence (shared-prefix mode: key split); z = pair of
   // query tiles, counted from the chunk's end in chunked prefill: the pairs nearest
@@ -170,12 +170,6 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
   // CTAs holds the shortest ones
   const int hkv = blockIdx.x, s = casc ? 0 : blockIdx.y, split = casc ? blockIdx.y : 0;
   const int pair = casc ? (int)blockIdx.z : (int)(gridDim.z - 1 - blockIdx.z);
-  // Shared-prefix mode with a single query tile: both tile slots hold the same
-  // query rows and take alternate key tiles (slot t: local tiles j = t mod 2),
-  // each with its own O, running max and sum; each writes its own partial
-  // (partial index 2 x split + t) for the merge.  This keeps both softmax
-  // warpgroups and both issuer pairs busy on one query tile.
-  const bool ilv = casc && a.kv_interleave != 0;
   const int G = a.G, QT = kM / G;                 // query tokens per query tile
 
   // shared-prefix mode: the prefix length comes with the launch (nothing launched
@@ -193,31 +187,20 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
     const int nt = (n + kN - 1) / kN;
     jt0 = (int)((long long)split * nt / a.S);
     const int jt1 = (int)((long long)(split + 1) * nt / a.S);
-    if (ilv) {
-      T = jt1 - jt0;
-      tiles[0] = (T + 1) / 2;
-      tiles[1] = T / 2;
-    } else {
 #pragma unroll
-      for (int t = 0; t < kQT; ++t)
-        tiles[t] = (pair * kQT + t) * QT < a.q_len ? jt1 - jt0 : 0;
-    }
+    for (int t = 0; t < kQT; ++t)
+      tiles[t] = (pair * kQT + t) * QT < a.q_len ? jt1 - jt0 : 0;
   } else {
 #pragma unroll
     for (int t = 0; t < kQT; ++t) tiles[t] = key_tiles(a, n, pair * kQT + t);
   }
-  if (!ilv) {
 #pragma unroll
-    for (int t = 0; t < kQT; ++t) T = max(T, tiles[t]);
-  }
-  // does slot t compute loaded tile j, and as which of its own tiles
-  auto owns = [&](int t, int j) { return ilv ? (j & 1) == t : j < tiles[t]; };
-  auto local = [&](int j) { return ilv ? j >> 1 : j; };
+  for (int t = 0; t < kQT; ++t) T = max(T, tiles[t]);
   // The K/V ring: kStages stages after the Q tiles; a CTA whose second query
   // tile is empty (a single 128-row tile: the shared-prefix pass, or the last
   // CTA of an odd tile count) also puts one in that tile's Q space, so one more
   // K/V tile is in flight while the memory system answers.
-  const int nst = (T > 0 && tiles[kQT - 1] == 0 && !ilv) ? kStages + 1 : kStages;
+  const int nst = (T > 0 && tiles[kQT - 1] == 0) ? kStages + 1 : kStages;
   auto stage_off = [&](int st) -> uint32_t {
     return st < kStages ? kSmemKV + (uint32_t)st * kStageBytes : kSmemQ + (kQT - 1) * 2 * kHalf;
   };
@@ -269,7 +252,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
     const int t = warp / 4, r = tid - 128 * t, i = r / G, g = r % G;
     // an empty tile is not staged: its S MMAs never run, and its Q space may
     // hold the ring's extra stage
-    const int tok = (pair * kQT + (ilv ? 0 : t)) * QT + i;
+    const int tok = (pair * kQT + t) * QT + i;
     const bool live = tok < a.q_len;
     const bool staged = tiles[t] > 0;
     const size_t qrow = ((size_t)s * a.q_len + tok) * a.Hq + (size_t)hkv * G + g;
@@ -586,9 +569,9 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
         ok = wait(&bars->q_ready, 0);
         for (int j = 0; j < T && ok; ++j) {
           ok = wait(&bars->kv_full[j % nst], (j / nst) & 1);
-          const bool mine = owns(t, j);
-          const int jl = local(j);
-          // S_tj overwrites the TMEM buffer of the slot's P two tiles back: its P V
+          const bool mine = j < tiles[t];
+          const int jl = j;
+          // S_tj overwrites the TMEM buffer of the tile's P two tiles back: its P V
           // must have read it
           if (ok && mine && jl >= 2) ok = wait(&bars->p_free[t][jl & 1], ((jl - 2) >> 1) & 1);
           if (!ok) break;
@@ -612,8 +595,8 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
           // paces this warp's releases: its arrival for the stage's next tile can
           // only follow that tile's load, which follows this tile's release
           ok = wait(&bars->kv_full[j % nst], (j / nst) & 1);
-          const int jl = local(j);
-          if (ok && owns(t, j)) {
+          const int jl = j;
+          if (ok && j < tiles[t]) {
             const int b = jl & 1;
             ok = wait(&bars->p_full[t][b], (jl >> 1) & 1);
             if (!kFp8 && ok && j == j_tail) ok = wait(&bars->v_zeroed, 0);
@@ -648,7 +631,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
   } else {
     // ------------------------------------------------------------ softmax, one row per thread
     const int t = warp / 4, r = tid - 128 * t, i = r / G, g = r % G;
-    const int tok = (pair * kQT + (ilv ? 0 : t)) * QT + i;
+    const int tok = (pair * kQT + t) * QT + i;
     const bool live = tok < a.q_len;
     // this query's last visible key: causal within the chunk, or its prefix length
     const int pos = casc ? (live ? __ldg(a.key_limit + tok) : 0) - 1 : n - a.q_len + tok;
@@ -678,7 +661,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
     const int nblk = (n + a.BS - 1) / a.BS;
     for (int jl = 0; jl < my_tiles && ok; ++jl) {
       const int b = jl & 1;
-      const int j = ilv ? 2 * jl + t : jl;            // the loaded tile
+      const int j = jl;
       const int kpos0 = (jt0 + j) * kN;
       float qsb[4] = {qs, qs, qs, qs};
       if (bscaled) {
@@ -802,7 +785,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
     // softmax waits for P V only before a rescale, so the last P V may be up to
     // two phases of o_done away: a one-shot barrier marks the end instead.
     // (shared-prefix mode: fp32 partial O and its natural log-sum-exp per split)
-    const int pidx = ilv ? 2 * split + t : split;     // this slot's partial set
+    const int pidx = split;                          // this split's partial set
     const size_t hrow = ((size_t)(casc ? pidx : s) * a.q_len + tok) * a.Hq + (size_t)hkv * G + g;
     const size_t orow = hrow * kD;
     const int odt = casc ? PKV_F32 : a.out_dtype;
