@@ -1,4 +1,5 @@
-"""Decode attention on seeded random shapes against the fp64 oracle (needs a GPU).
+"""Seeded random shapes against the fp64 oracle (needs a GPU): decode, chunked
+prefill on the tcgen05 kernel, and shared-prefix decode.
 
 Forty configurations drawn from a fixed seed, each a small batch through the
 public entry points: KV heads 1-8, GQA groups 1-8 (the mhpn.cn long-context
@@ -96,3 +97,108 @@ def test_random_shape_matches_oracle(i):
     for s in seqs:
         err = float(np.abs(got[s] - refm[s]).max())
         assert err <= TOL[c["kv"]] * vm[s], f"rand{i} mq seq {s}: {err} {c}"
+
+
+N_PREFILL = 16
+
+
+def _prefill_config(i):
+    r = np.random.RandomState(9700 + i)
+    hkv = int(r.choice([1, 2, 4, 8]))
+    g = int(r.choice([1, 2, 4, 8, 16]))
+    bs = int(r.choice([16, 32, 64]))
+    kv = str(r.choice(["bf16", "f16", "e4m3"]))
+    q = kv if kv != "e4m3" else str(r.choice(["bf16", "f16"]))
+    b = int(r.randint(1, 5))
+    q_len = int(r.randint(max(17, 16 // g + 1), 301))
+    lens = [int(r.choice([r.randint(1, q_len + 1), r.randint(q_len, 3001), bs * r.randint(1, 40)]))
+            for _ in range(b)]
+    kernel = int(r.choice([0, 3]))
+    return dict(hkv=hkv, g=g, bs=bs, kv=kv, q=q, lens=lens, q_len=q_len, kernel=kernel)
+
+
+@pytest.mark.parametrize("i", range(N_PREFILL))
+def test_random_chunked_prefill_matches_oracle(i):
+    """Chunked prefill (q_len 17-300, more than 16 query rows per KV head, so the
+    automatic route and kernel = 3 both take the tcgen05 kernel) over random head
+    counts, GQA groups up to 16, block sizes, pool and query dtypes and lengths
+    (some shorter than the chunk), against the oracle's causal multi-token
+    attention ("Unlocking long context", section 5.2)."""
+    from paged_kv_cache_215_gb300 import build, pkv
+    build.build()
+    c = _prefill_config(i)
+    case = wl.make_case(f"rand_pf{i}", c["lens"], c["hkv"] * c["g"], c["hkv"], 128, c["bs"],
+                        c["kv"], c["q"], c["q"], seed=9800 + i)
+    tens = wl.make_tensors(case)
+    gc = GpuCase(case, tens)
+    gc.pool.append(case.layer, gc.k_new, gc.v_new, gc.tables, gc.new_pos, gc.k_scale, gc.v_scale)
+    pool, _, seqs = oracle_side(case, tens, None, gc.k_scale, gc.v_scale)
+    g = torch.Generator().manual_seed(9900 + i)
+    q = torch.randn(case.batch, c["q_len"], case.num_q_heads, 128, generator=g).to(
+        wl.TORCH_DT[c["q"]])
+    ref, _ = oracle.decode_mq(np_raw(q), c["q"], pool, c["kv"], case.geometry, case.layer,
+                              case.tables, case.seq_lens, c["q_len"], case.scale, gc.k_scale,
+                              gc.v_scale)
+    out = torch.full((case.batch, c["q_len"], case.num_q_heads, 128), float("nan"), device="cuda")
+    pkv.paged_decode_attention_mq(out, q.cuda(), gc.pool, case.layer, gc.tables, gc.seq_lens,
+                                  gc.max_seq_len, case.scale, gc.k_scale, gc.v_scale,
+                                  opts=pkv.launch_opts(kernel=c["kernel"]))
+    torch.cuda.synchronize()
+    assert gc.status() == 0
+    vm = vmax_per_seq(case, pool, seqs, gc.v_scale)
+    got = out.double().cpu().numpy()
+    assert np.all(np.isfinite(got)), c
+    for s in seqs:
+        err = float(np.abs(got[s] - ref[s]).max())
+        assert err <= TOL[c["kv"]] * vm[s], f"rand_pf{i} seq {s}: {err} {c}"
+
+
+N_CASCADE = 12
+
+
+def _cascade_config(i):
+    r = np.random.RandomState(10100 + i)
+    hkv = int(r.choice([2, 4, 8]))
+    g = int(r.choice([1, 2, 4, 8]))
+    bs = int(r.choice([16, 32, 64]))
+    kv = str(r.choice(["bf16", "f16", "e4m3"]))
+    q = "f16" if kv == "f16" else "bf16"
+    prefix = bs * int(r.randint(1, 2049 // bs + 1))
+    b = int(r.randint(2, 9))
+    # inside the prefix, exactly the prefix, or the prefix and a private suffix
+    lens = [int(r.choice([r.randint(1, prefix + 1), prefix, prefix + r.randint(1, 2001)]))
+            for _ in range(b)]
+    used = int(r.choice([prefix, bs * r.randint(1, prefix // bs + 1)]))
+    route = int(r.choice([0, 3]))
+    return dict(hkv=hkv, g=g, bs=bs, kv=kv, q=q, prefix=prefix, lens=lens, used=used, route=route)
+
+
+@pytest.mark.parametrize("i", range(N_CASCADE))
+def test_random_shared_prefix_matches_oracle(i):
+    """paged_decode_attention_cascade over random shared prefixes (one block to
+    2,048 tokens, all or part of it declared shared), sequences inside, equal to
+    or beyond the prefix, GQA groups 1-8, block sizes and pool dtypes, by the
+    forced prefix pass or the automatic route: each sequence's output against the
+    oracle's attention over its whole table ("Unlocking long context", section 3.1
+    shared blocks)."""
+    from paged_kv_cache_215_gb300 import build, pkv
+    build.build()
+    c = _cascade_config(i)
+    case = wl.make_case(f"rand_casc{i}", c["lens"], c["hkv"] * c["g"], c["hkv"], 128, c["bs"],
+                        c["kv"], c["q"], c["q"], seed=10200 + i,
+                        shared_prefix_tokens=c["prefix"])
+    tens = wl.make_tensors(case)
+    gc = GpuCase(case, tens)
+    pool, ref, seqs = oracle_side(case, tens, None, gc.k_scale, gc.v_scale)
+    gc.pool.append(case.layer, gc.k_new, gc.v_new, gc.tables, gc.new_pos, gc.k_scale, gc.v_scale)
+    table, P, plens = wl.prefix_args(case, c["used"])
+    out = torch.full((case.batch, case.num_q_heads, 128), float("nan"),
+                     dtype=wl.TORCH_DT[c["q"]], device="cuda")
+    pkv.paged_decode_attention_cascade(out, gc.q, gc.pool, case.layer,
+                                       torch.from_numpy(table).cuda(), P,
+                                       torch.from_numpy(plens).cuda(), gc.tables, gc.seq_lens,
+                                       gc.max_seq_len, case.scale, gc.k_scale, gc.v_scale,
+                                       opts=pkv.launch_opts(kernel=c["route"]))
+    torch.cuda.synchronize()
+    assert gc.status() == 0
+    assert_parity(case, out, ref, pool, seqs, gc.v_scale, f"rand_casc{i} {c}", out_dtype=c["q"])
