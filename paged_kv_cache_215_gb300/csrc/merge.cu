@@ -175,6 +175,10 @@ __global__ void __launch_bounds__(kThreads) merge_units_kernel(const DecodeArgs 
 // row, 8 rows per CTA; lane l holds columns 4l .. 4l+3 (+128 ...), every lane
 // reads each partial's lse (a broadcast) and computes its weight.
 constexpr int kRowsPerCta = 8;
+// partial rows the shared-prefix merge's warps load at once (a row there merges
+// the decode's partials and every split of the prefix pass: about 20 on the
+// long shared documents)
+constexpr int kInFlight = 16;
 __global__ void __launch_bounds__(32 * kRowsPerCta) merge_units_warp_kernel(const DecodeArgs a) {
   grid_launch_dependents();
   grid_dependency_wait();
@@ -382,7 +386,7 @@ __global__ void __launch_bounds__(128) merge_units_ext_kernel(const DecodeArgs a
 
 // Many rows (head_dim 128): one warp per row, 8 rows per CTA.  Lane l holds
 // columns 4l .. 4l+3; the partials' weights are computed 32 at a time, one per
-// lane, and broadcast by shuffle while eight partial rows are in flight.
+// lane, and broadcast by shuffle while kInFlight partial rows are in flight.
 __global__ void __launch_bounds__(256) merge_units_ext_warp_kernel(const DecodeArgs a) {
   grid_launch_dependents();
   grid_dependency_wait();
@@ -420,17 +424,17 @@ __global__ void __launch_bounds__(256) merge_units_ext_warp_kernel(const DecodeA
     for (int base = 0; base < total; base += 32) {
       const int cnt = min(32, total - base);
       const float wl = lane < cnt ? exp2f((lse_of(base + lane) - M) * kLog2e) : 0.f;
-      for (int k = 0; k < cnt; k += 8) {
-        float4 v[8];
-        float wt[8];
+      for (int k = 0; k < cnt; k += kInFlight) {
+        float4 v[kInFlight];
+        float wt[kInFlight];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < kInFlight; ++e) {
           wt[e] = __shfl_sync(0xffffffffu, wl, (k + e) & 31);
           v[e] = k + e < cnt ? reinterpret_cast<const float4*>(o_of(base + k + e))[lane]
                              : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < kInFlight; ++e) {
           if (k + e >= cnt) break;
           W += wt[e];
           acc.x = fmaf(wt[e], v[e].x, acc.x);
