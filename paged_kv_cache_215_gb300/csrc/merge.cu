@@ -415,6 +415,13 @@ __global__ void __launch_bounds__(256) merge_units_ext_warp_kernel(const DecodeA
     return p < info.y ? a.part_o + (row0 + (size_t)p * HGR) * a.D
                       : a.ext_o + ((size_t)(p - info.y) * rows + q_row) * a.D;
   };
+  // the first kInFlight partial rows are requested before the lse maximum is
+  // known, so that their loads overlap the lse round trip
+  float4 v[kInFlight];
+#pragma unroll
+  for (int e = 0; e < kInFlight; ++e)
+    v[e] = e < total ? reinterpret_cast<const float4*>(o_of(e))[lane]
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
   float M = -INFINITY;
   for (int p = lane; p < total; p += 32) M = fmaxf(M, lse_of(p));
   M = warp_max(M);
@@ -425,13 +432,13 @@ __global__ void __launch_bounds__(256) merge_units_ext_warp_kernel(const DecodeA
       const int cnt = min(32, total - base);
       const float wl = lane < cnt ? exp2f((lse_of(base + lane) - M) * kLog2e) : 0.f;
       for (int k = 0; k < cnt; k += kInFlight) {
-        float4 v[kInFlight];
         float wt[kInFlight];
 #pragma unroll
         for (int e = 0; e < kInFlight; ++e) {
           wt[e] = __shfl_sync(0xffffffffu, wl, (k + e) & 31);
-          v[e] = k + e < cnt ? reinterpret_cast<const float4*>(o_of(base + k + e))[lane]
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
+          if (base > 0 || k > 0)                     // the first rows are in already
+            v[e] = k + e < cnt ? reinterpret_cast<const float4*>(o_of(base + k + e))[lane]
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int e = 0; e < kInFlight; ++e) {
