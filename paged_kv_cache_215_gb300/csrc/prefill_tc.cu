@@ -35,7 +35,10 @@
 // its P V MMAs (a single thread issues a UMMA about every 70 cycles, short of
 // what these tiles take on the tensor core; issuers in different warps multiply
 // the rate), warp 12 the K/V loads (8 boxes per tile at block size 16, from 8
-// lanes).  mbarriers (all waits bounded) pass the tiles between the roles; a
+// lanes).  One warp's TMA requests stream at about 17 B/clk into an SM, two
+// warps' at the HBM rate: in the shared-prefix pass, where the loads are on the
+// critical path, warp 13 takes every other key tile (in chunked prefill it
+// stays idle: its polling there would cost the softmax warps issue slots).  mbarriers (all waits bounded) pass the tiles between the roles; a
 // stage is refilled once every issuer's MMAs reading it have completed.
 #include "device.cuh"
 #include "launch.h"
@@ -51,7 +54,8 @@ constexpr int kSoftmaxWarps = 4 * kQT;
 constexpr int kWarpS = kSoftmaxWarps;        // S MMAs of query tile t: warp kWarpS + t
 constexpr int kWarpPV = kWarpS + kQT;        // P V MMAs of query tile t: warp kWarpPV + t
 constexpr int kWarpTMA = kWarpPV + kQT;      // K/V loads
-constexpr int kWarpConv = kWarpTMA + 1;      // E4M3 pools: warps converting K/V tiles to f16
+constexpr int kWarpConv = kWarpTMA + 1;      // E4M3 pools: warps converting K/V tiles to f16;
+                                             // 16-bit pools: the second producer
 constexpr int kIssuers = 2 * kQT;            // MMA issuers committing each stage's release
 constexpr uint32_t kHalf = 16384;            // 128 rows x 128 B: one 64-column half of Q
 constexpr uint32_t kKVHalf = kN * 128;       // 64 rows x 128 B
@@ -76,7 +80,11 @@ struct PfCfg {
   static constexpr bool kBf16 = KVT == PKV_BF16;      // else f16 operands (f16 and E4M3 pools)
   static constexpr int kStages = 5;                   // K/V tiles in flight
   static constexpr int kConvWarps = kFp8 ? 3 : 0;
-  static constexpr int kThreads = 32 * (kWarpConv + kConvWarps);
+  // producer warps (16-bit pools: a second one, after warp 12, that the
+  // shared-prefix pass uses; E4M3 tiles are half the bytes and their converters
+  // fill the warp budget)
+  static constexpr int kProducers = kFp8 ? 1 : 2;
+  static constexpr int kThreads = 32 * (kWarpConv + kConvWarps + kProducers - 1);
   static constexpr uint32_t kSmemBytes = kSmemKV + kStages * kStageBytes;
 };
 
@@ -97,6 +105,7 @@ static_assert(PfCfg<PKV_BF16>::kSmemBytes + sizeof(Bars) + kAlignSlack <= 227u *
 static_assert(PfCfg<PKV_FP8_E4M3>::kSmemBytes + sizeof(Bars) + kAlignSlack <= 227u * 1024u, "smem");
 // 16 warps at most: four to a scheduler keeps 128 registers a thread
 static_assert(PfCfg<PKV_FP8_E4M3>::kThreads <= 512, "threads");
+static_assert(PfCfg<PKV_BF16>::kThreads <= 512, "threads");
 
 // Two FP32 lanes in one 64-bit register, for the f32x2 instructions (each lane
 // rounds exactly as the scalar instruction does).
@@ -328,7 +337,10 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
       const uint64_t d_v = kFp8 ? smem_desc_sw128(base, kKVHalf, 1024)
                                 : smem_desc_sw128(base, 1024, 2048);
       bool ok = true;
-      if (warp == kWarpTMA) {
+      if (warp == kWarpTMA || (!kFp8 && warp >= kWarpConv)) {
+        // producer prod of P loads key tiles prod, prod + P, ...
+        const int P = casc ? C::kProducers : 1;
+        const int prod = warp == kWarpTMA ? 0 : warp - kWarpConv + 1;
         const int bpt = kN / a.BS;                             // blocks per key tile
         const int nblk = (n + a.BS - 1) / a.BS;
         const int32_t* trow = a.tables + (size_t)s * a.max_blocks;
@@ -405,17 +417,19 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
               if (last_load[st] >= 0)
                 mbar_wait_bounded(&bars->s8_full[st], (last_load[st] / nst) & 1);
         } else {
-        for (int j = 0; j < T && j < nst; ++j) load_tile(j);
         // key tile k goes into the stage of tile k - nst once every issuer's
-        // MMAs reading that tile have completed
-        for (int k = nst; k < T && ok; ++k) {
-          ok = wait(&bars->kv_empty[(k - nst) % nst], ((k - nst) / nst) & 1);
-          if (!ok) break;
+        // MMAs reading that tile have completed (the issuers release the tiles in
+        // order, whichever producer loaded them)
+        for (int k = prod; prod < P && k < T && ok; k += P) {
+          if (k >= nst) {
+            ok = wait(&bars->kv_empty[(k - nst) % nst], ((k - nst) / nst) & 1);
+            if (!ok) break;
+          }
           load_tile(k);
         }
         // keys past the sequence end in its last tile: zero their V rows once the
         // tile has landed, so that P = 0 never meets an unwritten (possibly NaN) slot
-        if (ok && j_tail >= 0) {
+        if (ok && j_tail >= 0 && j_tail % P == prod) {
           ok = wait(&bars->kv_full[j_tail % nst], (j_tail / nst) & 1);
           if (ok) {
             const int valid = n - (jt0 + j_tail) * kN;
@@ -432,11 +446,17 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
         }
         // every TMA load issued must land before the CTA may exit.  A stage's key
         // tile k is requested only after tile k - nst landed and was read, so
-        // waiting for the phase of the last tile requested into it covers all.
+        // waiting for the phase of the last tile requested into each stage covers
+        // all.  That wait belongs to the producer that requested it: with an odd
+        // ring depth the producers take turns on a stage, and the other one's
+        // earlier tile there is two or more phases back (its parity no longer
+        // tells that phase from the current, incomplete one).
         if (leader)
-          for (int st = 0; st < nst; ++st)
-            if (last_load[st] >= 0)
-              mbar_wait_bounded(&bars->kv_full[st], (last_load[st] / nst) & 1);
+          for (int st = 0; st < nst; ++st) {
+            const int k_last = st < T ? st + (T - 1 - st) / nst * nst : -1;
+            if (k_last >= 0 && k_last % P == prod)
+              mbar_wait_bounded(&bars->kv_full[st], (k_last / nst) & 1);
+          }
         }
       } else if (warp >= kWarpConv) {
         if constexpr (kFp8) {
