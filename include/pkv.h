@@ -384,9 +384,11 @@ PKV_API size_t paged_decode_workspace_bytes_mq(const pkv_geometry* geom, int bat
  *   2. the prefix keys are attended by all batch x num_q_heads query rows at
  *      once on the tcgen05 kernel (128-row query tiles, key range split across
  *      CTAs), each row limited to its own prefix length, giving fp32 partials;
- *   3. each sequence's remaining tokens go through the decode kernel over a
- *      suffix table built in the workspace, and one merge combines all partials
- *      by log-sum-exp ([SEQPAR] incremental softmax).
+ *   3. each sequence's remaining tokens go through the decode kernel, which
+ *      reads its own table from entry d_prefix_lens[s] / block_size on (a
+ *      sequence whose prefix fails the check of step 1 is read from its first
+ *      token), and one merge combines all partials by log-sum-exp ([SEQPAR]
+ *      incremental softmax).
  * d_prefix_table: int32 [prefix_blocks], prefix_len_max <= prefix_blocks *
  * block_size (0: plain decode through the same path).  bf16 / f16 pools with q
  * in the pool's dtype, or E4M3 pools with bf16 / f16 q (k_scale / v_scale as in
@@ -405,13 +407,13 @@ PKV_API size_t paged_decode_workspace_bytes_mq(const pkv_geometry* geom, int bat
  * sequences' own tables, after the same check of step 1.  opts->kernel (opts
  * may be NULL): 0 that automatic choice, 2 always the plain decode, 3 always the
  * prefix pass; other values PKV_EINVAL.  opts->phase splits the call so that a
- * caller can time its parts: 0 everything, 1 steps 1-2 (the suffix tables and
+ * caller can time its parts: 0 everything, 1 steps 1-2 (the prefix check and
  * the prefix pass), 2 step 3 (the suffix decode and the merge; needs a phase-1
  * call with the same arguments and workspace before it on the stream); other
  * values PKV_EINVAL.  The other fields are ignored.
- * Measured on one GB300: 32 sequences sharing 64K tokens (268 MB of K/V), 7x
+ * Measured on one GB300: 32 sequences sharing 64K tokens (268 MB of K/V), 7.6x
  * faster than paged_decode_attention; 64 sequences sharing 4K tokens (17 MB),
- * the prefix pass 2% slower than the plain decode. */
+ * the prefix pass (the automatic choice there) 3% faster than the plain decode. */
 PKV_API int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void* d_q,
                                            pkv_dtype q_dtype, const pkv_pool* pool, int layer,
                                            const int32_t* d_prefix_table, int prefix_blocks,

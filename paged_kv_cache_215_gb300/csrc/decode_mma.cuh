@@ -65,6 +65,14 @@ struct KvTraits<PKV_FP8_E4M3> {
   static constexpr int kRegions = 1;   // 128 one-byte columns fill one line
 };
 
+// First token of sequence s that a shared-prefix launch (kOff, a.len_off set)
+// reads: the end of the sequence's shared prefix, whole blocks; a prefix the
+// check before the launch reported bad reads the sequence from token 0.
+__device__ __forceinline__ int first_token(const DecodeArgs& a, int s, int n) {
+  const int o = __ldg(a.len_off + s);
+  return (o < 0 || o > n || o % a.BS != 0) ? 0 : o;
+}
+
 // Iteration state over the blocks a CTA processes; identical in every warp.
 struct Cursor {
   int s, hg, j, n, nb;     // unit (s, hg), local block j, tokens and blocks of s
@@ -73,6 +81,7 @@ struct Cursor {
   long long remaining;     // blocks left in this CTA's run
 };
 
+template <bool kOff>
 __device__ __forceinline__ int clamp_len(const DecodeArgs& a, int s) {
   int n = __ldg(a.seq_lens + s);
   int cap = a.max_blocks * a.BS;
@@ -80,12 +89,14 @@ __device__ __forceinline__ int clamp_len(const DecodeArgs& a, int s) {
     record_error(a.status, PKV_EBOUNDS);
     n = n < 0 ? 0 : cap;
   }
+  if constexpr (kOff) n -= first_token(a, s, n);
   return n;
 }
 
 __device__ __forceinline__ int blocks_of(int n, int BS) { return (n + BS - 1) / BS; }
 
 // Move to the next block; crosses into the next non-empty unit when needed.
+template <bool kOff>
 __device__ __forceinline__ void cursor_next(Cursor& c, const DecodeArgs& a) {
   ++c.j;
   ++c.gb;
@@ -97,7 +108,7 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const DecodeArgs& a) {
       c.hg = 0;
       do {
         ++c.s;
-        c.n = clamp_len(a, c.s);
+        c.n = clamp_len<kOff>(a, c.s);
         c.nb = blocks_of(c.n, a.BS);
       } while (c.nb == 0);
     }
@@ -785,7 +796,8 @@ __device__ __forceinline__ size_t part_base(const DecodeArgs& a, int w, long lon
   return (size_t)p;
 }
 
-template <int KVT, int BS, int NT, bool kCausal>
+// kOff: a shared-prefix launch, each sequence read from token a.len_off[s] on.
+template <int KVT, int BS, int NT, bool kCausal, bool kOff>
 __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeArgs a) {
   using T = KvTraits<KVT>;
@@ -818,7 +830,7 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
     long long total = 0;
     for (int base = 0; base < a.B; base += 32) {
       const int s = base + lane;
-      int nb = s < a.B ? blocks_of(clamp_len(a, s), BS) : 0;
+      int nb = s < a.B ? blocks_of(clamp_len<kOff>(a, s), BS) : 0;
       total += (long long)__reduce_add_sync(0xffffffffu, (unsigned)nb);
       // units of a sequence with no tokens get no piece: mark them once
       if (blockIdx.x == 0 && __any_sync(0xffffffffu, s < a.B && nb == 0)) {
@@ -839,7 +851,7 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
       bool found = false;
       for (int base = 0; base < a.B && !found; base += 32) {
         const int s = base + lane;
-        const int nbs = s < a.B ? blocks_of(clamp_len(a, s), BS) : 0;
+        const int nbs = s < a.B ? blocks_of(clamp_len<kOff>(a, s), BS) : 0;
         const int nbu = nbs * a.NHG;
         int incl = nbu;
 #pragma unroll
@@ -889,13 +901,13 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
     cur.j = hdr->j;
     cur.gb = hdr->gb0;
     cur.remaining = hdr->gb1 - hdr->gb0;
-    cur.n = cur.remaining > 0 ? clamp_len(a, cur.s) : 0;
+    cur.n = cur.remaining > 0 ? clamp_len<kOff>(a, cur.s) : 0;
     cur.nb = blocks_of(cur.n, BS);
   } else {
     const int u = blockIdx.y;
     cur.s = u / a.NHG;
     cur.hg = u % a.NHG;
-    cur.n = clamp_len(a, cur.s);
+    cur.n = clamp_len<kOff>(a, cur.s);
     cur.nb = blocks_of(cur.n, BS);
     part_p = blockIdx.x;
     const int jb = (int)((long long)part_p * cur.nb / a.S);
@@ -919,7 +931,13 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
         id_unit_s = cur.s;
         id_base = cur.j;
         const int jj = id_base + lane;
-        ids = jj < cur.nb ? __ldg(a.tables + (size_t)cur.s * a.max_blocks + jj) : 0;
+        // shared-prefix decode: the sequence's private blocks, after its prefix
+        // (offset from the length clamp_len clamps, so jo + cur.nb <= max_blocks)
+        int jo = 0;
+        if constexpr (kOff)
+          jo = first_token(a, cur.s, min(max(__ldg(a.seq_lens + cur.s), 0), a.max_blocks * BS)) /
+               BS;
+        ids = jj < cur.nb ? __ldg(a.tables + (size_t)cur.s * a.max_blocks + jo + jj) : 0;
       }
       int blk = __shfl_sync(0xffffffffu, ids, cur.j - id_base);
       const bool blk_ok = blk >= 0 && blk < a.num_blocks;
@@ -998,7 +1016,7 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
         stage = 0;
         ++round;
       }
-      cursor_next(cur, a);
+      cursor_next<kOff>(cur, a);
     }
     // drain: every stage still in flight must land before the CTA may exit
     if (lane == 0) {
@@ -1102,7 +1120,7 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
       }
       cons.finish(a, cur.s, hkv, lane, whole, part_base(a, w, slot, part_p), a.mode == 0);
     }
-    cursor_next(cur, a);
+    cursor_next<kOff>(cur, a);
     if (cur.remaining > 0 && cur.j == 0) {
       hkv = cur.hg * a.HG + w;
       cons.load_q(a, cur.s, cur.n, hkv, lane);
@@ -1114,13 +1132,13 @@ __global__ void __launch_bounds__(32 * (kMaxHG + 1), 1)
   grid_launch_dependents();
 }
 
-template <int KVT, int BS, int NT, bool kCausal>
+template <int KVT, int BS, int NT, bool kCausal, bool kOff = false>
 cudaError_t launch_t(const CUtensorMap* map, const DecodeArgs& a, int gx, int gy,
                      cudaStream_t stream) {
   // the ring needs mma_smem_bytes; a larger request (a.smem_bytes) caps how many
   // CTAs can share an SM
   const size_t smem = std::max(mma_smem_bytes(KVT, BS, a.HG, a.stages), (size_t)a.smem_bytes);
-  auto kern = decode_mma_kernel<KVT, BS, NT, kCausal>;
+  auto kern = decode_mma_kernel<KVT, BS, NT, kCausal, kOff>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};

@@ -55,6 +55,10 @@ struct DecodeArgs {
   const float* ext_o;
   const float* ext_lse;
   int ext_count;
+  // with ext partials: per sequence, the tokens before its private part (the
+  // shared prefix, whole blocks); the decode reads sequence s from token
+  // len_off[s] on (table entry len_off[s] / BS on).  nullptr: from token 0.
+  const int32_t* len_off;
   // Prefill kernel over a shared prefix: query token i is sequence i, it sees keys
   // [0, key_limit[i]) (no causal mask); the key range is cut into S splits
   // (blockIdx.y), each writing fp32 normalised O to out and its lse to out_lse at
@@ -79,16 +83,13 @@ cudaError_t launch_merge_units(const DecodeArgs& a, bool pdl, cudaStream_t strea
 // Cascade merge: the decode's balanced-mode partials of each row plus a.ext_count
 // external partials.
 cudaError_t launch_merge_units_ext(const DecodeArgs& a, cudaStream_t stream);
-// Suffix tables of a shared-prefix decode: suffix_tables[s][j] = tables[s][j + pb_s]
-// with pb_s = prefix_lens[s] / BS, suffix_lens[s] = seq_lens[s] - prefix_lens[s];
-// n_prefix[0] = prefix_len_max.  A prefix that is not the shared table, not a
-// multiple of BS, or longer than the sequence is recorded as PKV_EINVAL.
-// suffix_tables == nullptr: only that check (suffix_lens, n_prefix untouched).
-cudaError_t launch_suffix_tables(const int32_t* tables, int max_blocks, const int32_t* seq_lens,
-                                 const int32_t* prefix_table, int prefix_blocks,
-                                 const int32_t* prefix_lens, int prefix_len_max, int B, int BS,
-                                 int32_t* suffix_tables, int32_t* suffix_lens, int32_t* n_prefix,
-                                 int32_t* status, cudaStream_t stream);
+// Shared-prefix check: each sequence's prefix length is whole blocks, within its
+// length and the shared list, and its table starts with the shared blocks; a
+// mismatch is recorded as PKV_EINVAL.  Lets the next launch be scheduled at once.
+cudaError_t launch_prefix_check(const int32_t* tables, int max_blocks, const int32_t* seq_lens,
+                                const int32_t* prefix_table, int prefix_blocks,
+                                const int32_t* prefix_lens, int prefix_len_max, int B, int BS,
+                                int32_t* status, cudaStream_t stream);
 // Merge of [rows, S, D] partials (the public merge_partials layout).
 cudaError_t launch_merge_rows(void* out, int out_dtype, const float* part_o, const float* part_lse,
                               int rows, int S, int D, bool pdl, cudaStream_t stream);

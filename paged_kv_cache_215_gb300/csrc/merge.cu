@@ -460,12 +460,16 @@ __global__ void __launch_bounds__(256) merge_units_ext_warp_kernel(const DecodeA
   store_from_float(a.out, o + 3, a.out_dtype, acc.w * inv);
 }
 
-// Suffix tables: one thread per (sequence, entry).
-__global__ void suffix_tables_kernel(const int32_t* tables, int max_blocks, const int32_t* seq_lens,
-                                     const int32_t* prefix_table, int prefix_blocks,
-                                     const int32_t* prefix_lens, int prefix_len_max, int B, int BS,
-                                     int32_t* suffix_tables, int32_t* suffix_lens,
-                                     int32_t* n_prefix, int32_t* status) {
+// The shared-prefix check, one thread per (sequence, prefix entry): each
+// sequence's prefix length is whole blocks within its length and the shared
+// list, and its table starts with the shared blocks; a mismatch is reported as
+// PKV_EINVAL (the decode then reads that sequence from its first token).  Nothing
+// launched after it reads what it writes, so the next launch may start at once.
+__global__ void prefix_check_kernel(const int32_t* tables, int max_blocks, const int32_t* seq_lens,
+                                    const int32_t* prefix_table, int prefix_blocks,
+                                    const int32_t* prefix_lens, int prefix_len_max, int B, int BS,
+                                    int32_t* status) {
+  grid_launch_dependents();
   const int s = blockIdx.y;
   if (s >= B) return;
   const int n = seq_lens[s], pl = prefix_lens[s];
@@ -473,19 +477,9 @@ __global__ void suffix_tables_kernel(const int32_t* tables, int max_blocks, cons
                    pl / BS > prefix_blocks || n > max_blocks * BS;
   if (bad && threadIdx.x == 0 && blockIdx.x == 0) record_error(status, PKV_EINVAL);
   const int pb = bad ? 0 : pl / BS;
-  // suffix_tables == nullptr: the check alone, over the prefix entries
-  const int jn = suffix_tables ? max_blocks : pb;
-  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < jn; j += gridDim.x * blockDim.x) {
-    if (j < pb && tables[(size_t)s * max_blocks + j] != prefix_table[j])
+  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < pb; j += gridDim.x * blockDim.x)
+    if (tables[(size_t)s * max_blocks + j] != prefix_table[j])
       record_error(status, PKV_EINVAL);                     // not the shared prefix
-    if (suffix_tables)
-      suffix_tables[(size_t)s * max_blocks + j] =
-          j + pb < max_blocks ? tables[(size_t)s * max_blocks + j + pb] : -1;
-  }
-  if (suffix_tables && blockIdx.x == 0 && threadIdx.x == 0) {
-    suffix_lens[s] = bad ? 0 : n - pl;
-    if (s == 0) n_prefix[0] = prefix_len_max;
-  }
 }
 
 }  // namespace
@@ -513,17 +507,16 @@ cudaError_t launch_merge_units_ext(const DecodeArgs& a, cudaStream_t stream) {
   return e;
 }
 
-cudaError_t launch_suffix_tables(const int32_t* tables, int max_blocks, const int32_t* seq_lens,
-                                 const int32_t* prefix_table, int prefix_blocks,
-                                 const int32_t* prefix_lens, int prefix_len_max, int B, int BS,
-                                 int32_t* suffix_tables, int32_t* suffix_lens, int32_t* n_prefix,
-                                 int32_t* status, cudaStream_t stream) {
+cudaError_t launch_prefix_check(const int32_t* tables, int max_blocks, const int32_t* seq_lens,
+                                const int32_t* prefix_table, int prefix_blocks,
+                                const int32_t* prefix_lens, int prefix_len_max, int B, int BS,
+                                int32_t* status, cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
-  const int span = suffix_tables ? max_blocks : std::min(max_blocks, prefix_blocks);
+  const int span = std::min(max_blocks, prefix_blocks);
   const int gx = std::max(1, (span + 255) / 256);
-  suffix_tables_kernel<<<dim3(gx > 64 ? 64 : gx, B), 256, 0, stream>>>(
+  prefix_check_kernel<<<dim3(gx > 64 ? 64 : gx, B), 256, 0, stream>>>(
       tables, max_blocks, seq_lens, prefix_table, prefix_blocks, prefix_lens, prefix_len_max, B, BS,
-      suffix_tables, suffix_lens, n_prefix, status);
+      status);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) count_launch();
   return e;

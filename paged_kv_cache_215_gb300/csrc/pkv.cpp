@@ -623,9 +623,10 @@ size_t paged_decode_workspace_bytes(const pkv_geometry* g, int batch, int max_se
 
 // Partials computed over a shared prefix, merged into every output row.
 struct ExtPartials {
-  const float* o;      // [count][B * Hq][D]
-  const float* lse;    // [count][B * Hq]
+  const float* o;          // [count][B * Hq][D]
+  const float* lse;        // [count][B * Hq]
   int count;
+  const int32_t* len_off;  // per sequence: the tokens before its private part
 };
 
 // Shared body of paged_decode_attention_ex and paged_decode_step.  With k_new
@@ -826,6 +827,7 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
         a.ext_o = ext->o;
         a.ext_lse = ext->lse;
         a.ext_count = ext->count;
+        a.len_off = ext->len_off;
       }
       if (phase != 2 && launch_decode_mma(map, a, plan.grid, 1, stream) != cudaSuccess)
         return PKV_ECUDA;
@@ -875,11 +877,10 @@ static int decode_common(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_
 }
 
 // ---------------------------------------------------------------- shared-prefix decode
-// Workspace sections: prefix length (one int), suffix lengths [B], suffix tables
-// [B, max_blocks], prefix partials O [S][B*Hq][D] and lse [S][B*Hq], then the
+// Workspace sections: prefix partials O [S][B*Hq][D] and lse [S][B*Hq], then the
 // decode's own workspace.
 struct CascadeWs {
-  size_t n_off, lens_off, tab_off, o_off, lse_off, dec_off, bytes;
+  size_t o_off, lse_off, dec_off, bytes;
   int S;          // key splits of the prefix pass
 };
 static CascadeWs cascade_ws(const pkv_geometry& g, int batch, int max_blocks, int prefix_len_max,
@@ -896,10 +897,8 @@ static CascadeWs cascade_ws(const pkv_geometry& g, int batch, int max_blocks, in
   S = std::max(1, std::min(S, std::min(std::max(ktiles, 1), 64)));
   w.S = S;
   const size_t rows = (size_t)batch * g.num_q_heads;
-  w.n_off = 0;
-  w.lens_off = 256;
-  w.tab_off = w.lens_off + align256((size_t)batch * 4);
-  w.o_off = w.tab_off + align256((size_t)batch * max_blocks * 4);
+  (void)max_blocks;
+  w.o_off = 0;
   w.lse_off = w.o_off + align256((size_t)w.S * rows * g.head_dim * 4);
   w.dec_off = w.lse_off + align256((size_t)w.S * rows * 4);
   w.bytes = w.dec_off + decode_bytes;
@@ -978,20 +977,16 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
                                      saved_us <= cost_us);
   if (ws_bytes < w.bytes) return PKV_ENOMEM;
   char* ws = static_cast<char*>(d_workspace);
-  int32_t* n_prefix = reinterpret_cast<int32_t*>(ws + w.n_off);
-  int32_t* suf_lens = reinterpret_cast<int32_t*>(ws + w.lens_off);
-  int32_t* suf_tab = reinterpret_cast<int32_t*>(ws + w.tab_off);
   float* ext_o = reinterpret_cast<float*>(ws + w.o_off);
   float* ext_lse = reinterpret_cast<float*>(ws + w.lse_off);
 
-  // 1. suffix tables and lengths (and the check that each prefix is the shared
-  //    one; the plain route runs the check alone)
-  if (phase != 2 && launch_suffix_tables(d_block_tables, max_blocks_per_seq, d_seq_lens,
-                           prefix_len_max > 0 ? d_prefix_table : d_block_tables,
-                           prefix_len_max > 0 ? prefix_blocks : 0, d_prefix_lens, prefix_len_max,
-                           batch, g.block_size, plain ? nullptr : suf_tab,
-                           plain ? nullptr : suf_lens, plain ? nullptr : n_prefix, p->d_status,
-                           stream) != cudaSuccess)
+  // 1. the check that each sequence's prefix is the shared one (it lets the
+  //    prefix pass be scheduled at once: nothing after it reads what it writes)
+  if (phase != 2 && launch_prefix_check(d_block_tables, max_blocks_per_seq, d_seq_lens,
+                                        prefix_len_max > 0 ? d_prefix_table : d_block_tables,
+                                        prefix_len_max > 0 ? prefix_blocks : 0, d_prefix_lens,
+                                        prefix_len_max, batch, g.block_size, p->d_status,
+                                        stream) != cudaSuccess)
     return PKV_ECUDA;
   if (plain)
     return phase == 1 ? PKV_OK
@@ -1010,7 +1005,7 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
     t.out_lse = ext_lse;
     t.key_limit = d_prefix_lens;
     t.tables = d_prefix_table;
-    t.seq_lens = n_prefix;
+    t.seq_lens = d_prefix_lens;                   // unread: the length comes with the launch
     t.status = p->d_status;
     t.B = 1;
     t.Hq = g.num_q_heads;
@@ -1028,8 +1023,8 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
     t.q_len = batch;
     t.R = G * batch;
     t.S = w.S;
-    // chained behind the suffix-table kernel: the pass reads only the caller's
-    // inputs (the prefix length comes with the launch)
+    // chained behind the prefix check: the pass reads only the caller's inputs (the
+    // prefix length comes with the launch)
     t.casc_len = prefix_len_max;
     t.pdl = 1;
     // E4M3: per-tensor scales on the softmax scale and the partial O (as the
@@ -1039,18 +1034,21 @@ int paged_decode_attention_cascade(void* d_out, pkv_dtype out_dtype, const void*
     t.block_scales = bscales;
     if (launch_prefill_tc(map, t, stream) != cudaSuccess) return PKV_ECUDA;
   }
-  // 3. the private suffixes, merged with the prefix partials; chained behind the
-  //    prefix pass when this call launched it (the decode takes SMs as the pass's
-  //    CTAs retire and waits for the pass before it writes)
+  // 3. the private suffixes, merged with the prefix partials: the decode reads each
+  //    sequence's own table from the end of its prefix (prefix_lens[s] tokens, whole
+  //    blocks); chained behind the prefix pass when this call launched it (the
+  //    decode takes SMs as the pass's CTAs retire and waits for the pass before it
+  //    writes)
   if (phase == 1) return PKV_OK;
-  const ExtPartials ext{ext_o, ext_lse, prefix_len_max > 0 ? w.S : 0};
+  const ExtPartials ext{ext_o, ext_lse, prefix_len_max > 0 ? w.S : 0,
+                        prefix_len_max > 0 ? d_prefix_lens : nullptr};
   pkv_launch_opts chained{};
   chained.pdl = 1;
   const bool chain = prefix_len_max > 0 && phase == 0;
-  return decode_common(d_out, out_dtype, d_q, q_dtype, 1, nullptr, nullptr, 0, pool, layer, suf_tab,
-                       max_blocks_per_seq, suf_lens, batch, max_seq_len, scale, k_scale, v_scale, 0,
-                       ws + w.dec_off, ws_bytes - w.dec_off, chain ? &chained : nullptr, stream,
-                       &ext);
+  return decode_common(d_out, out_dtype, d_q, q_dtype, 1, nullptr, nullptr, 0, pool, layer,
+                       d_block_tables, max_blocks_per_seq, d_seq_lens, batch, max_seq_len, scale,
+                       k_scale, v_scale, 0, ws + w.dec_off, ws_bytes - w.dec_off,
+                       chain ? &chained : nullptr, stream, &ext);
 }
 
 int paged_decode_attention_ex(void* d_out, pkv_dtype out_dtype, const void* d_q, pkv_dtype q_dtype,

@@ -34,6 +34,9 @@ def _cases():
         # E4M3 pool, per-tensor scales (the prefix pass converts each tile to f16)
         (wl.make_case("casc_fp8", [300, 40, 2000, 777], 32, 8, 128, 16, "e4m3", "bf16", "bf16",
                       seed=92, shared_prefix_tokens=256), [256, 128]),
+        # 16 query heads per KV head (two n-tiles in the decode kernel), block size 32
+        (wl.make_case("casc_g16_bs32", [700, 300, 2000], 128, 8, 128, 32, "bf16", "bf16", "bf16",
+                      seed=93, shared_prefix_tokens=256), [256]),
     ]
 
 

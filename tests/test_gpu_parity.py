@@ -378,3 +378,23 @@ def test_launch_counter_counts_kernels():
     gc.step()
     torch.cuda.synchronize()
     assert pkv.launch_count() - n0 == 3                         # append, attention, merge
+
+
+@pytest.mark.parametrize("kv,bs", [("bf16", 16), ("f16", 32), ("e4m3", 16), ("bf16", 32)])
+def test_decode_sixteen_query_heads_per_kv_head(kv, bs):
+    """Single-token decode with G = 16 (128 query / 8 KV heads, and 16 / 1): the
+    tensor-core kernel holds the 16 query rows of a KV head as two n-tiles
+    (the mhpn.cn long-context article, section 3.2 grouping), against the oracle."""
+    from paged_kv_cache_215_gb300 import pkv
+    for hq, hkv, lens in ((128, 8, [1, 17, 700, 2100]), (16, 1, [33, 1500])):
+        q = "f16" if kv == "f16" else "bf16"
+        case = wl.make_case(f"g16_{kv}_bs{bs}_{hq}", lens, hq, hkv, 128, bs, kv, q, "f32",
+                            seed=150 + bs + hq, spike_frac=0.01)
+        tens = wl.make_tensors(case)
+        gc = GpuCase(case, tens)
+        pool, ref, seqs = oracle_side(case, tens, None, gc.k_scale, gc.v_scale)
+        for splits in (0, 3):
+            out = gc.step(num_splits=splits, opts=pkv.launch_opts(kernel=2))
+            torch.cuda.synchronize()
+            assert gc.status() == 0
+            assert_parity(case, out, ref, pool, seqs, gc.v_scale, f"{case.name} splits {splits}")
