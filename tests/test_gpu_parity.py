@@ -398,3 +398,8 @@ def test_decode_sixteen_query_heads_per_kv_head(kv, bs):
             torch.cuda.synchronize()
             assert gc.status() == 0
             assert_parity(case, out, ref, pool, seqs, gc.v_scale, f"{case.name} splits {splits}")
+        # the decode step with the new token's store fused into the attention launch
+        out = gc.fused_step()
+        torch.cuda.synchronize()
+        assert gc.status() == 0
+        assert_parity(case, out, ref, pool, seqs, gc.v_scale, f"{case.name} fused step")
