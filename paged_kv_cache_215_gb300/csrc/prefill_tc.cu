@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
         const int bpt = kN / a.BS;                             // blocks per key tile
         const int nblk = (n + a.BS - 1) / a.BS;
         const int32_t* trow = a.tables + (size_t)s * a.max_blocks;
-        int last_load[kMaxStages];                             // last key tile requested per stage
+        int last_load[kMaxStages];             // E4M3: last key tile requested per stage
 #pragma unroll
         for (int i = 0; i < kMaxStages; ++i) last_load[i] = -1;
         // block ids of the sequence, 32 at a time: lane i holds entry id_base + i
@@ -352,7 +352,6 @@ __global__ void __launch_bounds__(PfCfg<KVT>::kThreads, 1)
         int ids = 0, id_base = -1;
         auto load_tile = [&](int j) {
           const int st = j % nst;
-          last_load[st] = j;
           const int first = (jt0 + j) * bpt;                    // < nblk for every tile loaded
           if (id_base < 0 || first + bpt > id_base + 32) {
             id_base = first;
