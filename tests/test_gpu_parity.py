@@ -403,3 +403,24 @@ def test_decode_sixteen_query_heads_per_kv_head(kv, bs):
         torch.cuda.synchronize()
         assert gc.status() == 0
         assert_parity(case, out, ref, pool, seqs, gc.v_scale, f"{case.name} fused step")
+
+
+@pytest.mark.parametrize("stages", [2, 3, 5])
+@pytest.mark.parametrize("name", ["llama8b_f16_b3", "fp8_b3_h32-8_d128", "ragged_edges_bf16"])
+def test_decode_parity_ring_depths(name, stages):
+    """An explicit ring depth (opts.stages) on the tensor-core decode kernel: the
+    producer/consumer barrier phases wrap at every depth; a depth the shared
+    memory cannot hold is refused with PKV_EUNSUPPORTED."""
+    from paged_kv_cache_215_gb300 import pkv
+    case = next(c for c in CASES if c.name == name)
+    gc, pool, ref, seqs = _sides(case)
+    opts = pkv.launch_opts(kernel=2, stages=stages)
+    try:
+        out = gc.step(opts=opts)
+    except pkv.PkvError as e:
+        if e.code == pkv.PKV_EUNSUPPORTED:
+            pytest.skip("the ring does not fit at this depth")
+        raise
+    torch.cuda.synchronize()
+    assert gc.status() == 0
+    assert_parity(case, out, ref, pool, seqs, gc.v_scale, f"{case.name} stages {stages}")
