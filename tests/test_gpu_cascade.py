@@ -37,6 +37,10 @@ def _cases():
         # 16 query heads per KV head (two n-tiles in the decode kernel), block size 32
         (wl.make_case("casc_g16_bs32", [700, 300, 2000], 128, 8, 128, 32, "bf16", "bf16", "bf16",
                       seed=93, shared_prefix_tokens=256), [256]),
+        (wl.make_case("casc_g16_bs16", [900, 200, 1700], 128, 8, 128, 16, "bf16", "bf16", "bf16",
+                      seed=94, shared_prefix_tokens=512), [512, 256]),
+        (wl.make_case("casc_g16_fp8_bs16", [900, 200, 1700], 64, 4, 128, 16, "e4m3", "bf16",
+                      "bf16", seed=95, shared_prefix_tokens=512), [512]),
     ]
 
 
